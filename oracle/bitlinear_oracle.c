@@ -1,0 +1,308 @@
+/*
+ * CPU oracle for the BitNet b1.58 BitLinear hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
+ * call this file: only the tests, the smoke check and the benchmark's CPU
+ * baseline leg use it.  It shares no code, header, table or constant
+ * generator with the CUDA library; both sides implement the same written
+ * definitions independently.
+ *
+ * Plain, slow, obviously correct.  Each function cites the passage of the
+ * source pages it follows.  Pages (by title):
+ *   [P1] asi.tokyo, "BitNet B1.58 2B4T" write-up (2025-04-27)
+ *   [P2] cheatsheet.md, "1ビットLarge Language Models時代：マイクロソフトがBitNet b1.58を紹介"
+ *   [P3] lumen-it.ai, BitNet (original 1-bit BitNet) article
+ *
+ * Build: gcc -O2 -std=c11 -fPIC -shared -ffp-contract=off -fopenmp
+ * (no -ffast-math: every float operation below must be one IEEE-754
+ * correctly rounded operation, in the order written).
+ */
+#include <math.h>
+#include <stdint.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------ */
+/* bf16 <-> fp32 (bit level)                                           */
+/* ------------------------------------------------------------------ */
+
+static float bf16_to_f32(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* Round-to-nearest-even fp32 -> bf16 (NaN kept quiet). */
+static uint16_t f32_to_bf16_rne(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu) != 0)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7fffu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+uint16_t bl_oracle_f32_to_bf16(float f) { return f32_to_bf16_rne(f); }
+
+/* ------------------------------------------------------------------ */
+/* Step 1: absmean scale gamma = mean |W|.                             */
+/* [P2] section "BitNet b1.58とは？": weights are scaled by their mean   */
+/* absolute value, then rounded to the nearest integer in {-1,0,+1}.   */
+/* [P1]: the "absmean quantiser" picks the chip for every weight.      */
+/*                                                                      */
+/* The sum S = sum |W| is computed exactly with Shewchuk's adaptive     */
+/* non-overlapping partials (Shewchuk 1997, "Adaptive precision         */
+/* floating-point arithmetic"), the method behind Python's math.fsum,  */
+/* and rounded once to double.  gamma = (float)(S_double / (N*K)).     */
+/* ------------------------------------------------------------------ */
+
+/* Exact sum of |w[i]| rounded once to the nearest double (ties to even). */
+double bl_oracle_sum_abs(const float *w, int64_t n) {
+    int cap = 64, np = 0;
+    double *p = (double *)malloc(sizeof(double) * cap);
+    for (int64_t i = 0; i < n; ++i) {
+        double x = fabs((double)w[i]);
+        int j = 0;
+        for (int k = 0; k < np; ++k) {
+            double y = p[k];
+            if (fabs(x) < fabs(y)) { double t = x; x = y; y = t; }
+            double hi = x + y;
+            double lo = y - (hi - x);      /* exact error of hi (|x|>=|y|) */
+            if (lo != 0.0) p[j++] = lo;
+            x = hi;
+        }
+        if (j >= cap) { cap *= 2; p = (double *)realloc(p, sizeof(double) * cap); }
+        p[j++] = x;
+        np = j;
+    }
+    /* The partials are non-overlapping and increasing in magnitude; their
+     * exact sum is the true sum.  Round it once to double: add from the
+     * top until the first inexact addition, then correct the half-way
+     * case using the sign of the remaining partials. */
+    double hi = 0.0;
+    if (np > 0) {
+        int k = np - 1;
+        hi = p[k];
+        double lo = 0.0;
+        while (k > 0) {
+            double x = hi;
+            double y = p[--k];
+            hi = x + y;
+            double yr = hi - x;
+            lo = y - yr;
+            if (lo != 0.0) break;
+        }
+        if (k > 0 && ((lo < 0.0 && p[k - 1] < 0.0) || (lo > 0.0 && p[k - 1] > 0.0))) {
+            double y = lo * 2.0;
+            double x = hi + y;
+            double yr = x - hi;
+            if (y == yr) hi = x;
+        }
+    }
+    free(p);
+    return hi;
+}
+
+/* gamma = mean|W| over the whole tensor (per-tensor scale). */
+float bl_oracle_gamma(const float *w, int64_t N, int64_t K) {
+    double s = bl_oracle_sum_abs(w, N * K);
+    double m = s / (double)(N * K);
+    return (float)m;
+}
+
+/* ------------------------------------------------------------------ */
+/* Step 2: ternarise.  [P2] "BitNet b1.58とは？": divide by the mean    */
+/* absolute value and round to the nearest integer, constrained to     */
+/* {-1, 0, +1}.  Wq = clip(round(W / (gamma + eps)), -1, 1), computed   */
+/* in fp32 (one rounded add, one rounded divide), round half to even.  */
+/* ------------------------------------------------------------------ */
+void bl_oracle_ternarize(const float *w, int64_t n, float gamma, float eps, int8_t *wq) {
+    float d = gamma + eps;                 /* fp32 add, rounded once */
+    for (int64_t i = 0; i < n; ++i) {
+        float t = w[i] / d;                /* fp32 divide, rounded once */
+        float r = rintf(t);                /* nearest, ties to even */
+        int v = (r > 1.0f) ? 1 : (r < -1.0f) ? -1 : (int)r;
+        wq[i] = (int8_t)v;
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Step 3: pack four ternary weights per byte.  [P1]: the custom kernel */
+/* packs four chips into one byte and unpacks them next to the math     */
+/* units.  Code = Wq + 1 (00 = -1, 01 = 0, 10 = +1, 11 invalid).        */
+/*                                                                      */
+/* Layout (tiles of 16 rows x 128 k, 512 bytes each):                   */
+/*   Np = 16*ceil(N/16), Kp = 128*ceil(K/128), KT = Kp/128              */
+/*   r = n/16, i = n%16, c = k/128, kk = k%128                          */
+/*   g = i%8, u = i/8              (row g+8u of the row group)          */
+/*   t = kk/32, j = kk%32          (lane 4g+t owns k in [32t, 32t+32))  */
+/*   P = j/16, m = (j%16)/4, sb = (j%4)/2, h = j%2                      */
+/*   p = 2m + sb                   (bit pair inside a 16-bit half)      */
+/*   lane = 4g + t, word = 2P + u, bit = 16h + 2p                       */
+/*   byte = 512*(r*KT + c) + 16*lane + 4*word + bit/8, shift = bit%8    */
+/* Positions with n >= N or k >= K hold code 01 (weight 0).             */
+/* ------------------------------------------------------------------ */
+int64_t bl_oracle_packed_bytes(int64_t N, int64_t K) {
+    int64_t Np = (N + 15) / 16 * 16;
+    int64_t Kp = (K + 127) / 128 * 128;
+    return Np * Kp / 4;
+}
+
+static void position(int64_t n, int64_t k, int64_t KT, int64_t *byte, int *shift) {
+    int64_t r = n / 16, c = k / 128;
+    int i = (int)(n % 16), kk = (int)(k % 128);
+    int g = i % 8, u = i / 8;
+    int t = kk / 32, j = kk % 32;
+    int P = j / 16, m = (j % 16) / 4, sb = (j % 4) / 2, h = j % 2;
+    int p = 2 * m + sb;
+    int lane = 4 * g + t, word = 2 * P + u, bit = 16 * h + 2 * p;
+    *byte = 512 * (r * KT + c) + 16 * lane + 4 * word + bit / 8;
+    *shift = bit % 8;
+}
+
+/* Byte offset and bit shift of weight (n, k); exported for the tests. */
+void bl_oracle_position(int64_t n, int64_t k, int64_t K, int64_t *byte, int *shift) {
+    position(n, k, (K + 127) / 128, byte, shift);
+}
+
+void bl_oracle_pack(const int8_t *wq, int64_t N, int64_t K, uint8_t *packed) {
+    int64_t Np = (N + 15) / 16 * 16, Kp = (K + 127) / 128 * 128, KT = Kp / 128;
+    memset(packed, 0, (size_t)(Np * Kp / 4));
+    for (int64_t n = 0; n < Np; ++n)
+        for (int64_t k = 0; k < Kp; ++k) {
+            int code = (n < N && k < K) ? wq[n * K + k] + 1 : 1;
+            int64_t byte; int shift;
+            position(n, k, KT, &byte, &shift);
+            packed[byte] |= (uint8_t)(code << shift);
+        }
+}
+
+/* Inverse of bl_oracle_pack.  Returns the number of invalid codes (11)
+ * plus the number of padding positions that do not hold code 01. */
+int64_t bl_oracle_unpack(const uint8_t *packed, int64_t N, int64_t K, int8_t *wq) {
+    int64_t Np = (N + 15) / 16 * 16, Kp = (K + 127) / 128 * 128, KT = Kp / 128;
+    int64_t bad = 0;
+    for (int64_t n = 0; n < Np; ++n)
+        for (int64_t k = 0; k < Kp; ++k) {
+            int64_t byte; int shift;
+            position(n, k, KT, &byte, &shift);
+            int code = (packed[byte] >> shift) & 3;
+            if (code == 3) { ++bad; continue; }
+            if (n < N && k < K) wq[n * K + k] = (int8_t)(code - 1);
+            else if (code != 1) ++bad;
+        }
+    return bad;
+}
+
+/* ------------------------------------------------------------------ */
+/* Step 4: RMSNorm + per-token absmax int8.                             */
+/* [P2] "BitNet b1.58とは？": activations are scaled per token into      */
+/* [-Qb, Qb] (8 bit); the LLaMA parts include RMSNorm.  [P3]: absmax    */
+/* quantisation of activations.  [P1]: 8-bit activations.              */
+/*                                                                      */
+/* Per token m, with v_k = x_k * g_k (fp32 product, exact for bf16):    */
+/*   mx = max_k |v_k|  (clamped below at 1e-5)                          */
+/*   c  = 127 / mx                    (fp32 divide)                     */
+/*   q_k = clamp(rint(v_k * c), -128, 127)   (fp32 multiply)            */
+/*   r  = 1 / sqrt(sum_k v_k^2 / K + eps)    (fp64)                     */
+/*   s_tok = (float)(r * mx / 127)                                      */
+/* RMSNorm's factor r > 0 cancels inside absmax, so q is computed from  */
+/* v directly; s_tok carries r so that q * s_tok approximates the       */
+/* normalised activation x * r * g.                                     */
+/* ------------------------------------------------------------------ */
+void bl_oracle_quant_act(const uint16_t *x, const uint16_t *gain, int64_t M, int64_t K,
+                         float eps, int8_t *q, float *s_tok) {
+    #pragma omp parallel for schedule(static)
+    for (int64_t mi = 0; mi < M; ++mi) {
+        const uint16_t *xr = x + mi * K;
+        float mx = 0.0f;
+        double ss = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            float v = bf16_to_f32(xr[k]);
+            if (gain) v = v * bf16_to_f32(gain[k]);
+            float a = fabsf(v);
+            if (a > mx) mx = a;
+            ss += (double)v * (double)v;
+        }
+        if (!(mx >= 1e-5f)) mx = 1e-5f;
+        float c = 127.0f / mx;
+        for (int64_t k = 0; k < K; ++k) {
+            float v = bf16_to_f32(xr[k]);
+            if (gain) v = v * bf16_to_f32(gain[k]);
+            float y = v * c;
+            float r = rintf(y);
+            if (r > 127.0f) r = 127.0f;
+            if (r < -128.0f) r = -128.0f;
+            q[mi * K + k] = (int8_t)(int)r;
+        }
+        double rr = 1.0 / sqrt(ss / (double)K + (double)eps);
+        s_tok[mi] = (float)(rr * (double)mx / 127.0);
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Step 5: acc[m,n] = sum_k q[m,k] * Wq[n,k], exact.  [P1]: unpacked    */
+/* weights are multiplied with the 8-bit blocks; [P2]: the matmul is    */
+/* mostly additions.  Accumulated in int64; returns nonzero if a result */
+/* does not fit int32.                                                  */
+/* ------------------------------------------------------------------ */
+int bl_oracle_matmul(const int8_t *q, const int8_t *wq, int64_t M, int64_t N, int64_t K,
+                     int32_t *acc) {
+    int overflow = 0;
+    #pragma omp parallel for schedule(static) reduction(|:overflow)
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t mi = 0; mi < M; ++mi) {
+            int64_t s = 0;
+            for (int64_t k = 0; k < K; ++k) s += (int64_t)q[mi * K + k] * (int64_t)wq[n * K + k];
+            if (s > INT32_MAX || s < INT32_MIN) overflow = 1;
+            acc[mi * N + n] = (int32_t)s;
+        }
+    return overflow;
+}
+
+/* Same contraction for a list of (m, n) pairs only (for large shapes). */
+void bl_oracle_matmul_pairs(const int8_t *q, const int8_t *wq, int64_t K, const int64_t *ms,
+                            const int64_t *ns, int64_t cnt, int32_t *acc) {
+    for (int64_t i = 0; i < cnt; ++i) {
+        int64_t s = 0;
+        for (int64_t k = 0; k < K; ++k) s += (int64_t)q[ms[i] * K + k] * (int64_t)wq[ns[i] * K + k];
+        acc[i] = (int32_t)s;
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Step 6: rescale.  The integer result is dequantised by the weight    */
+/* scale gamma and the token scale s_tok:                               */
+/*   f = gamma * s_tok[m]           (fp32 multiply)                     */
+/*   out = bf16_rne((float)acc * f) (fp32 multiply, then RNE to bf16)   */
+/* ------------------------------------------------------------------ */
+void bl_oracle_epilogue(const int32_t *acc, const float *s_tok, float gamma, int64_t M,
+                        int64_t N, uint16_t *out) {
+    for (int64_t mi = 0; mi < M; ++mi) {
+        float f = gamma * s_tok[mi];
+        for (int64_t n = 0; n < N; ++n) {
+            float y = (float)acc[mi * N + n] * f;
+            out[mi * N + n] = f32_to_bf16_rne(y);
+        }
+    }
+}
+
+/* Number of OpenMP threads the parallel loops above use. */
+int bl_oracle_threads(void) {
+    int t = 1;
+    #pragma omp parallel
+    {
+        #pragma omp single
+        {
+#ifdef _OPENMP
+            t = omp_get_num_threads();
+#endif
+        }
+    }
+    return t;
+}

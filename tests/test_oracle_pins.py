@@ -1,0 +1,331 @@
+"""Pins for the CPU oracle against facts the pages and mathematics fix.
+
+None of these compares the oracle with itself or with a retyped copy of its
+own formula: each check uses a hand-computed value, a closed form, an
+invariant, an independent library routine (math.fsum, numpy, torch's bf16
+cast) or brute force with exact rationals.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bitlinear_02_b300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def bf16(a) -> np.ndarray:
+    """float array -> bf16 bit patterns via torch's RNE cast (library routine)."""
+    t = torch.as_tensor(np.asarray(a, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------- gamma ---
+
+def test_sum_abs_hand_example():
+    # |0.5| + |-1.5| + |0| + |2| = 4 exactly; mean over 4 elements = 1.
+    w = np.array([[0.5, -1.5], [0.0, 2.0]], np.float32)
+    assert oracle.sum_abs(w) == 4.0
+    assert oracle.gamma(w) == np.float32(1.0)
+
+
+def test_sum_abs_matches_fsum_and_exact_rationals():
+    rng = np.random.default_rng(11)
+    for trial in range(20):
+        n = int(rng.integers(1, 3000))
+        # wide dynamic range, including subnormal fp32 and huge values
+        w = (rng.standard_normal(n) * np.exp2(rng.integers(-140, 120, n))).astype(np.float32)
+        got = oracle.sum_abs(w)
+        assert got == math.fsum(abs(float(v)) for v in w)
+        if n < 400:
+            exact = sum(Fraction(abs(float(v))) for v in w)
+            assert got == float(exact)  # Fraction -> float rounds correctly
+
+
+def test_sum_abs_where_naive_sum_fails():
+    # 2^60 followed by many ones: a double running sum drops every 1.
+    w = np.array([2.0 ** 60] + [1.0] * 4096, np.float32)
+    assert oracle.sum_abs(w) == 2.0 ** 60 + 4096.0
+    # Half-way case across partials: 2^53 + 1 + 2^-40 rounds up, not to even.
+    w2 = np.array([2.0 ** 53, 1.0, 2.0 ** -40], np.float32)
+    assert oracle.sum_abs(w2) == 2.0 ** 53 + 2.0
+
+
+def test_gamma_constant_matrix():
+    for c in (0.02, 1.0, 3.5e-3):
+        w = np.full((7, 9), c, np.float32)
+        assert oracle.gamma(w) == np.float32(c)
+
+
+def test_gamma_gaussian_closed_form():
+    # W ~ N(0, s^2): E|W| = s * sqrt(2/pi).  With 2^20 samples the relative
+    # standard error is ~7e-4; 0.5% is about 7 sigma.
+    s = 0.02
+    w = inputs.weights_fp32(1024, 1024, seed=123).numpy()
+    g = float(oracle.gamma(w))
+    assert abs(g / (s * math.sqrt(2 / math.pi)) - 1) < 5e-3
+    # Fraction of zeros after ternarisation: P(|z| <= 0.5 (gamma+eps)/s).
+    wq = oracle.ternarize(w, g, 1e-5)
+    z = 0.5 * (g + 1e-5) / s
+    p0 = math.erf(z / math.sqrt(2))
+    assert abs(float((wq == 0).mean()) - p0) < 5e-3
+    assert abs(p0 - 0.310) < 0.01  # about a third, as the workload recipe says
+
+
+# ------------------------------------------------------------ ternarise ---
+
+def test_ternarize_rounding_table():
+    # gamma = 1, eps = 0: t = W itself.  Round to nearest, ties to even, clip.
+    w = np.array([0.49, 0.5, 0.51, -0.5, -0.51, 1.5, -1.5, 2.5, -7.0, 0.0, -0.0, 1e-30, 0.9, -1.0],
+                 np.float32)
+    want = np.array([0, 0, 1, 0, -1, 1, -1, 1, -1, 0, 0, 0, 1, -1], np.int8)
+    np.testing.assert_array_equal(oracle.ternarize(w, 1.0, 0.0), want)
+
+
+def test_ternarize_values_and_eps():
+    # Every output lies in {-1, 0, +1} (the pages' ternary set, log2(3) bits).
+    w = inputs.weights_fp32(64, 300, seed=5).numpy() * 50
+    g = oracle.gamma(w)
+    wq = oracle.ternarize(w, g, 1e-5)
+    assert set(np.unique(wq).tolist()) <= {-1, 0, 1}
+    # constant positive matrix c: c / (c + eps) rounds to 1 for c >> eps
+    c = np.full((3, 5), 0.7, np.float32)
+    assert (oracle.ternarize(c, oracle.gamma(c), 1e-5) == 1).all()
+    # c == eps gives exactly 1/2, a tie, which rounds to even (0)
+    e = np.full((2, 2), 1e-5, np.float32)
+    assert (oracle.ternarize(e, np.float32(1e-5), np.float32(1e-5)) == 0).all()
+
+
+# ----------------------------------------------------------------- pack ---
+
+def test_packed_bytes_four_per_byte():
+    for N, K in [(16, 128), (512, 256), (2560, 6912), (17, 130), (1, 1)]:
+        Np = -(-N // 16) * 16
+        Kp = -(-K // 128) * 128
+        assert oracle.packed_bytes(N, K) == Np * Kp // 4
+
+
+def test_pack_positions_golden():
+    n_lines = 0
+    with open(os.path.join(GOLDEN, "pack_positions.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].split()
+            if not line:
+                continue
+            n, k, K, b, s = map(int, line)
+            assert oracle.position(n, k, K) == (b, s), (n, k, K)
+            # and through pack itself: a single +1 in a zero matrix
+            N = max(16, (n // 16 + 1) * 16)
+            wq = np.zeros((N, K), np.int8)
+            wq[n, k] = 1
+            p = oracle.pack(wq)
+            base = np.full_like(p, 0x55)  # every code 01 (weight 0)
+            diff = np.nonzero(p != base)[0]
+            assert diff.tolist() == [b]
+            assert (int(p[b]) >> s) & 3 == 2  # code of +1 is 10
+            n_lines += 1
+    assert n_lines >= 10
+
+
+def test_pack_round_trip_all_patterns_every_byte():
+    # every one of the 3^4 = 81 ternary patterns at every byte of a tile:
+    # byte b of pass j holds pattern (b + j) % 81, four codes Wq+1 at bits 2i
+    pats = np.array([[(p // 3 ** i) % 3 - 1 for i in range(4)] for p in range(81)], np.int8)
+    where = {}
+    for n in range(16):
+        for k in range(128):
+            where[(n, k)] = oracle.position(n, k, 128)
+    for j in range(81):
+        wq = np.zeros((16, 128), np.int8)
+        for (n, k), (b, s) in where.items():
+            wq[n, k] = pats[(b + j) % 81][s // 2]
+        want = np.array([sum((int(v) + 1) << (2 * i) for i, v in enumerate(pats[(b + j) % 81]))
+                         for b in range(512)], np.uint8)
+        p = oracle.pack(wq)
+        np.testing.assert_array_equal(p, want)
+        back, bad = oracle.unpack(p, 16, 128)
+        assert bad == 0
+        np.testing.assert_array_equal(back, wq)
+
+
+def test_pack_round_trip_ragged_and_padding():
+    rng = np.random.default_rng(3)
+    for N, K in [(1, 16), (17, 144), (33, 8640 // 10), (512, 256), (100, 1000)]:
+        wq = rng.integers(-1, 2, (N, K)).astype(np.int8)
+        p = oracle.pack(wq)
+        back, bad = oracle.unpack(p, N, K)
+        assert bad == 0, (N, K)
+        np.testing.assert_array_equal(back, wq)
+        # corrupting a padding position or writing code 11 is detected
+        if N % 16 or K % 128:
+            q = p.copy()
+            q[-1] = 0xFF
+            assert oracle.unpack(q, N, K)[1] > 0
+
+
+def test_pack_tile_locality():
+    # all weights of row-group r and k-tile c live in bytes [512*(r*KT+c), +512),
+    # and the 16 bytes of lane 4g+t hold only rows g and g+8, k in [32t, 32t+32)
+    K = 256
+    KT = 2
+    for n in range(0, 48, 5):
+        for k in range(0, K, 7):
+            b, s = oracle.position(n, k, K)
+            r, c = n // 16, k // 128
+            assert 512 * (r * KT + c) <= b < 512 * (r * KT + c + 1)
+            lane = (b % 512) // 16
+            assert lane // 4 == (n % 16) % 8
+            assert lane % 4 == (k % 128) // 32
+            word = (b % 16) // 4
+            assert word % 2 == (n % 16) // 8  # even words row g, odd words row g+8
+
+
+# ---------------------------------------------------------- activations ---
+
+def test_quant_identity_on_integer_tokens():
+    # integers in [-127, 127] with max |x| = 127: scale 127/127 = 1, q == x
+    rng = np.random.default_rng(0)
+    x = rng.integers(-127, 128, (5, 64)).astype(np.float32)
+    x[:, 3] = 127.0
+    q, s = oracle.quant_act(bf16(x), None, 1e-5)
+    np.testing.assert_array_equal(q, x.astype(np.int8))
+
+
+def test_quant_power_of_two_invariance_and_bounds():
+    x = inputs.activations_bf16(6, 320, seed=1).float().numpy()
+    q0, s0 = oracle.quant_act(bf16(x), None, 1e-12)
+    for j in (-6, -1, 3, 9):
+        q1, s1 = oracle.quant_act(bf16(x * 2.0 ** j), None, 1e-12)
+        np.testing.assert_array_equal(q1, q0)
+        np.testing.assert_allclose(s1, s0, rtol=1e-6)
+    assert np.abs(q0.astype(int)).max() <= 127
+    assert (np.abs(q0.astype(int)).max(axis=1) == 127).all()  # every non-zero token hits 127
+
+
+def test_quant_zero_token_and_scale_longhand():
+    x = inputs.activations_bf16(4, 256, seed=2).float().numpy()
+    x[2] = 0.0
+    eps = 1e-5
+    q, s = oracle.quant_act(bf16(x), None, eps)
+    assert (q[2] == 0).all() and np.isfinite(s[2])
+    xb = bf16_to_f64(bf16(x))
+    for m in (0, 1, 3):
+        rms = math.sqrt(float(np.mean(xb[m] ** 2)) + eps)   # numpy's pairwise mean
+        want = (1.0 / rms) * np.abs(xb[m]).max() / 127.0
+        assert abs(s[m] / want - 1) < 1e-6
+
+
+def test_quant_approximates_rmsnorm_within_half_step():
+    # q * s_tok reproduces RMSNorm(x) * g to within half a quantisation step
+    x = inputs.activations_bf16(8, 512, seed=4, outlier_frac=0.01).float().numpy()
+    gvec = inputs.gain_bf16(512, seed=9).float().numpy()
+    eps = 1e-5
+    q, s = oracle.quant_act(bf16(x), bf16(gvec), eps)
+    xb, gb = bf16_to_f64(bf16(x)), bf16_to_f64(bf16(gvec))
+    for m in range(8):
+        v = xb[m] * gb
+        y = v / math.sqrt(float(np.mean(xb[m] ** 2 * gb ** 2)) + eps)  # RMSNorm with gain
+        err = np.abs(q[m].astype(np.float64) * float(s[m]) - y)
+        assert err.max() <= 0.5 * float(s[m]) * (1 + 1e-5)
+
+
+# --------------------------------------------------------------- matmul ---
+
+def test_matmul_vs_numpy_int64():
+    rng = np.random.default_rng(5)
+    for M, N, K in [(1, 7, 16), (3, 33, 130), (9, 64, 512)]:
+        q = rng.integers(-127, 128, (M, K)).astype(np.int8)
+        wq = rng.integers(-1, 2, (N, K)).astype(np.int8)
+        want = q.astype(np.int64) @ wq.astype(np.int64).T
+        np.testing.assert_array_equal(oracle.matmul(q, wq), want)
+        ms = rng.integers(0, M, 11)
+        ns = rng.integers(0, N, 11)
+        np.testing.assert_array_equal(oracle.matmul_pairs(q, wq, ms, ns), want[ms, ns])
+
+
+def test_matmul_exhaustive_k4():
+    pats = np.array([[(p // 3 ** i) % 3 - 1 for i in range(4)] for p in range(81)], np.int8)
+    grid = np.array([[a, b, c, d] for a in (-127, -1, 0, 5) for b in (-128, 3, 127)
+                     for c in (0, 64) for d in (-9, 100)], np.int8)
+    acc = oracle.matmul(grid, pats)
+    for i, qv in enumerate(grid):
+        for j, wv in enumerate(pats):
+            assert acc[i, j] == sum(int(a) * int(b) for a, b in zip(qv, wv))
+
+
+def test_matmul_extreme_magnitude_fits_int32():
+    K = 28672  # largest K of the workloads
+    q = np.full((1, K), -128, np.int8)
+    wq = np.full((2, K), -1, np.int8)
+    wq[1] = 1
+    acc = oracle.matmul(q, wq)
+    assert acc[0, 0] == 128 * K and acc[0, 1] == -128 * K
+
+
+# ------------------------------------------------------------- epilogue ---
+
+def test_bf16_rounding_matches_torch():
+    rng = np.random.default_rng(6)
+    f = (rng.standard_normal(5000) * np.exp2(rng.integers(-30, 30, 5000))).astype(np.float32)
+    want = bf16(f)
+    got = np.array([oracle.f32_to_bf16(v) for v in f], np.uint16)
+    np.testing.assert_array_equal(got, want)
+
+
+def test_epilogue_powers_of_two_and_error_bound():
+    acc = np.array([[1 << 10, -(1 << 3), 0, 1]], np.int32)
+    out = oracle.epilogue(acc, np.array([2.0 ** -7], np.float32), 2.0 ** -4)
+    np.testing.assert_array_equal(bf16_to_f64(out)[0], [2.0 ** -1, -(2.0 ** -8), 0.0, 2.0 ** -11])
+    rng = np.random.default_rng(7)
+    acc = rng.integers(-3_000_000, 3_000_000, (4, 300)).astype(np.int32)
+    s = rng.uniform(1e-4, 1e-1, 4).astype(np.float32)
+    g = np.float32(0.0173)
+    out = bf16_to_f64(oracle.epilogue(acc, s, g))
+    exact = acc.astype(np.float64) * (float(g) * s.astype(np.float64))[:, None]
+    nz = exact != 0
+    rel = np.abs(out[nz] - exact[nz]) / np.abs(exact[nz])
+    # bf16 keeps 8 significant bits: unit roundoff 2^-8, plus two fp32 roundings
+    assert rel.max() <= 2.0 ** -8 + 3 * 2.0 ** -24
+
+
+# ---------------------------------------------------------- end to end ---
+
+def test_pipeline_is_dequantised_product_and_tracks_float_matmul():
+    # tiny shapes: the oracle's output equals gamma*s*acc, which is the product
+    # of the dequantised operands; and it approximates RMSNorm(x) @ (gamma*Wq)^T
+    # within the activation quantisation error bound.
+    M, N, K = 3, 8, 16
+    w = inputs.weights_fp32(N, K, seed=21).numpy()
+    x = inputs.activations_bf16(M, K, seed=22)
+    xb = inputs.bf16_bits(x)
+    g, packed, q, s, acc, out = oracle.forward(xb, w, 1e-5, 1e-5)
+    wq, bad = oracle.unpack(packed, N, K)
+    assert bad == 0
+    deq = (q.astype(np.float64) * s[:, None]) @ (wq.astype(np.float64) * float(g)).T
+    np.testing.assert_allclose(deq, float(g) * s[:, None].astype(np.float64) * acc, rtol=1e-12)
+    xf = bf16_to_f64(xb)
+    y = xf / np.sqrt(np.mean(xf ** 2, axis=1, keepdims=True) + 1e-5)
+    ref = y @ (wq.astype(np.float64) * float(g)).T
+    bound = 0.5 * s[:, None] * float(g) * np.abs(wq).sum(axis=1)[None, :] + 1e-6
+    res = bf16_to_f64(out)
+    assert (np.abs(res - ref) <= bound + np.abs(ref) * 2.0 ** -8).all()
+
+
+def test_layer_small_workload_invariants():
+    wl = inputs.WORKLOADS["layer_small"]
+    _, N, K = wl["shapes"][0]
+    w = inputs.weights_fp32(N, K, seed=wl["seed"]).numpy()
+    x = inputs.bf16_bits(inputs.activations_bf16(1, K, seed=wl["seed"] + 1))
+    g, packed, q, s, acc, out = oracle.forward(x, w, wl["eps_w"], wl["eps_a"])
+    assert packed.size == N * K // 4
+    assert np.abs(acc).max() <= 127 * K
+    assert 0.015 < float(g) < 0.017
