@@ -1,0 +1,195 @@
+"""BitNet b1.58 BitLinear on one B300: thin Python binding of ``libbitlinear.so``.
+
+The functions named ``bitlinear_*`` mirror the C ABI in ``include/bitlinear.h``
+one to one: they only turn torch tensors into device pointers, pass the
+current CUDA stream and raise on a non-zero status.  Every step of the path
+runs in the library's CUDA kernels; there is no CPU fallback.  If the
+library is missing (not built) every call raises ``RuntimeError``.
+
+Convenience wrappers (``pack_weights``, ``quant_act``, ``forward``,
+``bitlinear``) allocate the outputs with torch and call the same entry points.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "BitLinearError", "library_path", "load_library",
+    "bitlinear_packed_bytes", "bitlinear_pack_weights", "bitlinear_pack_ternary",
+    "bitlinear_quant_act", "bitlinear_forward", "bitlinear_check_status",
+    "bitlinear_set_wait_limit", "bitlinear_status_string", "bitlinear_version",
+    "pack_weights", "pack_ternary", "quant_act", "forward", "bitlinear",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "libbitlinear.so"
+
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_UNSUPPORTED = 2
+ERR_CUDA = 3
+ERR_TIMEOUT = 4
+
+
+class BitLinearError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {bitlinear_status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, _LIB_NAME)
+
+
+_lib = None
+
+
+def load_library():
+    """Load the in-tree CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it with `python bitlinear_02_b300/build.py` "
+            "(or __graft_entry__.build()); there is no CPU fallback")
+    L = ctypes.CDLL(path)
+    P, I64, F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float
+    L.bitlinear_status_string.argtypes = [ctypes.c_int]
+    L.bitlinear_status_string.restype = ctypes.c_char_p
+    L.bitlinear_version.restype = ctypes.c_int
+    L.bitlinear_packed_bytes.argtypes = [I64, I64]
+    L.bitlinear_packed_bytes.restype = ctypes.c_size_t
+    L.bitlinear_pack_weights.argtypes = [P, I64, I64, F, P, P, P]
+    L.bitlinear_pack_ternary.argtypes = [P, I64, I64, P, P]
+    L.bitlinear_quant_act.argtypes = [P, P, I64, I64, F, P, P, P]
+    L.bitlinear_forward.argtypes = [P, P, P, P, I64, I64, I64, P, P, P]
+    L.bitlinear_check_status.argtypes = [P]
+    L.bitlinear_set_wait_limit.argtypes = [ctypes.c_uint32]
+    L.bitlinear_set_wait_limit.restype = None
+    for name in ("bitlinear_pack_weights", "bitlinear_pack_ternary", "bitlinear_quant_act",
+                 "bitlinear_forward", "bitlinear_check_status"):
+        getattr(L, name).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return ctypes.c_void_p(t)
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        raise BitLinearError(status, what)
+
+
+# ---------------------------------------------------------------- C names ---
+
+def bitlinear_status_string(status: int) -> str:
+    return load_library().bitlinear_status_string(int(status)).decode()
+
+
+def bitlinear_version() -> int:
+    return int(load_library().bitlinear_version())
+
+
+def bitlinear_packed_bytes(N: int, K: int) -> int:
+    return int(load_library().bitlinear_packed_bytes(int(N), int(K)))
+
+
+def bitlinear_pack_weights(W, N: int, K: int, eps: float, packed, gamma, stream=None) -> None:
+    _check(load_library().bitlinear_pack_weights(_ptr(W), int(N), int(K), float(eps), _ptr(packed),
+                                                 _ptr(gamma), _stream(stream)),
+           "bitlinear_pack_weights")
+
+
+def bitlinear_pack_ternary(Wq, N: int, K: int, packed, stream=None) -> None:
+    _check(load_library().bitlinear_pack_ternary(_ptr(Wq), int(N), int(K), _ptr(packed),
+                                                 _stream(stream)),
+           "bitlinear_pack_ternary")
+
+
+def bitlinear_quant_act(x, gain, M: int, K: int, eps: float, q, tok_scale, stream=None) -> None:
+    _check(load_library().bitlinear_quant_act(_ptr(x), _ptr(gain), int(M), int(K), float(eps),
+                                              _ptr(q), _ptr(tok_scale), _stream(stream)),
+           "bitlinear_quant_act")
+
+
+def bitlinear_forward(q, tok_scale, packed, gamma, M: int, N: int, K: int, out, acc_out=None,
+                      stream=None) -> None:
+    _check(load_library().bitlinear_forward(_ptr(q), _ptr(tok_scale), _ptr(packed), _ptr(gamma),
+                                            int(M), int(N), int(K), _ptr(out), _ptr(acc_out),
+                                            _stream(stream)),
+           "bitlinear_forward")
+
+
+def bitlinear_check_status(stream=None) -> int:
+    """Returns the status code (OK or ERR_TIMEOUT); does not raise."""
+    return int(load_library().bitlinear_check_status(_stream(stream)))
+
+
+def bitlinear_set_wait_limit(iterations: int) -> None:
+    load_library().bitlinear_set_wait_limit(int(iterations))
+
+
+# ------------------------------------------------------------ convenience ---
+
+def pack_weights(W: torch.Tensor, eps: float = 1e-5):
+    """fp32 [N, K] CUDA tensor -> (packed uint8 tensor, gamma float32 [1] tensor)."""
+    N, K = W.shape
+    packed = torch.empty(bitlinear_packed_bytes(N, K), dtype=torch.uint8, device=W.device)
+    gamma = torch.empty(1, dtype=torch.float32, device=W.device)
+    bitlinear_pack_weights(W, N, K, eps, packed, gamma)
+    return packed, gamma
+
+
+def pack_ternary(Wq: torch.Tensor) -> torch.Tensor:
+    N, K = Wq.shape
+    packed = torch.empty(bitlinear_packed_bytes(N, K), dtype=torch.uint8, device=Wq.device)
+    bitlinear_pack_ternary(Wq, N, K, packed)
+    return packed
+
+
+def quant_act(x: torch.Tensor, gain: torch.Tensor | None = None, eps: float = 1e-5):
+    """bf16 [M, K] -> (q int8 [M, K], tok_scale float32 [M])."""
+    M, K = x.shape
+    q = torch.empty(M, K, dtype=torch.int8, device=x.device)
+    s = torch.empty(M, dtype=torch.float32, device=x.device)
+    bitlinear_quant_act(x, gain, M, K, eps, q, s)
+    return q, s
+
+
+def forward(q: torch.Tensor, tok_scale: torch.Tensor, packed: torch.Tensor, gamma: torch.Tensor,
+            N: int, out: torch.Tensor | None = None, acc_out: torch.Tensor | None = None):
+    M, K = q.shape
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=q.device)
+    bitlinear_forward(q, tok_scale, packed, gamma, M, N, K, out, acc_out)
+    return out
+
+
+def bitlinear(x: torch.Tensor, packed: torch.Tensor, gamma: torch.Tensor, N: int,
+              gain: torch.Tensor | None = None, eps: float = 1e-5) -> torch.Tensor:
+    """One BitLinear layer: RMSNorm + int8 quantisation, then the ternary matmul."""
+    q, s = quant_act(x, gain, eps)
+    return forward(q, s, packed, gamma, N)

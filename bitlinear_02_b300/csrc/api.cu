@@ -1,0 +1,83 @@
+// Entry points of the BitLinear matmul: argument checks, engine choice,
+// status reporting.  The kernels live in pack.cu, quant.cu, gemv.cu and
+// gemm.cu.
+#include <atomic>
+
+#include "bl_device.cuh"
+
+namespace bl {
+cudaError_t launch_gemv(const int8_t *q, const float *tok_scale, const uint8_t *packed,
+                        const float *gamma, int M, int N, int K, __nv_bfloat16 *out,
+                        int32_t *acc_out, cudaStream_t st, int num_sms);
+cudaError_t launch_gemm(const int8_t *q, const float *tok_scale, const uint8_t *packed,
+                        const float *gamma, int M, int N, int K, __nv_bfloat16 *out,
+                        int32_t *acc_out, cudaStream_t st, uint32_t wait_limit);
+cudaError_t gemm_status(unsigned int *out, cudaStream_t st);
+
+namespace {
+constexpr uint32_t kDefaultWaitLimit = 1u << 22;
+std::atomic<uint32_t> g_wait_limit{kDefaultWaitLimit};
+int g_sms[64] = {0};
+
+int num_sms() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!g_sms[dev]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+        g_sms[dev] = v;
+    }
+    return g_sms[dev];
+}
+}  // namespace
+}  // namespace bl
+
+extern "C" const char *bitlinear_status_string(int status) {
+    switch (status) {
+        case BITLINEAR_OK: return "ok";
+        case BITLINEAR_ERR_INVALID_ARG: return "invalid argument";
+        case BITLINEAR_ERR_UNSUPPORTED: return "unsupported device or shape";
+        case BITLINEAR_ERR_CUDA: return "CUDA runtime error";
+        case BITLINEAR_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
+        default: return "unknown status";
+    }
+}
+
+extern "C" int bitlinear_version(void) { return 100; }
+
+extern "C" void bitlinear_set_wait_limit(uint32_t iterations) {
+    bl::g_wait_limit.store(iterations ? iterations : bl::kDefaultWaitLimit);
+}
+
+extern "C" bitlinear_status_t bitlinear_forward(const int8_t *q, const float *tok_scale,
+                                                const uint8_t *packed, const float *gamma,
+                                                int64_t M, int64_t N, int64_t K, void *out_bf16,
+                                                int32_t *acc_out, void *stream) {
+    using namespace bl;
+    if (M < 0 || N < 1 || K < 16 || (K % 16) != 0 || K > 65536 || N > (1ll << 30) ||
+        M > (1ll << 30))
+        return BITLINEAR_ERR_INVALID_ARG;
+    if (M == 0) return BITLINEAR_OK;
+    if (!q || !tok_scale || !packed || !gamma || !out_bf16) return BITLINEAR_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned4(tok_scale) || !aligned16(packed) || !aligned4(gamma) ||
+        !aligned16(out_bf16) || (acc_out && !aligned16(acc_out)))
+        return BITLINEAR_ERR_INVALID_ARG;
+    if ((N + 15) / 16 > 65535 * 4 && M <= 16) return BITLINEAR_ERR_UNSUPPORTED;
+    if ((M + 63) / 64 > 65535) return BITLINEAR_ERR_UNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    auto *out = static_cast<__nv_bfloat16 *>(out_bf16);
+    cudaError_t e;
+    if (M <= 16)
+        e = launch_gemv(q, tok_scale, packed, gamma, static_cast<int>(M), static_cast<int>(N),
+                        static_cast<int>(K), out, acc_out, st, num_sms());
+    else
+        e = launch_gemm(q, tok_scale, packed, gamma, static_cast<int>(M), static_cast<int>(N),
+                        static_cast<int>(K), out, acc_out, st, g_wait_limit.load());
+    return e == cudaSuccess ? BITLINEAR_OK : BITLINEAR_ERR_CUDA;
+}
+
+extern "C" bitlinear_status_t bitlinear_check_status(void *stream) {
+    unsigned int v = 0;
+    if (bl::gemm_status(&v, static_cast<cudaStream_t>(stream)) != cudaSuccess) return BITLINEAR_ERR_CUDA;
+    return v ? BITLINEAR_ERR_TIMEOUT : BITLINEAR_OK;
+}

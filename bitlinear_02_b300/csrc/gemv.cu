@@ -1,0 +1,260 @@
+// Decode engine (M <= 16 tokens): HBM-bound stream of packed ternary weights.
+//
+// asi.tokyo 2B4T write-up: the weights travel packed four per byte and are
+// unpacked right next to the math units, then multiplied with 8-bit
+// activations.  Here every 16-byte lane chunk of the packed layout is
+// loaded once (128-bit, streaming), unpacked in registers and fed to the
+// legacy tensor-core MMA (m16n8k16, f16 inputs, fp32 accumulate) - on B300
+// its f16 rate is four times its int8 rate and far above dp4a.
+//
+// Unpacking costs one AND per two weights: a 2-bit code c = Wq + 1 kept in
+// place at bit pair p of each 16-bit half reads, as an f16, c * 2^(E(p)-24)
+// (a subnormal or the smallest normals; E = 0,2,4,6,8,10 for p = 0..5, and
+// pairs 6,7 are shifted down by 8 bits to E = 4,6).  The matching
+// activation operand is q * 2^-E(p), exact in f16, so every product is
+// c*q*2^-24 and the fp32 sums are exact multiples of 2^-24 below 1.  The
+// accumulator times 2^24 is the integer sum of c*q; subtracting sum(q)
+// (from dp4a) gives sum((c-1)*q) = sum(Wq*q) exactly.
+//
+// Work split: a CTA of 4 warps owns 64 output rows (4 row groups) and a
+// range of 128-k tiles; warp w takes every 4th tile of that range and all
+// 4 row groups, reusing each activation fragment 4 times.  A thread-block
+// cluster of S CTAs splits K; partial int32 sums are combined through
+// distributed shared memory, and each CTA of the cluster finishes a slice
+// of the outputs.  Weight loads for the first tiles are issued before the
+// programmatic-dependent-launch wait, so they overlap the previous kernel.
+#include "bl_device.cuh"
+
+namespace bl {
+
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kGroups = 4;  // 16-row groups per CTA
+constexpr int kRows = 16 * kGroups;
+
+// f16x2 constants: 2^-E(p) and -1152 * 2^-E(p) in both halves.
+__device__ __forceinline__ uint32_t scale_c(int p) {
+    constexpr uint32_t s[8] = {0x3C003C00u, 0x34003400u, 0x2C002C00u, 0x24002400u,
+                               0x1C001C00u, 0x14001400u, 0x2C002C00u, 0x24002400u};
+    return s[p];
+}
+__device__ __forceinline__ uint32_t offset_c(int p) {
+    constexpr uint32_t o[8] = {0xE480E480u, 0xDC80DC80u, 0xD480D480u, 0xCC80CC80u,
+                               0xC480C480u, 0xBC80BC80u, 0xD480D480u, 0xCC80CC80u};
+    return o[p];
+}
+// A operand register for bit pair p of a packed word (see header comment).
+__device__ __forceinline__ uint32_t code_reg(uint32_t w, int p) {
+    if (p < 6) return w & (0x00030003u << (2 * p));
+    return (w >> 8) & (0x00030003u << (2 * (p - 4)));
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <int NT>
+struct Stage {
+    uint4 w[kGroups];  // one 16-byte chunk per row group
+    uint4 q[NT][2];    // 32 activation bytes per 8-token tile
+};
+
+template <int NT>
+__global__ void __launch_bounds__(kWarps * 32, 3)
+    gemv_kernel(const int8_t *__restrict__ q, const float *__restrict__ tok_scale,
+                const uint8_t *__restrict__ packed, const float *__restrict__ gamma, int M, int N,
+                int K, int KT, int RGN, int tiles_per_cta, __nv_bfloat16 *__restrict__ out,
+                int32_t *__restrict__ acc_out) {
+    __shared__ int32_t part[kWarps][NT * 8][kRows];
+    __shared__ int32_t total[NT * 8 * kRows];
+
+    pdl_launch_dependents();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int rb = blockIdx.y;
+    const int S = gridDim.x, s = blockIdx.x;
+    const int c_begin = s * tiles_per_cta;
+    const int c_end = min(KT, c_begin + tiles_per_cta);
+
+    auto load_w = [&](Stage<NT> &st, int c) {
+        if (c >= c_end) return;
+#pragma unroll
+        for (int i = 0; i < kGroups; ++i) {
+            const int rg = rb * kGroups + i;
+            if (rg < RGN)
+                st.w[i] = ld_stream16(packed + (static_cast<int64_t>(rg) * KT + c) * 512 + lane * 16);
+            else
+                st.w[i] = make_uint4(0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u);
+        }
+    };
+    auto load_q = [&](Stage<NT> &st, int c) {
+        if (c >= c_end) return;
+        const int k0 = c * 128 + t * 32;
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            const int tok = 8 * j + g;
+            const int8_t *src = q + static_cast<int64_t>(tok) * K + k0;
+            st.q[j][0] = (tok < M && k0 < K) ? ld_ro16(src) : make_uint4(0, 0, 0, 0);
+            st.q[j][1] = (tok < M && k0 + 16 < K) ? ld_ro16(src + 16) : make_uint4(0, 0, 0, 0);
+        }
+    };
+
+    float d[kGroups][NT][4];
+#pragma unroll
+    for (int i = 0; i < kGroups; ++i)
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) d[i][j][e] = 0.0f;
+    int corr[NT];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) corr[j] = 0;
+
+    auto compute = [&](const Stage<NT> &st) {
+        uint32_t b[8][NT][2];
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            const uint32_t qw[8] = {st.q[j][0].x, st.q[j][0].y, st.q[j][0].z, st.q[j][0].w,
+                                    st.q[j][1].x, st.q[j][1].y, st.q[j][1].z, st.q[j][1].w};
+#pragma unroll
+            for (int mu = 0; mu < 8; ++mu) {
+                const int m = mu & 3;
+                const uint32_t x = qw[mu] ^ 0x80808080u;  // q + 128 per byte
+                const uint32_t lo = prmt(x, 0x64646464u, 0x4140u);  // f16 (1024 + u0, 1024 + u1)
+                const uint32_t hi = prmt(x, 0x64646464u, 0x4342u);
+                b[mu][j][0] = hfma2(lo, scale_c(2 * m), offset_c(2 * m));
+                b[mu][j][1] = hfma2(hi, scale_c(2 * m + 1), offset_c(2 * m + 1));
+                corr[j] = __dp4a(static_cast<int>(qw[mu]), 0x01010101, corr[j]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kGroups; ++i) {
+            const uint32_t wr[4] = {st.w[i].x, st.w[i].y, st.w[i].z, st.w[i].w};
+#pragma unroll
+            for (int P = 0; P < 2; ++P) {
+                const uint32_t X = wr[2 * P], Y = wr[2 * P + 1];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int mu = 4 * P + m;
+                    const uint32_t a0 = code_reg(X, 2 * m), a1 = code_reg(Y, 2 * m);
+                    const uint32_t a2 = code_reg(X, 2 * m + 1), a3 = code_reg(Y, 2 * m + 1);
+#pragma unroll
+                    for (int j = 0; j < NT; ++j)
+                        mma16816(d[i][j], a0, a1, a2, a3, b[mu][j][0], b[mu][j][1]);
+                }
+            }
+        }
+    };
+
+    // Two-deep software pipeline over this warp's tiles c, c+4, c+8, ...
+    Stage<NT> A, B;
+    int c = c_begin + warp;
+    load_w(A, c);
+    load_w(B, c + kWarps);
+    pdl_wait();  // activations, scales and gamma come from earlier kernels
+    load_q(A, c);
+    load_q(B, c + kWarps);
+    for (; c < c_end; c += 2 * kWarps) {
+        compute(A);
+        load_w(A, c + 2 * kWarps);
+        load_q(A, c + 2 * kWarps);
+        if (c + kWarps < c_end) {
+            compute(B);
+            load_w(B, c + 3 * kWarps);
+            load_q(B, c + 3 * kWarps);
+        }
+    }
+
+    // sum(q) over this warp's k for token 8j+g (reduce over the 4 t lanes),
+    // then fetch the sums of this thread's output tokens 8j+2t and 8j+2t+1.
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        corr[j] += __shfl_xor_sync(0xffffffffu, corr[j], 1);
+        corr[j] += __shfl_xor_sync(0xffffffffu, corr[j], 2);
+    }
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        const int ce = __shfl_sync(0xffffffffu, corr[j], 4 * (2 * t));
+        const int co = __shfl_sync(0xffffffffu, corr[j], 4 * (2 * t + 1));
+        const int t0 = 8 * j + 2 * t;
+#pragma unroll
+        for (int i = 0; i < kGroups; ++i) {
+            const int r0 = 16 * i + g;
+            part[warp][t0][r0] = __float2int_rn(d[i][j][0] * 16777216.0f) - ce;
+            part[warp][t0 + 1][r0] = __float2int_rn(d[i][j][1] * 16777216.0f) - co;
+            part[warp][t0][r0 + 8] = __float2int_rn(d[i][j][2] * 16777216.0f) - ce;
+            part[warp][t0 + 1][r0 + 8] = __float2int_rn(d[i][j][3] * 16777216.0f) - co;
+        }
+    }
+    __syncthreads();
+    constexpr int E = NT * 8 * kRows;
+    for (int e = threadIdx.x; e < E; e += kWarps * 32) {
+        const int tk = e / kRows, rr = e % kRows;
+        int v = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) v += part[w][tk][rr];
+        total[e] = v;
+    }
+
+    // Combine the cluster's partial sums; CTA s finishes entries [e0, e1).
+    int e0 = 0, e1 = E;
+    if (S > 1) {
+        cluster_sync();
+        const int per = (E + S - 1) / S;
+        e0 = s * per;
+        e1 = min(E, e0 + per);
+    } else {
+        __syncthreads();
+    }
+    const float gam = *gamma;
+    for (int e = e0 + threadIdx.x; e < e1; e += kWarps * 32) {
+        int v;
+        if (S > 1) {
+            v = 0;
+            const uint32_t la = smem_addr(&total[e]);
+            for (int r = 0; r < S; ++r) v += ld_cluster_s32(cluster_map(la, r));
+        } else {
+            v = total[e];
+        }
+        const int tk = e / kRows, rr = e % kRows;
+        const int n = rb * kRows + rr;
+        if (tk < M && n < N) {
+            const float f = __fmul_rn(gam, tok_scale[tk]);
+            out[static_cast<int64_t>(tk) * N + n] = __float2bfloat16_rn(__fmul_rn(static_cast<float>(v), f));
+            if (acc_out) acc_out[static_cast<int64_t>(tk) * N + n] = v;
+        }
+    }
+    if (S > 1) cluster_sync();  // keep this CTA's shared memory alive for its peers
+}
+
+}  // namespace
+
+// Host launcher (called by bitlinear_forward for M <= 16).
+cudaError_t launch_gemv(const int8_t *q, const float *tok_scale, const uint8_t *packed,
+                        const float *gamma, int M, int N, int K, __nv_bfloat16 *out,
+                        int32_t *acc_out, cudaStream_t st, int num_sms) {
+    const int KT = (K + 127) / 128;
+    const int RGN = (N + 15) / 16;
+    const int RB = (RGN + kGroups - 1) / kGroups;
+    int S = (2 * num_sms + RB - 1) / RB;
+    const int smax = KT / kWarps > 1 ? KT / kWarps : 1;
+    if (S > smax) S = smax;
+    if (S > 8) S = 8;
+    if (S < 1) S = 1;
+    int tpc = (KT + S - 1) / S;
+    S = (KT + tpc - 1) / tpc;
+    const dim3 grid(S, RB), block(kWarps * 32);
+    if (M <= 8)
+        return launch_pdl(gemv_kernel<1>, grid, block, 0, st, S, q, tok_scale, packed, gamma, M, N, K,
+                          KT, RGN, tpc, out, acc_out);
+    return launch_pdl(gemv_kernel<2>, grid, block, 0, st, S, q, tok_scale, packed, gamma, M, N, K, KT,
+                      RGN, tpc, out, acc_out);
+}
+
+}  // namespace bl

@@ -1,0 +1,153 @@
+// Fused RMSNorm + per-token absmax int8 quantisation of activations.
+//
+// BitNet b1.58 (cheatsheet.md, "BitNet b1.58とは？"): activations are scaled
+// per token into the 8-bit range; the LLaMA-style parts include RMSNorm.
+// lumen-it.ai: absmax quantisation of activations.
+//
+// Per token (v_k = x_k * gain_k in fp32, exact for bf16 inputs):
+//   mx = max(max |v_k|, 1e-5f);  c = 127 / mx  (fp32);  q_k = rint(v_k * c)
+//   tok_scale = (float)(1/sqrt(sum v_k^2 / K + eps) * mx / 127)   (double)
+// RMSNorm's positive factor cancels inside absmax, so q is decided by fp32
+// products of the raw inputs only: it is the same on every device and in
+// any reduction order.  The sum of squares is accumulated per thread as an
+// unevaluated pair of floats (two-sum plus the exact product residual),
+// then combined across threads in double.
+#include "bl_device.cuh"
+
+namespace bl {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 &v, float (&f)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+template <bool kGain>
+__global__ void __launch_bounds__(kThreads)
+    quant_act_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ gain, int64_t M,
+                     int64_t K, float eps, int8_t *__restrict__ q, float *__restrict__ tok_scale,
+                     int wpt) {
+    pdl_launch_dependents();
+    __shared__ float s_mx[kThreads / 32];
+    __shared__ double s_ss[kThreads / 32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tpc = (kThreads / 32) / wpt;               // tokens per CTA
+    const int64_t m = static_cast<int64_t>(blockIdx.x) * tpc + warp / wpt;
+    const int sub = warp % wpt;
+    const int nthr = wpt * 32, tid = sub * 32 + lane;
+    const int64_t chunks = K / 8;                        // 8 bf16 per 16-byte chunk
+    const bool active = m < M;
+    pdl_wait();
+
+    float mx = 0.0f, hi = 0.0f, lo = 0.0f;
+    if (active) {
+        const uint4 *xr = x + m * chunks;
+#pragma unroll 4
+        for (int64_t i = tid; i < chunks; i += nthr) {
+            float v[8];
+            bf16x8_to_f32(xr[i], v);
+            if (kGain) {
+                float gv[8];
+                bf16x8_to_f32(gain[i], gv);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], gv[j]);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                mx = fmaxf(mx, fabsf(v[j]));
+                const float p = __fmul_rn(v[j], v[j]);
+                const float e = __fmaf_rn(v[j], v[j], -p);   // exact residual of the product
+                const float s = __fadd_rn(hi, p);
+                const float bp = __fsub_rn(s, hi);
+                const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(p, bp));
+                hi = s;
+                lo = __fadd_rn(lo, __fadd_rn(err, e));
+            }
+        }
+    }
+    double ss = static_cast<double>(hi) + static_cast<double>(lo);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    }
+    if (lane == 0) {
+        s_mx[warp] = mx;
+        s_ss[warp] = ss;
+    }
+    __syncthreads();
+    if (wpt > 1) {
+        const int base = (warp / wpt) * wpt;
+        mx = 0.0f;
+        ss = 0.0;
+        for (int w = 0; w < wpt; ++w) {
+            mx = fmaxf(mx, s_mx[base + w]);
+            ss += s_ss[base + w];
+        }
+    }
+    if (!active) return;
+    if (!(mx >= 1e-5f)) mx = 1e-5f;
+    const float c = __fdiv_rn(127.0f, mx);
+    const uint4 *xr = x + m * chunks;
+    uint2 *qr = reinterpret_cast<uint2 *>(q + m * K);
+#pragma unroll 4
+    for (int64_t i = tid; i < chunks; i += nthr) {
+        float v[8];
+        bf16x8_to_f32(xr[i], v);
+        if (kGain) {
+            float gv[8];
+            bf16x8_to_f32(gain[i], gv);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], gv[j]);
+        }
+        uint32_t b[2] = {0u, 0u};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            int iv = __float2int_rn(__fmul_rn(v[j], c));
+            iv = iv > 127 ? 127 : (iv < -128 ? -128 : iv);
+            b[j >> 2] |= (static_cast<uint32_t>(iv) & 0xffu) << (8 * (j & 3));
+        }
+        qr[i] = make_uint2(b[0], b[1]);
+    }
+    if (tid == 0) {
+        const double r = 1.0 / sqrt(ss / static_cast<double>(K) + static_cast<double>(eps));
+        tok_scale[m] = static_cast<float>(r * static_cast<double>(mx) / 127.0);
+    }
+}
+
+}  // namespace
+}  // namespace bl
+
+extern "C" bitlinear_status_t bitlinear_quant_act(const void *x_bf16, const void *gain_bf16,
+                                                  int64_t M, int64_t K, float eps, int8_t *q,
+                                                  float *tok_scale, void *stream) {
+    using namespace bl;
+    if (M < 0 || K < 16 || (K % 16) != 0 || K > (1ll << 30)) return BITLINEAR_ERR_INVALID_ARG;
+    if (M == 0) return BITLINEAR_OK;
+    if (!x_bf16 || !q || !tok_scale) return BITLINEAR_ERR_INVALID_ARG;
+    if (!aligned16(x_bf16) || !aligned16(q) || !aligned4(tok_scale) ||
+        (gain_bf16 && !aligned16(gain_bf16)))
+        return BITLINEAR_ERR_INVALID_ARG;
+    // Few tokens: spread each token over more warps to cut latency.
+    int wpt = M <= 16 ? 8 : (M <= 64 ? 4 : (M <= 512 ? 2 : 1));
+    const int tpc = (kThreads / 32) / wpt;
+    const int64_t blocks = (M + tpc - 1) / tpc;
+    if (blocks > 0x7fffffffll) return BITLINEAR_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (gain_bf16)
+        e = launch_pdl(quant_act_kernel<true>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0,
+                       st, 1, static_cast<const uint4 *>(x_bf16),
+                       static_cast<const uint4 *>(gain_bf16), M, K, eps, q, tok_scale, wpt);
+    else
+        e = launch_pdl(quant_act_kernel<false>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0,
+                       st, 1, static_cast<const uint4 *>(x_bf16),
+                       static_cast<const uint4 *>(nullptr), M, K, eps, q, tok_scale, wpt);
+    return e == cudaSuccess ? BITLINEAR_OK : BITLINEAR_ERR_CUDA;
+}

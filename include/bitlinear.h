@@ -1,0 +1,193 @@
+/*
+ * bitlinear.h - C ABI of the B300 (sm_103a) BitNet b1.58 BitLinear library.
+ *
+ * The BitLinear layer of BitNet b1.58 (cheatsheet.md, "BitNet b1.58とは？")
+ * replaces a linear layer: weights are ternary {-1, 0, +1}, obtained by
+ * scaling with their mean absolute value and rounding; activations are
+ * 8-bit, scaled per token.  The asi.tokyo 2B4T write-up describes a GPU
+ * kernel that packs four ternary weights per byte and unpacks them next to
+ * the math units before multiplying with 8-bit activations.  This library
+ * is that path, written for one B300:
+ *
+ *   bitlinear_pack_weights   fp32 W -> gamma = mean|W| (exact) + packed 2-bit codes
+ *   bitlinear_pack_ternary   int8 Wq in {-1,0,1} -> packed 2-bit codes
+ *   bitlinear_quant_act      bf16 x -> RMSNorm + per-token absmax int8 q, token scale
+ *   bitlinear_forward        q x packed W -> exact int32 -> rescaled bf16 out
+ *
+ * Conventions shared by every entry point
+ *   - Pointers marked "device" are CUDA device pointers owned by the caller;
+ *     the library never frees or retains them past the call's stream work.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  All calls are asynchronous with respect to the host: they
+ *     enqueue kernels and return.  No call synchronises the device.
+ *   - Arguments are validated on the host before anything is enqueued; an
+ *     invalid argument returns BITLINEAR_ERR_INVALID_ARG and enqueues nothing.
+ *   - A failed kernel launch returns BITLINEAR_ERR_CUDA.
+ *   - No exception crosses this boundary and nothing is printed.
+ *   - Matrices are row-major.  W is [N out, K in] (K contiguous); x, q are
+ *     [M tokens, K]; out, acc are [M, N].
+ *   - K must be a multiple of 16 (so every row starts on a 16-byte
+ *     boundary); N >= 1, M >= 0 (M = 0 is a no-op).  Device pointers must be
+ *     16-byte aligned, except the scalar/vector ones noted (4-byte).
+ *
+ * Packed weight layout (shared by both matmul engines).  Np = 16*ceil(N/16),
+ * Kp = 128*ceil(K/128).  The buffer is Np*Kp/4 bytes of 2-bit codes
+ * (code = Wq + 1: 00 = -1, 01 = 0, 10 = +1; 11 never written).  It is made
+ * of 512-byte tiles, one per (row group r = n/16, k block c = k/128), tile
+ * index r*(Kp/128) + c.  Inside a tile, with i = n%16, kk = k%128:
+ *   g = i%8, u = i/8, t = kk/32, j = kk%32,
+ *   P = j/16, m = (j%16)/4, sb = (j%4)/2, h = j%2, p = 2m + sb,
+ *   byte = 16*(4g + t) + 4*(2P + u) + (16h + 2p)/8,  shift = (16h + 2p)%8.
+ * So the 16 bytes at 16*(4g+t) hold rows g and g+8 of the group over
+ * k in [32t, 32t+32), one 32-bit word per (row, 16-k half).  Padding
+ * positions (n >= N or k >= K) hold code 01.  The byte format is stable: a
+ * caller may save and reload packed buffers.
+ */
+#ifndef BITLINEAR_H_
+#define BITLINEAR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define BITLINEAR_API __attribute__((visibility("default")))
+#else
+#define BITLINEAR_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    BITLINEAR_OK = 0,
+    BITLINEAR_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment or stream */
+    BITLINEAR_ERR_UNSUPPORTED = 2, /* no sm_103a device / shape beyond limits */
+    BITLINEAR_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+    BITLINEAR_ERR_TIMEOUT = 4      /* a kernel gave up a bounded wait */
+} bitlinear_status_t;
+
+/* Static, NUL-terminated description of a status code (never NULL). */
+BITLINEAR_API const char *bitlinear_status_string(int status);
+
+/* Library ABI version (major*100 + minor). */
+BITLINEAR_API int bitlinear_version(void);
+
+/* Bytes of the packed buffer for an [N, K] weight matrix:
+ * 16*ceil(N/16) * 128*ceil(K/128) / 4.  Returns 0 if N < 1 or K < 1. */
+BITLINEAR_API size_t bitlinear_packed_bytes(int64_t N, int64_t K);
+
+/*
+ * Absmean ternarisation and packing of fp32 master weights
+ * (cheatsheet.md "BitNet b1.58とは？": weights scaled by their mean
+ * absolute value, rounded to the nearest integer in {-1,0,+1};
+ * asi.tokyo: four weights per byte).
+ *
+ *   gamma = (float)( round_to_double( sum_{n,k} |W[n,k]| ) / (N*K) )
+ *           where the sum is exact (order independent) and rounded once;
+ *   Wq    = clamp(rint_half_even( W / (gamma + eps) ), -1, 1)
+ *           with fp32 add and fp32 divide, each correctly rounded.
+ *
+ *   W        device, fp32 [N, K] row-major, 16-byte aligned, finite values
+ *            (non-finite values give an unspecified gamma and codes, and no
+ *            fault).
+ *   eps      added to gamma before dividing (1e-5 in the workloads).
+ *   packed   device, bitlinear_packed_bytes(N, K) bytes, 16-byte aligned;
+ *            fully overwritten (padding included).
+ *   gamma    device, one float, 4-byte aligned; written by the device.
+ *   stream   see conventions.
+ * Uses a small per-device workspace (256 64-bit counters) that the library
+ * allocates on the first call on each device and keeps until process exit;
+ * that first call is therefore not capturable in a CUDA graph.  Calls on
+ * different streams of the same device must not overlap in time.
+ * Errors: INVALID_ARG (null/misaligned pointer, N < 1, K < 1, K % 16 != 0),
+ * CUDA (workspace allocation or launch failure).
+ */
+BITLINEAR_API bitlinear_status_t bitlinear_pack_weights(const float *W, int64_t N, int64_t K, float eps,
+                                          uint8_t *packed, float *gamma, void *stream);
+
+/*
+ * Packing of weights that are already ternary (the scale gamma is kept by
+ * the caller).  Wq: device int8 [N, K] with values in {-1, 0, +1}
+ * (other values are clamped to that range).  packed as above.
+ * Errors: INVALID_ARG (null/misaligned pointer, N < 1, K < 1, K % 16 != 0).
+ */
+BITLINEAR_API bitlinear_status_t bitlinear_pack_ternary(const int8_t *Wq, int64_t N, int64_t K,
+                                          uint8_t *packed, void *stream);
+
+/*
+ * Fused RMSNorm + per-token absmax int8 quantisation of activations
+ * (cheatsheet.md "BitNet b1.58とは？": activations scaled per token to
+ * 8 bits; RMSNorm from the LLaMA parts; lumen-it.ai: absmax quantisation).
+ * For each token m, with v_k = x[m,k] * gain[k] (fp32; gain = 1 if NULL):
+ *   mx   = max(max_k |v_k|, 1e-5f)
+ *   c    = 127.0f / mx                              (fp32 divide)
+ *   q_k  = clamp(rint_half_even(v_k * c), -128, 127) (fp32 multiply)
+ *   r    = 1 / sqrt(sum_k v_k^2 / K + eps)          (double)
+ *   tok_scale[m] = (float)(r * mx / 127)
+ * RMSNorm's factor r > 0 cancels inside absmax, so q depends only on v;
+ * q * tok_scale approximates RMSNorm(x) * gain to half a quantisation step.
+ *
+ *   x_bf16     device, bf16 [M, K], 16-byte aligned.
+ *   gain_bf16  device, bf16 [K] or NULL, 16-byte aligned.
+ *   q          device, int8 [M, K], 16-byte aligned.
+ *   tok_scale  device, fp32 [M], 4-byte aligned.
+ * q is bit-exact (no float reduction decides it); tok_scale is computed
+ * with compensated sums and matches the double-precision definition to
+ * about 1e-7 relative.
+ * Errors: INVALID_ARG (null/misaligned pointer, M < 0, K < 16, K % 16 != 0).
+ */
+BITLINEAR_API bitlinear_status_t bitlinear_quant_act(const void *x_bf16, const void *gain_bf16, int64_t M,
+                                       int64_t K, float eps, int8_t *q, float *tok_scale,
+                                       void *stream);
+
+/*
+ * The BitLinear matmul (asi.tokyo: packed weights are unpacked next to
+ * the math units and multiplied with 8-bit blocks; cheatsheet.md: the
+ * matmul reduces to additions):
+ *   acc[m,n] = sum_k q[m,k] * Wq[n,k]                  (exact int32)
+ *   out[m,n] = bf16_rne( (float)acc[m,n] * (gamma * tok_scale[m]) )
+ *              (gamma * tok_scale[m] is one fp32 multiply, then one fp32
+ *              multiply by the accumulator, then round-to-nearest-even)
+ *
+ *   q          device, int8 [M, K] from bitlinear_quant_act, 16-byte aligned.
+ *   tok_scale  device, fp32 [M], 4-byte aligned.
+ *   packed     device, packed weights of an [N, K] matrix.
+ *   gamma      device, one float (the weight scale), 4-byte aligned.
+ *   out_bf16   device, bf16 [M, N], 16-byte aligned.
+ *   acc_out    device, int32 [M, N], 16-byte aligned, or NULL (the exact
+ *              integer accumulators, for checking).
+ * Engine choice is internal: M <= 16 runs the decode GEMV (legacy tensor
+ * MMA on register-unpacked codes, HBM-bound), larger M runs the prefill
+ * GEMM (tcgen05 MMA with TMEM accumulators).  Both give identical results.
+ * Every bounded wait inside the GEMM that expires sets a device status
+ * word; bitlinear_check_status reports it.
+ * Errors: INVALID_ARG (null/misaligned pointer, M < 0, N < 1, K < 16,
+ * K % 16 != 0, K > 65536: the fp32 tensor-core sums stay exact below
+ * that), CUDA (launch failure).
+ */
+BITLINEAR_API bitlinear_status_t bitlinear_forward(const int8_t *q, const float *tok_scale,
+                                     const uint8_t *packed, const float *gamma, int64_t M,
+                                     int64_t N, int64_t K, void *out_bf16, int32_t *acc_out,
+                                     void *stream);
+
+/*
+ * Reads and clears the current device's kernel status word (a bounded wait
+ * that gave up) after synchronising `stream`.  Returns BITLINEAR_OK or
+ * BITLINEAR_ERR_TIMEOUT; BITLINEAR_ERR_CUDA if the stream reports an error.
+ */
+BITLINEAR_API bitlinear_status_t bitlinear_check_status(void *stream);
+
+/*
+ * Test hook: sets the spin limit of every bounded wait in the library's
+ * kernels (iterations of a try-wait loop; 0 restores the default).  A tiny
+ * limit makes the waits give up, so the timeout path can be exercised
+ * without hanging or faulting the GPU.
+ */
+BITLINEAR_API void bitlinear_set_wait_limit(uint32_t iterations);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BITLINEAR_H_ */

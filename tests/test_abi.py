@@ -1,0 +1,113 @@
+"""The C ABI library builds, loads and exports every declared symbol; argument
+validation works without a GPU (it runs before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import bitlinear_02_b300 as bl
+from bitlinear_02_b300 import build as blbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bitlinear.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    blbuild.build()
+    return bl.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(bitlinear_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("bitlinear_pack_weights", "bitlinear_pack_ternary", "bitlinear_quant_act",
+                 "bitlinear_forward", "bitlinear_packed_bytes", "bitlinear_status_string",
+                 "bitlinear_check_status"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_only_abi_symbols_are_exported(lib):
+    # the build hides everything that is not declared extern "C" in the header
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", bl.library_path()], capture_output=True,
+                         text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    ours = {s for s in exported if s.startswith("bitlinear_")}
+    assert ours == set(declared_functions())
+
+
+def test_packed_bytes(lib):
+    assert bl.bitlinear_packed_bytes(512, 256) == 512 * 256 // 4
+    assert bl.bitlinear_packed_bytes(17, 144) == 32 * 256 // 4
+    assert bl.bitlinear_packed_bytes(0, 16) == 0
+    assert bl.bitlinear_packed_bytes(16, 0) == 0
+
+
+def test_status_strings(lib):
+    assert bl.bitlinear_status_string(0) == "ok"
+    assert "invalid" in bl.bitlinear_status_string(1)
+    assert "bounded wait" in bl.bitlinear_status_string(4)
+    assert bl.bitlinear_status_string(99) == "unknown status"
+    assert bl.bitlinear_version() == 100
+
+
+FAKE = 1 << 20  # an aligned non-null address: never dereferenced, checks fail first
+
+
+def test_forward_rejects_bad_arguments(lib):
+    L = lib
+    P = ctypes.c_void_p
+    ok = dict(q=P(FAKE), s=P(FAKE), p=P(FAKE), g=P(FAKE), o=P(FAKE))
+
+    def call(M=4, N=32, K=64, **kw):
+        a = dict(ok, **kw)
+        return L.bitlinear_forward(a["q"], a["s"], a["p"], a["g"], M, N, K, a["o"], None, None)
+
+    assert call(K=10) == bl.ERR_INVALID_ARG       # K not a multiple of 16
+    assert call(K=0) == bl.ERR_INVALID_ARG
+    assert call(K=65536 + 16) == bl.ERR_INVALID_ARG
+    assert call(N=0) == bl.ERR_INVALID_ARG
+    assert call(M=-1) == bl.ERR_INVALID_ARG
+    assert call(q=None) == bl.ERR_INVALID_ARG
+    assert call(o=P(FAKE + 2)) == bl.ERR_INVALID_ARG  # misaligned output
+    assert call(g=P(FAKE + 2)) == bl.ERR_INVALID_ARG  # misaligned gamma
+    assert call(M=0) == bl.OK                         # empty batch: nothing to do
+
+
+def test_quant_and_pack_reject_bad_arguments(lib):
+    L = lib
+    P = ctypes.c_void_p
+    assert L.bitlinear_quant_act(P(FAKE), None, 3, 24, 1e-5, P(FAKE), P(FAKE), None) == bl.ERR_INVALID_ARG
+    assert L.bitlinear_quant_act(None, None, 3, 32, 1e-5, P(FAKE), P(FAKE), None) == bl.ERR_INVALID_ARG
+    assert L.bitlinear_quant_act(P(FAKE + 8), None, 3, 32, 1e-5, P(FAKE), P(FAKE), None) == bl.ERR_INVALID_ARG
+    assert L.bitlinear_quant_act(P(FAKE), None, 0, 32, 1e-5, P(FAKE), P(FAKE), None) == bl.OK
+    assert L.bitlinear_pack_weights(P(FAKE), 0, 32, 1e-5, P(FAKE), P(FAKE), None) == bl.ERR_INVALID_ARG
+    assert L.bitlinear_pack_weights(P(FAKE), 4, 33, 1e-5, P(FAKE), P(FAKE), None) == bl.ERR_INVALID_ARG
+    assert L.bitlinear_pack_weights(None, 4, 32, 1e-5, P(FAKE), P(FAKE), None) == bl.ERR_INVALID_ARG
+    assert L.bitlinear_pack_ternary(P(FAKE), 4, 32, P(FAKE + 4), None) == bl.ERR_INVALID_ARG
+
+
+def test_python_binding_raises_on_error(lib):
+    with pytest.raises(bl.BitLinearError) as ei:
+        bl._check(bl.ERR_INVALID_ARG, "bitlinear_forward")
+    assert ei.value.status == bl.ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    import importlib
+    monkeypatch.setattr(bl, "_lib", None)
+    monkeypatch.setattr(bl, "_HERE", str(tmp_path))
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        bl.load_library()
