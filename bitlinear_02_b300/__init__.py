@@ -18,7 +18,8 @@ import torch
 
 __all__ = [
     "BitLinearError", "library_path", "load_library",
-    "bitlinear_packed_bytes", "bitlinear_pack_weights", "bitlinear_pack_ternary",
+    "bitlinear_packed_bytes", "bitlinear_pack_weights", "bitlinear_pack_weights_noalloc",
+    "bitlinear_pack_ternary",
     "bitlinear_quant_act", "bitlinear_forward", "bitlinear_check_status",
     "bitlinear_set_wait_limit", "bitlinear_status_string", "bitlinear_version",
     "pack_weights", "pack_ternary", "quant_act", "forward", "bitlinear",
@@ -66,12 +67,13 @@ def load_library():
     L.bitlinear_packed_bytes.restype = ctypes.c_size_t
     L.bitlinear_pack_weights.argtypes = [P, I64, I64, F, P, P, P]
     L.bitlinear_pack_ternary.argtypes = [P, I64, I64, P, P]
+    L.bitlinear_pack_weights_noalloc.argtypes = [P, I64, I64, F, P, P, P]
     L.bitlinear_quant_act.argtypes = [P, P, I64, I64, F, P, P, P]
     L.bitlinear_forward.argtypes = [P, P, P, P, I64, I64, I64, P, P, P]
     L.bitlinear_check_status.argtypes = [P]
     L.bitlinear_set_wait_limit.argtypes = [ctypes.c_uint32]
     L.bitlinear_set_wait_limit.restype = None
-    for name in ("bitlinear_pack_weights", "bitlinear_pack_ternary", "bitlinear_quant_act",
+    for name in ("bitlinear_pack_weights", "bitlinear_pack_weights_noalloc", "bitlinear_pack_ternary", "bitlinear_quant_act",
                  "bitlinear_forward", "bitlinear_check_status"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -121,6 +123,15 @@ def bitlinear_pack_weights(W, N: int, K: int, eps: float, packed, gamma, stream=
     _check(load_library().bitlinear_pack_weights(_ptr(W), int(N), int(K), float(eps), _ptr(packed),
                                                  _ptr(gamma), _stream(stream)),
            "bitlinear_pack_weights")
+
+
+def bitlinear_pack_weights_noalloc(W, N: int, K: int, eps: float, packed, gamma,
+                                   stream=None) -> None:
+    """bitlinear_pack_weights for callers that cannot allocate: its scratch
+    is a fixed array inside the library (see include/bitlinear.h)."""
+    _check(load_library().bitlinear_pack_weights_noalloc(_ptr(W), int(N), int(K), float(eps),
+                                                         _ptr(packed), _ptr(gamma), _stream(stream)),
+           "bitlinear_pack_weights_noalloc")
 
 
 def bitlinear_pack_ternary(Wq, N: int, K: int, packed, stream=None) -> None:

@@ -257,3 +257,76 @@ extern "C" bitlinear_status_t bitlinear_pack_ternary(const int8_t *Wq, int64_t N
         return BITLINEAR_ERR_CUDA;
     return BITLINEAR_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Packing without any allocation.
+//
+// Some callers cannot call cudaMalloc: code running under an allocator that
+// owns all device memory (a serving runtime's arena, a memory pool that must
+// not be fragmented), or code that must not take the driver's allocation
+// lock at that moment.  bitlinear_pack_weights allocates its 2 KB bucket
+// workspace on the first call per device; this variant instead keeps the
+// 256 exponent buckets in the fixed device array below, which every GPU
+// that loads the library holds until the process exits.
+// ---------------------------------------------------------------------------
+namespace bl {
+namespace {
+
+// 256 64-bit counters (2 KB): the whole scratch of the absmean sum.
+static __device__ __align__(256) unsigned long long g_noalloc_buckets[kBuckets];
+
+// Each bucket gathers up to N*K mantissas below 2^24; keeping N*K <= 2^40
+// keeps every counter below 2^64.
+constexpr int64_t kNoAllocMaxElems = 1ll << 40;
+
+std::mutex g_noalloc_mutex;
+unsigned long long *g_noalloc_ptr[64] = {nullptr};
+
+// Device address of g_noalloc_buckets on the current device, looked up once
+// per device.  In host code the array's name is only a host-side stand-in;
+// kernels must be given this address.
+cudaError_t noalloc_scratch(unsigned long long **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_buckets);
+        if (e != cudaSuccess) return e;
+        g_noalloc_ptr[dev] = static_cast<unsigned long long *>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace bl
+
+extern "C" bitlinear_status_t bitlinear_pack_weights_noalloc(const float *W, int64_t N, int64_t K,
+                                                             float eps, uint8_t *packed,
+                                                             float *gamma, void *stream) {
+    using namespace bl;
+    if (!W || !packed || !gamma || !shape_ok(N, K)) return BITLINEAR_ERR_INVALID_ARG;
+    if (!aligned16(W) || !aligned16(packed) || !aligned4(gamma)) return BITLINEAR_ERR_INVALID_ARG;
+    if (N * K > kNoAllocMaxElems) return BITLINEAR_ERR_UNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned long long *ws = nullptr;
+    if (noalloc_scratch(&ws) != cudaSuccess) return BITLINEAR_ERR_CUDA;
+    // The array keeps the previous call's sums: clear it first.
+    if (cudaMemsetAsync(ws, 0, kBuckets * sizeof(unsigned long long), st) != cudaSuccess)
+        return BITLINEAR_ERR_CUDA;
+    const int64_t n4 = N * K / 4;
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) != cudaSuccess) return BITLINEAR_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = 148;
+    const int64_t want = (n4 + 255) / 256;
+    const unsigned blocks = static_cast<unsigned>(want < sms * 8 ? (want < 1 ? 1 : want) : sms * 8);
+    absmean_buckets_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4 *>(W), n4, ws);
+    if (cudaGetLastError() != cudaSuccess) return BITLINEAR_ERR_CUDA;
+    gamma_finish_kernel<<<1, 32, 0, st>>>(ws, N * K, gamma);
+    if (cudaGetLastError() != cudaSuccess) return BITLINEAR_ERR_CUDA;
+    if (launch_pack(W, true, N, K, eps, gamma, packed, st) != cudaSuccess) return BITLINEAR_ERR_CUDA;
+    return BITLINEAR_OK;
+}

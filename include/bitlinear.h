@@ -107,6 +107,29 @@ BITLINEAR_API bitlinear_status_t bitlinear_pack_weights(const float *W, int64_t 
                                           uint8_t *packed, float *gamma, void *stream);
 
 /*
+ * Same result as bitlinear_pack_weights, for callers that cannot allocate
+ * device memory: code whose device memory is all owned by another allocator
+ * (a serving runtime's arena or pool), or code that must not take the
+ * driver's allocation lock at that point.  This entry point allocates
+ * nothing; the pages have no counterpart for it.
+ *
+ * Its scratch is a fixed device array of 256 64-bit counters (2 KB) built
+ * into the library, present on every GPU that loads the library until the
+ * process exits.  Limit: N*K <= 2^40 weights (each counter then stays below
+ * 2^64); larger matrices return BITLINEAR_ERR_UNSUPPORTED.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call clears and reuses the same array,
+ * so calls that overlap on the GPU (other streams, other threads) race and
+ * give wrong results: serialise them.
+ * Arguments, layout and other errors as bitlinear_pack_weights.
+ */
+BITLINEAR_API bitlinear_status_t bitlinear_pack_weights_noalloc(const float *W, int64_t N,
+                                                                int64_t K, float eps,
+                                                                uint8_t *packed, float *gamma,
+                                                                void *stream);
+
+/*
  * Packing of weights that are already ternary (the scale gamma is kept by
  * the caller).  Wq: device int8 [N, K] with values in {-1, 0, +1}
  * (other values are clamped to that range).  packed as above.
