@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libbitlinear.so")
-SOURCES = ["pack.cu", "quant.cu", "gemv.cu", "gemm.cu", "api.cu"]
+SOURCES = ["pack.cu", "quant.cu", "gemv.cu", "gemm.cu", "chain.cu", "api.cu"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
@@ -34,7 +34,7 @@ def _needs(out: str, deps: list[str]) -> bool:
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
     os.makedirs(OUT_DIR, exist_ok=True)
-    headers = [os.path.join(CSRC, "bl_device.cuh"),
+    headers = [os.path.join(CSRC, "bl_device.cuh"), os.path.join(CSRC, "decode_math.cuh"),
                os.path.join(os.path.dirname(HERE), "include", "bitlinear.h")]
     jobs = []
     objs = []

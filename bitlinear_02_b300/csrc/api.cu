@@ -45,6 +45,10 @@ extern "C" const char *bitlinear_status_string(int status) {
 
 extern "C" int bitlinear_version(void) { return 100; }
 
+namespace bl {
+uint32_t current_wait_limit() { return g_wait_limit.load(); }
+}  // namespace bl
+
 extern "C" void bitlinear_set_wait_limit(uint32_t iterations) {
     bl::g_wait_limit.store(iterations ? iterations : bl::kDefaultWaitLimit);
 }

@@ -264,6 +264,15 @@ cudaError_t launch_gemm(const int8_t *q, const float *tok_scale, const uint8_t *
     return launch_bn<256>(q, tok_scale, packed, gamma, M, N, K, out, acc_out, st, wait_limit);
 }
 
+// Device address of the status word, for kernels in other translation units.
+cudaError_t status_word(unsigned int **dev_ptr) {
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_gemm_status);
+    if (e != cudaSuccess) return e;
+    *dev_ptr = static_cast<unsigned int *>(p);
+    return cudaSuccess;
+}
+
 cudaError_t gemm_status(unsigned int *out, cudaStream_t st) {
     cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_gemm_status, sizeof(unsigned int), 0,
                                               cudaMemcpyDeviceToHost, st);

@@ -115,8 +115,6 @@ __global__ void __launch_bounds__(256) pack_kernel(const void *__restrict__ src,
                                                    int64_t K, int64_t KT, int64_t nchunks,
                                                    float eps, const float *__restrict__ gamma,
                                                    uint4 *__restrict__ packed) {
-    pdl_launch_dependents();
-    pdl_wait();
     int64_t id = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
     if (id >= nchunks) return;
     const int lane = static_cast<int>(id & 31);
@@ -201,16 +199,31 @@ cudaError_t workspace(unsigned long long **out) {
 
 bool shape_ok(int64_t N, int64_t K) { return N >= 1 && K >= 16 && (K % 16) == 0 && N <= (1ll << 31) && K <= (1ll << 31); }
 
+// The matmul kernels read packed weights before they wait for the kernel
+// that precedes them in the stream (weights are static, so their loads can
+// overlap that kernel).  The packers must therefore hand over weights that
+// are complete and visible: pack_kernel is an ordinary launch that never lets
+// its dependents start early, and it is followed by publish_kernel, another
+// ordinary launch, which starts only once pack_kernel has finished and its
+// writes are visible.  A kernel launched after the packer can start early
+// only relative to publish_kernel, when the packed bytes are already final.
+__global__ void publish_kernel() {}
+
 cudaError_t launch_pack(const void *src, bool from_float, int64_t N, int64_t K, float eps,
                         const float *gamma, uint8_t *packed, cudaStream_t st) {
     const int64_t Np = (N + 15) / 16 * 16, KT = (K + 127) / 128;
     const int64_t nchunks = (Np / 16) * KT * 32;
     const unsigned blocks = static_cast<unsigned>((nchunks + 255) / 256);
     if (from_float)
-        return launch_pdl(pack_kernel<true>, dim3(blocks), dim3(256), 0, st, 1, src, N, K, KT,
-                          nchunks, eps, gamma, reinterpret_cast<uint4 *>(packed));
-    return launch_pdl(pack_kernel<false>, dim3(blocks), dim3(256), 0, st, 1, src, N, K, KT,
-                      nchunks, eps, gamma, reinterpret_cast<uint4 *>(packed));
+        pack_kernel<true><<<blocks, 256, 0, st>>>(src, N, K, KT, nchunks, eps, gamma,
+                                                  reinterpret_cast<uint4 *>(packed));
+    else
+        pack_kernel<false><<<blocks, 256, 0, st>>>(src, N, K, KT, nchunks, eps, gamma,
+                                                   reinterpret_cast<uint4 *>(packed));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    publish_kernel<<<1, 32, 0, st>>>();
+    return cudaGetLastError();
 }
 
 }  // namespace
