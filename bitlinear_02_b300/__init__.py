@@ -53,7 +53,7 @@ class ChainPlan(ctypes.Structure):
                 ("part_bytes", ctypes.c_uint32), ("off_phases", ctypes.c_uint64),
                 ("off_projs", ctypes.c_uint64), ("off_xstats", ctypes.c_uint64),
                 ("off_partials", ctypes.c_uint64), ("eps", ctypes.c_float),
-                ("reserved", ctypes.c_int32), ("magic", ctypes.c_uint64)]
+                ("ring_bytes", ctypes.c_uint32), ("magic", ctypes.c_uint64)]
 
 
 class BitLinearError(RuntimeError):

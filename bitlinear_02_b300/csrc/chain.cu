@@ -41,12 +41,12 @@ cudaError_t status_word(unsigned int **dev_ptr);  // gemm.cu: the library's devi
 
 namespace chain {
 
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 7;  // + 1 producer warp: 8 warps, so 255 registers fit
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kThreads = kConsumers + 32;
-constexpr int kSlotBytes = 4096;  // up to 8 k-tiles of one 16-row group
-constexpr int kSlots = 32;
+constexpr int kDesc = 32;          // weight chunks in flight per CTA (one per task)
 constexpr int kMaxProjPerPhase = 4;
+constexpr int kMaxProj = 1024;     // gamma values staged in shared memory
 constexpr int kMaxCTA = 256;
 constexpr uint32_t kDrainLimit = 1u << 30;
 constexpr uint64_t kPlanMagic = 0x424c4348414e3031ull;
@@ -69,17 +69,24 @@ struct Phase {
     int32_t proj0, nproj, RGT, in_phase;  // in_phase: phase index that wrote the input
     int32_t qstride, rg_max, pad0, pad1;
 };
+static_assert(sizeof(Phase) % 16 == 0 && sizeof(Proj) % 8 == 0, "plan records");
+
+// Metadata image of one phase (contiguous, so one round trip fetches it).
+struct MetaImg {
+    Phase ph;
+    Proj pj[kMaxProjPerPhase];
+};
 
 struct Args {
-    const Phase *phases;
-    const Proj *projs;
+    const MetaImg *metas;
+    const float *const *gammas;  // device pointers of every projection's gamma
     const __nv_bfloat16 *x;
     unsigned long long *x_stats;
     unsigned long long *partials;
     unsigned int *ctl;     // [0] arrivals, [1] exits, [2] launch epoch
     unsigned int *status;  // library status word (bounded wait expired)
-    int32_t nphase, M, Mp, nCTA, K0;
-    uint32_t q_bytes, part_bytes, wait_limit;
+    int32_t nphase, nproj, M, Mp, nCTA, K0;
+    uint32_t ring_bytes, q_bytes, part_bytes, wait_limit;
     float eps;
 };
 
@@ -114,8 +121,10 @@ __host__ __device__ inline Work work_of(const Phase &ph, int cta) {
     return w;
 }
 
+// Task i of a CTA's phase work: up to 4 row groups x up to 8 k-tiles; its
+// weights travel as one chunk of the shared-memory ring.
 struct Task {
-    int rlo, rhi, tlo, thi, chunk_off;
+    int rlo, rhi, tlo, thi;
 };
 
 __host__ __device__ inline Task task_of(const Work &w, int i) {
@@ -126,15 +135,20 @@ __host__ __device__ inline Task task_of(const Work &w, int i) {
     const int kt = w.t1 - w.t0;
     t.tlo = w.t0 + piece * kt / w.npieces;
     t.thi = w.t0 + (piece + 1) * kt / w.npieces;
-    t.chunk_off = set * w.npieces * 4 + piece * (t.rhi - t.rlo);
     return t;
 }
 
-// Shared-memory layout (bytes): ring | q cache | partial sums | barriers | scalars.
-__host__ __device__ inline uint32_t smem_bytes_for(uint32_t q_bytes, uint32_t part_bytes) {
-    return kSlots * kSlotBytes + q_bytes + part_bytes + 2 * kSlots * 8 /*mbarriers*/ +
-           kConsumerWarps * kMaxProjPerPhase * 16 * (4 + 8) /*stat reduction*/ + 16 * 4 * 2 +
-           kMaxProjPerPhase * 4 + 64;
+constexpr int kMetaWords = static_cast<int>(sizeof(MetaImg) / 4);
+constexpr int kMetaPerLane = (kMetaWords + 31) / 32;
+
+// Shared-memory layout (bytes): ring | q cache | partial sums | metadata x2 |
+// mbarriers | chunk offsets | reductions | scalars.
+__host__ __device__ inline uint32_t smem_fixed_bytes() {
+    return 2 * static_cast<uint32_t>(sizeof(MetaImg)) + kMaxProj * 4 + 2 * kDesc * 8 + kDesc * 4 +
+           kConsumerWarps * kMaxProjPerPhase * 16 * 12 + 16 * 4 * 2 + 64;
+}
+__host__ __device__ inline uint32_t smem_bytes_for(uint32_t ring, uint32_t q_bytes, uint32_t part_bytes) {
+    return ring + q_bytes + part_bytes + smem_fixed_bytes();
 }
 
 // ------------------------------------------------------------- device ----
@@ -147,22 +161,16 @@ __device__ __forceinline__ uint32_t tag_of(uint32_t epoch, int phase_idx) {
 }
 __device__ __forceinline__ uint32_t tag16_of(uint32_t tag) { return tag % 65535u + 1u; }
 
-__device__ __forceinline__ int proj_of(const Phase &ph, const Proj *projs, int r) {
-    int j = 0;
-    for (; j < ph.nproj - 1; ++j) {
-        const Proj &P = projs[ph.proj0 + j];
-        if (r < P.rg_base + P.RG) break;
-    }
-    return j;
-}
-
 struct Shared {
     uint8_t *ring, *qc;
     int32_t *part;
+    MetaImg *meta;    // [2]
+    float *gall;      // gamma of every projection
     uint64_t *full, *empty;
-    float *red_mx;   // [warp][proj][16]
-    double *red_ss;  // [warp][proj][16]
-    float *c, *ts, *gam;
+    uint32_t *coff;   // ring offset (monotonic) of each chunk descriptor
+    float *red_hi, *red_lo;  // [warp][proj][16]
+    float *red_mx;           // [warp][proj][16]
+    float *c, *ts;
     volatile int *abort_flag;
     uint32_t *epoch;
 };
@@ -170,18 +178,23 @@ struct Shared {
 __device__ __forceinline__ Shared carve(uint8_t *base, const Args &A) {
     Shared S;
     S.ring = base;
-    S.qc = base + kSlots * kSlotBytes;
+    S.qc = base + A.ring_bytes;
     S.part = reinterpret_cast<int32_t *>(S.qc + A.q_bytes);
     uint8_t *p = reinterpret_cast<uint8_t *>(S.part) + A.part_bytes;
+    S.meta = reinterpret_cast<MetaImg *>(p);
+    p += 2 * sizeof(MetaImg);
+    S.gall = reinterpret_cast<float *>(p);
+    p += kMaxProj * 4;
     S.full = reinterpret_cast<uint64_t *>(p);
-    S.empty = S.full + kSlots;
-    S.red_ss = reinterpret_cast<double *>(S.empty + kSlots);
-    S.red_mx = reinterpret_cast<float *>(S.red_ss + kConsumerWarps * kMaxProjPerPhase * 16);
+    S.empty = S.full + kDesc;
+    S.coff = reinterpret_cast<uint32_t *>(S.empty + kDesc);
+    S.red_hi = reinterpret_cast<float *>(S.coff + kDesc);
+    S.red_lo = S.red_hi + kConsumerWarps * kMaxProjPerPhase * 16;
+    S.red_mx = S.red_lo + kConsumerWarps * kMaxProjPerPhase * 16;
     S.c = S.red_mx + kConsumerWarps * kMaxProjPerPhase * 16;
     S.ts = S.c + 16;
-    S.gam = S.ts + 16;
-    S.abort_flag = reinterpret_cast<volatile int *>(S.gam + kMaxProjPerPhase);
-    S.epoch = reinterpret_cast<uint32_t *>(S.gam + kMaxProjPerPhase) + 1;
+    S.abort_flag = reinterpret_cast<volatile int *>(S.ts + 16);
+    S.epoch = reinterpret_cast<uint32_t *>(S.ts + 16) + 1;
     return S;
 }
 
@@ -190,116 +203,196 @@ __device__ __forceinline__ void raise_abort(const Shared &S, unsigned int *statu
     atomicOr(status, 1u);
 }
 
-// Re-read a tagged word until (word >> shift) & mask == want; false on
-// timeout or when another CTA reported a failure.
-__device__ __noinline__ bool poll_tag(const unsigned long long *p, unsigned long long &v, uint32_t want,
-                                      uint32_t mask, int shift, uint32_t limit, const unsigned *status) {
+// Re-read a tagged word until (word >> shift) & mask == want, backing off
+// between reads.  Returns the word; on timeout, or when another CTA
+// reported a failure, returns it with the tag field cleared (never a valid
+// tag), which the caller treats as failure.  Out of line: the slow path.
+__device__ __noinline__ unsigned long long poll_tag(const unsigned long long *p, uint32_t want, uint32_t mask,
+                                                    int shift, uint32_t limit, const unsigned *status) {
     for (uint32_t i = 0; i < limit; ++i) {
-        v = ld_relaxed_u64(p);
-        if (static_cast<uint32_t>(v >> shift & mask) == want) return true;
-        if ((i & 63u) == 63u && ld_relaxed_u32(status) != 0u) return false;
+        __nanosleep(32);
+        const unsigned long long v = ld_cg_u64(p);
+        if (static_cast<uint32_t>(v >> shift & mask) == want) return v;
+        if ((i & 63u) == 63u && ld_relaxed_u32(status) != 0u) break;
     }
-    return false;
+    return 0ull;
+}
+__device__ __forceinline__ bool tag_ok(unsigned long long v, uint32_t want, uint32_t mask, int shift) {
+    return static_cast<uint32_t>(v >> shift & mask) == want;
 }
 
-// Per-token reduction of (max, sum of squares) over the 256 consumer
+// Compensated fp32 sums (hi + lo, error-free two-sum steps): B300's FP64
+// units are far too slow for this path.  Squares of bf16 values are exact in
+// fp32, so a sum of squares carries about 2^-48 relative error.
+struct FF {
+    float hi = 0.0f, lo = 0.0f;
+    __device__ __forceinline__ void add(float p) {
+        const float s = __fadd_rn(hi, p);
+        const float bp = __fsub_rn(s, hi);
+        lo = __fadd_rn(lo, __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(p, bp)));
+        hi = s;
+    }
+    __device__ __forceinline__ void add(const FF &o) {
+        add(o.hi);
+        lo = __fadd_rn(lo, o.lo);
+    }
+    __device__ __forceinline__ void add_sq(float v) { add(__fmul_rn(v, v)); }
+    __device__ __forceinline__ float value() const { return __fadd_rn(hi, lo); }
+};
+
+// Per-token reduction of (max, sum of squares) over the consumer
 // threads, where thread t holds token t % Mp: a fixed shuffle tree, then a
-// fixed-order sum over warps.  Results for proj slot j land in red_*[0][j][m].
-__device__ __forceinline__ void reduce_stats(const Shared &S, int j, float mx, double ss, int Mp,
-                                             int warp, int lane) {
+// fixed-order sum over warps (combine_stats).
+__device__ __forceinline__ void reduce_stats(const Shared &S, int j, float mx, FF ss, int Mp, int warp,
+                                             int lane) {
     for (int off = 16; off >= Mp; off >>= 1) {
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        FF o;
+        o.hi = __shfl_xor_sync(0xffffffffu, ss.hi, off);
+        o.lo = __shfl_xor_sync(0xffffffffu, ss.lo, off);
+        ss.add(o);
     }
     if (lane < Mp) {
         S.red_mx[(warp * kMaxProjPerPhase + j) * 16 + lane] = mx;
-        S.red_ss[(warp * kMaxProjPerPhase + j) * 16 + lane] = ss;
+        S.red_hi[(warp * kMaxProjPerPhase + j) * 16 + lane] = ss.hi;
+        S.red_lo[(warp * kMaxProjPerPhase + j) * 16 + lane] = ss.lo;
     }
 }
-__device__ __forceinline__ void combine_stats(const Shared &S, int j, int m, float &mx, double &ss) {
+__device__ __forceinline__ void combine_stats(const Shared &S, int j, int m, float &mx, FF &ss) {
     mx = 0.0f;
-    ss = 0.0;
+    ss = FF();
     for (int w = 0; w < kConsumerWarps; ++w) {
         mx = fmaxf(mx, S.red_mx[(w * kMaxProjPerPhase + j) * 16 + m]);
-        ss += S.red_ss[(w * kMaxProjPerPhase + j) * 16 + m];
+        FF o;
+        o.hi = S.red_hi[(w * kMaxProjPerPhase + j) * 16 + m];
+        o.lo = S.red_lo[(w * kMaxProjPerPhase + j) * 16 + m];
+        ss.add(o);
     }
 }
-__device__ __forceinline__ unsigned long long stats_word(float mx, double ss, uint32_t tag) {
+__device__ __forceinline__ unsigned long long stats_word(float mx, const FF &ss, uint32_t tag) {
     const uint32_t mb = __float_as_uint(mx) >> 16;  // mx is a bf16 value: exact
-    const uint32_t sb = __float_as_uint(__double2float_rn(ss));
+    const uint32_t sb = __float_as_uint(ss.value());
     return static_cast<unsigned long long>(mb | (tag16_of(tag) << 16)) |
            (static_cast<unsigned long long>(sb) << 32);
 }
 
-__device__ __forceinline__ int8_t quant1(float v, float c) {
+__device__ __forceinline__ uint32_t quant1(float v, float c) {
     int iv = __float2int_rn(__fmul_rn(v, c));
     iv = iv > 127 ? 127 : (iv < -128 ? -128 : iv);
-    return static_cast<int8_t>(iv);
+    return static_cast<uint32_t>(iv) & 0xffu;
 }
+
+// Metadata prefetch of one phase by one warp: issue (one round trip, 4
+// words per lane) early, commit to shared memory late.
+struct MetaLoad {
+    uint32_t v[kMetaPerLane];
+    __device__ __forceinline__ void issue(const Args &A, int p, int lane) {
+        const uint32_t *src = reinterpret_cast<const uint32_t *>(A.metas + p);
+#pragma unroll
+        for (int u = 0; u < kMetaPerLane; ++u) {
+            const int w = lane + 32 * u;
+            v[u] = w < kMetaWords ? __ldg(src + w) : 0u;
+        }
+    }
+    __device__ __forceinline__ void commit(const Shared &S, int p, int lane) const {
+        uint32_t *dst = reinterpret_cast<uint32_t *>(&S.meta[p & 1]);
+#pragma unroll
+        for (int u = 0; u < kMetaPerLane; ++u) {
+            const int w = lane + 32 * u;
+            if (w < kMetaWords) dst[w] = v[u];
+        }
+    }
+};
 
 // ------------------------------------------------------------- producer --
 
+// Ring of weight chunks (one per task), allocated first-in first-out in a
+// byte ring so that small chunks do not waste space: the producer waits for
+// the oldest chunks to be released until the new chunk fits.
 __device__ void producer(const Args &A, const Shared &S) {
     const int cta = blockIdx.x;
-    uint32_t idx = 0;
+    const uint32_t RB = A.ring_bytes;
+    uint32_t idx = 0, tail = 0, head = 0;
     bool ok = true;
     for (int p = 0; p < A.nphase && ok; ++p) {
-        const Phase ph = A.phases[p];
+        // this phase's metadata in registers: all loads issued together
+        const MetaImg &MI = A.metas[p];
+        const Phase ph = MI.ph;
+        const uint8_t *pk[kMaxProjPerPhase];
+        int rb[kMaxProjPerPhase], re[kMaxProjPerPhase];
+#pragma unroll
+        for (int j = 0; j < kMaxProjPerPhase; ++j) {
+            pk[j] = MI.pj[j].packed;
+            rb[j] = MI.pj[j].rg_base;
+            re[j] = MI.pj[j].rg_base + MI.pj[j].RG;
+        }
         const Work w = work_of(ph, cta);
         if (!w.valid || w.npieces == 0) continue;
         const int ntask = w.nsets * w.npieces;
+        const int64_t KT = ph.KT;
         for (int i = 0; i < ntask && ok; ++i) {
             const Task t = task_of(w, i);
-            for (int r = t.rlo; r < t.rhi; ++r) {
-                const Proj &P = A.projs[ph.proj0 + proj_of(ph, A.projs, r)];
-                const int local = r - P.rg_base;
-                const uint8_t *src = P.packed + (static_cast<int64_t>(local) * ph.KT + t.tlo) * 512;
-                const uint32_t bytes = static_cast<uint32_t>(t.thi - t.tlo) * 512u;
-                const uint32_t slot = idx % kSlots, par = (idx / kSlots) & 1u;
-                if (!mbar_wait_bounded(&S.empty[slot], par ^ 1u, A.wait_limit) || *S.abort_flag) {
+            const uint32_t per = static_cast<uint32_t>(t.thi - t.tlo) * 512u;
+            const uint32_t bytes = per * static_cast<uint32_t>(t.rhi - t.rlo);
+            const uint32_t pos = head % RB;
+            if (pos + bytes > RB) head += RB - pos;
+            // free space: [head, coff[tail] + RB) once the chunks before tail are released
+            while (ok && tail < idx && (idx - tail >= static_cast<uint32_t>(kDesc) ||
+                                        head + bytes > S.coff[tail % kDesc] + RB)) {
+                if (!mbar_wait_bounded(&S.empty[tail % kDesc], (tail / kDesc) & 1u, A.wait_limit) ||
+                    *S.abort_flag)
                     ok = false;
-                    break;
-                }
-                mbar_arrive_expect_tx(&S.full[slot], bytes);
-                bulk_g2s(S.ring + slot * kSlotBytes, src, bytes, &S.full[slot]);
-                ++idx;
+                ++tail;
             }
+            if (!ok) break;
+            const uint32_t d = idx % kDesc;
+            S.coff[d] = head;
+            mbar_arrive_expect_tx(&S.full[d], bytes);
+            uint8_t *dst = S.ring + head % RB;
+            for (int r = t.rlo; r < t.rhi; ++r) {
+                const uint8_t *base = pk[0];
+                int rg0 = rb[0];
+#pragma unroll
+                for (int j = 1; j < kMaxProjPerPhase; ++j)
+                    if (j < ph.nproj && r >= re[j - 1]) {
+                        base = pk[j];
+                        rg0 = rb[j];
+                    }
+                bulk_g2s(dst + (r - t.rlo) * per, base + (static_cast<int64_t>(r - rg0) * KT + t.tlo) * 512, per,
+                         &S.full[d]);
+            }
+            head += bytes;
+            ++idx;
         }
     }
     if (!ok) raise_abort(S, A.status);
     // Every copy issued must land before the CTA may exit.
-    const uint32_t first = idx > kSlots ? idx - kSlots : 0u;
+    const uint32_t first = idx > static_cast<uint32_t>(kDesc) ? idx - kDesc : 0u;
     for (uint32_t k = first; k < idx; ++k)
-        mbar_wait_bounded(&S.full[k % kSlots], (k / kSlots) & 1u, kDrainLimit);
+        mbar_wait_bounded(&S.full[k % kDesc], (k / kDesc) & 1u, kDrainLimit);
 }
 
 // ------------------------------------------------------------- consumers -
 
 template <int NT>
-__device__ void run_task(const Args &A, const Shared &S, const Phase &ph, const Work &w, const Task &t,
-                         uint32_t chunk_base, int lane) {
+__device__ __forceinline__ void run_task(const Args &A, const Shared &S, const Phase &ph, const Work &w,
+                                         const Task &t, uint32_t idx, int lane) {
     const int g = lane >> 2, tq = lane & 3;
     const int nrg = t.rhi - t.rlo;
-    uint32_t slot[4];
-    bool ok = true;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t idx = chunk_base + t.chunk_off + static_cast<uint32_t>(i);
-        slot[i] = idx % kSlots;
-        if (i < nrg && ok && !mbar_wait_warp(&S.full[slot[i]], (idx / kSlots) & 1u, A.wait_limit))
-            ok = false;
-    }
-    if (!ok) {
+    const uint32_t d = idx % kDesc;
+    if (!mbar_wait_warp(&S.full[d], (idx / kDesc) & 1u, A.wait_limit)) {
         if (lane == 0) raise_abort(S, A.status);
         return;
     }
-    float d[4][NT][4];
+    const uint8_t *chunk = S.ring + S.coff[d] % A.ring_bytes;
+    const uint32_t per = static_cast<uint32_t>(t.thi - t.tlo) * 512u;
+    float acc[4][NT][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < NT; ++j)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) d[i][j][e] = 0.0f;
+            for (int e = 0; e < 4; ++e) acc[i][j][e] = 0.0f;
     int corr[NT];
 #pragma unroll
     for (int j = 0; j < NT; ++j) corr[j] = 0;
@@ -317,19 +410,15 @@ __device__ void run_task(const Args &A, const Shared &S, const Phase &ph, const 
             }
             dm::build_b(q0, q1, b[j], corr[j]);
         }
+        const uint8_t *wt = chunk + (kt - t.tlo) * 512 + lane * 16;
+        uint4 wv[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if (i < nrg) {
-                const uint4 wv = *reinterpret_cast<const uint4 *>(S.ring + slot[i] * kSlotBytes +
-                                                                  (kt - t.tlo) * 512 + lane * 16);
-#pragma unroll
-                for (int j = 0; j < NT; ++j) dm::mma_chunk(wv, b[j], d[i][j]);
-            }
-        }
+        for (int i = 0; i < 4; ++i)
+            wv[i] = i < nrg ? *reinterpret_cast<const uint4 *>(wt + i * per) : make_uint4(0, 0, 0, 0);
+        dm::mma_tile<NT>(wv, nrg, b, acc);
     }
     __syncwarp();
-    if (lane == 0)
-        for (int i = 0; i < nrg; ++i) mbar_arrive(&S.empty[slot[i]]);
+    if (lane == 0) mbar_arrive(&S.empty[d]);
     // sum(q) per token: reduce over the four t lanes, then fetch this lane's tokens.
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
@@ -347,12 +436,12 @@ __device__ void run_task(const Args &A, const Shared &S, const Phase &ph, const 
             if (i >= nrg) continue;
             int32_t *pr = S.part + ((t.rlo - w.r0 + i) * 16) * Mp;
             if (t0k < A.M) {
-                atomicAdd(pr + g * Mp + t0k, __float2int_rn(d[i][j][0] * 16777216.0f) - ce);
-                atomicAdd(pr + (g + 8) * Mp + t0k, __float2int_rn(d[i][j][2] * 16777216.0f) - ce);
+                atomicAdd(pr + g * Mp + t0k, __float2int_rn(acc[i][j][0] * 16777216.0f) - ce);
+                atomicAdd(pr + (g + 8) * Mp + t0k, __float2int_rn(acc[i][j][2] * 16777216.0f) - ce);
             }
             if (t0k + 1 < A.M) {
-                atomicAdd(pr + g * Mp + t0k + 1, __float2int_rn(d[i][j][1] * 16777216.0f) - co);
-                atomicAdd(pr + (g + 8) * Mp + t0k + 1, __float2int_rn(d[i][j][3] * 16777216.0f) - co);
+                atomicAdd(pr + g * Mp + t0k + 1, __float2int_rn(acc[i][j][1] * 16777216.0f) - co);
+                atomicAdd(pr + (g + 8) * Mp + t0k + 1, __float2int_rn(acc[i][j][3] * 16777216.0f) - co);
             }
         }
     }
@@ -366,33 +455,39 @@ __device__ void consumers(const Args &A, const Shared &S) {
     const uint32_t epoch = *S.epoch;
     const uint32_t lim = A.wait_limit;
 
+    for (int j = tid; j < A.nproj; j += kConsumers) S.gall[j] = __ldg(A.gammas[j]);
+    if (warp == 1 && A.nphase > 0) {
+        MetaLoad ml;
+        ml.issue(A, 0, lane);
+        ml.commit(S, 0, lane);
+    }
     // ---- phase index 0: statistics of the chain input x over this CTA's k-range
     {
         const int chunks = A.K0 / 8;
         const int c0 = static_cast<int>(static_cast<int64_t>(cta) * chunks / A.nCTA);
         const int c1 = static_cast<int>(static_cast<int64_t>(cta + 1) * chunks / A.nCTA);
         float mx = 0.0f;
-        double ss = 0.0;
+        FF ss;
         const int m = tid % Mp;
         for (int e = tid; e < (c1 - c0) * Mp; e += kConsumers) {
             if (m >= M) continue;
-            const int ch = c0 + e / Mp;
-            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(A.x + static_cast<int64_t>(m) * A.K0) + ch);
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(A.x + static_cast<int64_t>(m) * A.K0) + c0 + e / Mp);
             const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const float a = __uint_as_float(wv[i] << 16), b = __uint_as_float(wv[i] & 0xffff0000u);
                 mx = fmaxf(mx, fmaxf(fabsf(a), fabsf(b)));
-                ss += static_cast<double>(a) * a + static_cast<double>(b) * b;
+                ss.add_sq(a);
+                ss.add_sq(b);
             }
         }
         reduce_stats(S, 0, mx, ss, Mp, warp, lane);
         named_sync(1, kConsumers);
         if (tid < M) {
             float cm;
-            double cs;
+            FF cs;
             combine_stats(S, 0, tid, cm, cs);
-            st_relaxed_u64(A.x_stats + cta * Mp + tid, stats_word(cm, cs, tag_of(epoch, 0)));
+            st_cg_u64(A.x_stats + cta * Mp + tid, stats_word(cm, cs, tag_of(epoch, 0)));
         }
         named_sync(1, kConsumers);
         if (tid == 0) red_relaxed_add_u32(A.ctl, 1u);
@@ -400,8 +495,6 @@ __device__ void consumers(const Args &A, const Shared &S) {
 
     uint32_t chunk_base = 0;
     for (int p = 0; p < A.nphase; ++p) {
-        const Phase ph = A.phases[p];
-        const Work w = work_of(ph, cta);
         const uint32_t tag = tag_of(epoch, p + 1);
         // ---- wait until every CTA finished the previous phase
         if (tid == 0) {
@@ -417,39 +510,53 @@ __device__ void consumers(const Args &A, const Shared &S) {
             if (!ok) raise_abort(S, A.status);
         }
         if (named_sync_or(1, kConsumers, *S.abort_flag != 0)) break;
+        const MetaImg &MT = S.meta[p & 1];
+        const Phase ph = MT.ph;
+        MetaLoad next;  // metadata of the next phase: fetched now, stored in the epilogue
+        if (warp == 1 && p + 1 < A.nphase) next.issue(A, p + 1, lane);
+        const Work w = work_of(ph, cta);
 
         // ---- statistics of the input: combine the producers' partials
         {
             const uint32_t want = tag16_of(tag_of(epoch, ph.in_phase));
             const int m = tid % Mp;
+            const int n = A.nCTA * Mp;
             float mx = 0.0f;
-            double ss = 0.0;
+            FF ss;
             bool ok = true;
-            for (int e = tid; e < A.nCTA * Mp; e += kConsumers) {
-                if (m >= M) continue;
-                unsigned long long v = ld_relaxed_u64(ph.stats_in + e);
-                if (static_cast<uint32_t>(v >> 16 & 0xffffu) != want &&
-                    !poll_tag(ph.stats_in + e, v, want, 0xffffu, 16, lim, A.status)) {
-                    ok = false;
-                    break;
+            for (int e0 = tid; e0 < n; e0 += 12 * kConsumers) {
+            unsigned long long v[12];
+#pragma unroll
+            for (int u = 0; u < 12; ++u) {
+                const int e = e0 + u * kConsumers;
+                if (e < n && m < M) v[u] = ld_cg_u64(ph.stats_in + e);
+            }
+#pragma unroll
+            for (int u = 0; u < 12; ++u) {
+                const int e = e0 + u * kConsumers;
+                if (e >= n || m >= M) continue;
+                if (!tag_ok(v[u], want, 0xffffu, 16)) {
+                    v[u] = poll_tag(ph.stats_in + e, want, 0xffffu, 16, lim, A.status);
+                    ok = ok && tag_ok(v[u], want, 0xffffu, 16);
                 }
-                mx = fmaxf(mx, __uint_as_float(static_cast<uint32_t>(v & 0xffffu) << 16));
-                ss += static_cast<double>(__uint_as_float(static_cast<uint32_t>(v >> 32)));
+                mx = fmaxf(mx, __uint_as_float(static_cast<uint32_t>(v[u] & 0xffffu) << 16));
+                ss.add(__uint_as_float(static_cast<uint32_t>(v[u] >> 32)));
+            }
             }
             if (!ok) raise_abort(S, A.status);
             reduce_stats(S, 0, mx, ss, Mp, warp, lane);
             named_sync(1, kConsumers);
             if (tid < M) {
                 float cm;
-                double cs;
+                FF cs;
                 combine_stats(S, 0, tid, cm, cs);
                 if (!(cm >= 1e-5f)) cm = 1e-5f;
                 S.c[tid] = __fdiv_rn(127.0f, cm);
-                const double r = 1.0 / sqrt(cs / static_cast<double>(ph.K) + static_cast<double>(A.eps));
-                S.ts[tid] = static_cast<float>(r * static_cast<double>(cm) / 127.0);
+                // tok_scale = rms^-1 * max / 127, every step correctly rounded fp32
+                const float ms = __fadd_rn(__fdiv_rn(cs.value(), static_cast<float>(ph.K)), A.eps);
+                const float r = __fdiv_rn(1.0f, __fsqrt_rn(ms));
+                S.ts[tid] = __fdiv_rn(__fmul_rn(r, cm), 127.0f);
             }
-            if (tid < ph.nproj) S.gam[tid] = *A.projs[ph.proj0 + tid].gamma;
-            if (named_sync_or(1, kConsumers, *S.abort_flag != 0)) break;
         }
 
         const bool has = w.valid && w.npieces > 0;
@@ -457,64 +564,71 @@ __device__ void consumers(const Args &A, const Shared &S) {
             // ---- quantise this CTA's k-slice of the input into the q cache
             const int klo = w.t0 * 128, khi = min(w.t1 * 128, ph.K), kend = w.t1 * 128;
             const int qs = ph.qstride;
-            const uint32_t in_tag = tag_of(epoch, ph.in_phase);
+            named_sync(1, kConsumers);  // S.c ready
             bool ok = true;
             if (ph.act_in == nullptr) {
                 const int per = (khi - klo) / 8;
-                for (int e = tid; e < M * per; e += kConsumers) {
-                    const int m = e / per, k = klo + 8 * (e % per);
-                    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(A.x + static_cast<int64_t>(m) * ph.K + k));
-                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-                    const float c = S.c[m];
-                    uint32_t o[2] = {0u, 0u};
+                const int n = M * per;
+                for (int e0 = tid; e0 < n; e0 += 8 * kConsumers) {
+                    uint4 v[8];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint32_t lo = static_cast<uint8_t>(quant1(__uint_as_float(wv[i] << 16), c));
-                        const uint32_t hi = static_cast<uint8_t>(quant1(__uint_as_float(wv[i] & 0xffff0000u), c));
-                        o[i >> 1] |= (lo | (hi << 8)) << (16 * (i & 1));
+                    for (int u = 0; u < 8; ++u) {
+                        const int e = e0 + u * kConsumers;
+                        if (e < n)
+                            v[u] = __ldg(reinterpret_cast<const uint4 *>(A.x + static_cast<int64_t>(e / per) * ph.K +
+                                                                         klo + 8 * (e % per)));
                     }
-                    *reinterpret_cast<uint2 *>(S.qc + m * qs + (k - klo)) = make_uint2(o[0], o[1]);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int e = e0 + u * kConsumers;
+                        if (e >= n) continue;
+                        const int m = e / per, k = klo + 8 * (e % per);
+                        const uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                        const float c = S.c[m];
+                        uint32_t o[2] = {0u, 0u};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const uint32_t lo = quant1(__uint_as_float(wv[i] << 16), c);
+                            const uint32_t hi = quant1(__uint_as_float(wv[i] & 0xffff0000u), c);
+                            o[i >> 1] |= (lo | (hi << 8)) << (16 * (i & 1));
+                        }
+                        *reinterpret_cast<uint2 *>(S.qc + m * qs + (k - klo)) = make_uint2(o[0], o[1]);
+                    }
                 }
             } else {
+                const uint32_t in_tag = tag_of(epoch, ph.in_phase);
                 const int per = (khi - klo) / 2;
                 const int half = ph.K / 2;
-                for (int e0 = tid; e0 < M * per && ok; e0 += 4 * kConsumers) {
-                    unsigned long long v[4];
+                const int n = M * per;
+                for (int e0 = tid; e0 < n; e0 += 8 * kConsumers) {
+                    unsigned long long v[8];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
+                    for (int u = 0; u < 8; ++u) {
                         const int e = e0 + u * kConsumers;
-                        if (e < M * per) {
-                            const int m = e / per, k = klo + 2 * (e % per);
-                            v[u] = ld_relaxed_u64(ph.act_in + static_cast<int64_t>(m) * half + k / 2);
-                        }
+                        if (e < n)
+                            v[u] = ld_cg_u64(ph.act_in + static_cast<int64_t>(e / per) * half + klo / 2 + e % per);
                     }
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
+                    for (int u = 0; u < 8; ++u) {
                         const int e = e0 + u * kConsumers;
-                        if (e >= M * per) continue;
+                        if (e >= n) continue;
                         const int m = e / per, k = klo + 2 * (e % per);
-                        if (static_cast<uint32_t>(v[u] >> 32) != in_tag &&
-                            !poll_tag(ph.act_in + static_cast<int64_t>(m) * half + k / 2, v[u], in_tag,
-                                      0xffffffffu, 32, lim, A.status)) {
-                            ok = false;
-                            continue;
+                        if (!tag_ok(v[u], in_tag, 0xffffffffu, 32)) {
+                            v[u] = poll_tag(ph.act_in + static_cast<int64_t>(m) * half + k / 2, in_tag, 0xffffffffu, 32,
+                                            lim, A.status);
+                            ok = ok && tag_ok(v[u], in_tag, 0xffffffffu, 32);
                         }
                         const uint32_t bits = static_cast<uint32_t>(v[u]);
                         const float c = S.c[m];
-                        const uint32_t lo = static_cast<uint8_t>(quant1(__uint_as_float(bits << 16), c));
-                        const uint32_t hi = static_cast<uint8_t>(quant1(__uint_as_float(bits & 0xffff0000u), c));
-                        *reinterpret_cast<uint16_t *>(S.qc + m * qs + (k - klo)) =
-                            static_cast<uint16_t>(lo | (hi << 8));
+                        const uint32_t lo = quant1(__uint_as_float(bits << 16), c);
+                        const uint32_t hi = quant1(__uint_as_float(bits & 0xffff0000u), c);
+                        *reinterpret_cast<uint16_t *>(S.qc + m * qs + (k - klo)) = static_cast<uint16_t>(lo | (hi << 8));
                     }
                 }
             }
             if (!ok) raise_abort(S, A.status);
-            // k beyond K in the last tile reads as zero
-            const int tail = kend - khi;
-            for (int e = tid; e < M * tail; e += kConsumers) {
-                const int m = e / tail, k = khi + e % tail;
-                S.qc[m * qs + (k - klo)] = 0;
-            }
+            const int tail = kend - khi;  // k beyond K in the last tile reads as zero
+            for (int e = tid; e < M * tail; e += kConsumers) S.qc[(e / tail) * qs + (khi - klo) + e % tail] = 0;
             for (int e = tid; e < w.nrgs * 16 * Mp; e += kConsumers) S.part[e] = 0;
         }
         if (named_sync_or(1, kConsumers, *S.abort_flag != 0)) break;
@@ -523,8 +637,8 @@ __device__ void consumers(const Args &A, const Shared &S) {
         if (has) {
             const int ntask = w.nsets * w.npieces;
             for (int i = warp; i < ntask; i += kConsumerWarps)
-                run_task<NT>(A, S, ph, w, task_of(w, i), chunk_base, lane);
-            chunk_base += static_cast<uint32_t>(w.nrgs * w.npieces);
+                run_task<NT>(A, S, ph, w, task_of(w, i), chunk_base + static_cast<uint32_t>(i), lane);
+            chunk_base += static_cast<uint32_t>(ntask);
         }
         if (named_sync_or(1, kConsumers, *S.abort_flag != 0)) break;
 
@@ -540,28 +654,39 @@ __device__ void consumers(const Args &A, const Shared &S) {
                     if ((rl >= o0 && rl < o1) || m >= M) continue;
                     const int row = (e / Mp) % 16;
                     const int64_t gi = ((static_cast<int64_t>(w.r0 + rl) * ph.S + w.s) * 16 + row) * Mp + m;
-                    st_relaxed_u64(A.partials + gi, static_cast<unsigned long long>(static_cast<uint32_t>(S.part[e])) |
+                    st_cg_u64(A.partials + gi, static_cast<unsigned long long>(static_cast<uint32_t>(S.part[e])) |
                                                         (static_cast<unsigned long long>(tag) << 32));
                 }
                 bool ok = true;
                 const int own = (o1 - o0) * 16 * Mp;
-                for (int e = tid; e < own && ok; e += kConsumers) {
-                    const int m = e % Mp;
-                    if (m >= M) continue;
+                const int S1 = ph.S - 1;
+                const int total = own * S1;  // (entry, peer) pairs
+                // index of (owned entry, peer) pair f in the partial-sum buffer, or -1
+                auto pidx = [&](int f) -> int64_t {
+                    const int e = f / S1, k = f % S1, m = e % Mp;
+                    if (f >= total || m >= M) return -1;
+                    const int s2 = k < w.s ? k : k + 1;
                     const int rl = o0 + e / (16 * Mp), row = (e / Mp) % 16;
-                    int32_t sum = 0;
-                    for (int s2 = 0; s2 < ph.S; ++s2) {
-                        if (s2 == w.s) continue;
-                        const int64_t gi = ((static_cast<int64_t>(w.r0 + rl) * ph.S + s2) * 16 + row) * Mp + m;
-                        unsigned long long v = ld_relaxed_u64(A.partials + gi);
-                        if (static_cast<uint32_t>(v >> 32) != tag &&
-                            !poll_tag(A.partials + gi, v, tag, 0xffffffffu, 32, lim, A.status)) {
-                            ok = false;
-                            break;
-                        }
-                        sum += static_cast<int32_t>(static_cast<uint32_t>(v));
+                    return ((static_cast<int64_t>(w.r0 + rl) * ph.S + s2) * 16 + row) * Mp + m;
+                };
+                for (int f0 = tid; f0 < total; f0 += 8 * kConsumers) {
+                    unsigned long long v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int64_t gi = pidx(f0 + u * kConsumers);
+                        if (gi >= 0) v[u] = ld_cg_u64(A.partials + gi);
                     }
-                    S.part[(rl * 16 + row) * Mp + m] += sum;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int f = f0 + u * kConsumers;
+                        const int64_t gi = pidx(f);
+                        if (gi < 0) continue;
+                        if (!tag_ok(v[u], tag, 0xffffffffu, 32)) {
+                            v[u] = poll_tag(A.partials + gi, tag, 0xffffffffu, 32, lim, A.status);
+                            ok = ok && tag_ok(v[u], tag, 0xffffffffu, 32);
+                        }
+                        atomicAdd(&S.part[o0 * 16 * Mp + f / S1], static_cast<int32_t>(static_cast<uint32_t>(v[u])));
+                    }
                 }
                 if (!ok) raise_abort(S, A.status);
             }
@@ -569,58 +694,52 @@ __device__ void consumers(const Args &A, const Shared &S) {
         if (named_sync_or(1, kConsumers, *S.abort_flag != 0)) break;
 
         // ---- epilogue: rescale, store, publish tagged outputs and statistics
+        if (warp == 1 && p + 1 < A.nphase) next.commit(S, p + 1, lane);
         {
-            float mx[kMaxProjPerPhase];
-            double ss[kMaxProjPerPhase];
-#pragma unroll
-            for (int j = 0; j < kMaxProjPerPhase; ++j) {
-                mx[j] = 0.0f;
-                ss[j] = 0.0;
-            }
             const int m = tid % Mp;
-            const int nent = (o1 - o0) * 8 * Mp;
-            for (int e = tid; e < nent; e += kConsumers) {
-                if (m >= M) continue;
-                const int rp = (e / Mp) % 8, rl = o0 + e / (8 * Mp);
-                const int r = w.r0 + rl;
-                const int j = proj_of(ph, A.projs, r);
-                const Proj &P = A.projs[ph.proj0 + j];
-                const int n0 = (r - P.rg_base) * 16 + 2 * rp;
-                const float f = __fmul_rn(S.gam[j], S.ts[m]);
-                uint32_t vb[2] = {0u, 0u};
+            for (int j = 0; j < ph.nproj; ++j) {
+                const Proj &P = MT.pj[j];
+                float mx = 0.0f;
+                FF ss;
+                // owned local row groups of projection j
+                const int lo = max(o0, P.rg_base - w.r0), hi = min(o1, P.rg_base + P.RG - w.r0);
+                const int nent = hi > lo ? (hi - lo) * 8 * Mp : 0;
+                const float f = __fmul_rn(S.gall[ph.proj0 + j], S.ts[m < M ? m : 0]);
+                for (int e = tid; e < nent; e += kConsumers) {
+                    if (m >= M) continue;
+                    const int rp = (e / Mp) % 8, rl = lo + e / (8 * Mp);
+                    const int n0 = (w.r0 + rl - P.rg_base) * 16 + 2 * rp;
+                    uint32_t vb[2] = {0u, 0u};
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int n = n0 + h;
-                    if (n >= P.N) continue;
-                    const int32_t acc = S.part[(rl * 16 + 2 * rp + h) * Mp + m];
-                    const __nv_bfloat16 v = __float2bfloat16_rn(__fmul_rn(static_cast<float>(acc), f));
-                    const float vf = __bfloat162float(v);
-                    vb[h] = static_cast<uint32_t>(__bfloat16_as_ushort(v));
-                    if (P.out) P.out[static_cast<int64_t>(m) * P.N + n] = v;
-                    if (P.acc_out) P.acc_out[static_cast<int64_t>(m) * P.N + n] = acc;
-#pragma unroll
-                    for (int jj = 0; jj < kMaxProjPerPhase; ++jj)
-                        if (jj == j) {
-                            mx[jj] = fmaxf(mx[jj], fabsf(vf));
-                            ss[jj] += static_cast<double>(vf) * vf;
-                        }
+                    for (int h = 0; h < 2; ++h) {
+                        const int n = n0 + h;
+                        if (n >= P.N) continue;
+                        const int32_t acc = S.part[(rl * 16 + 2 * rp + h) * Mp + m];
+                        const __nv_bfloat16 v = __float2bfloat16_rn(__fmul_rn(static_cast<float>(acc), f));
+                        const float vf = __bfloat162float(v);
+                        vb[h] = static_cast<uint32_t>(__bfloat16_as_ushort(v));
+                        if (P.out) P.out[static_cast<int64_t>(m) * P.N + n] = v;
+                        if (P.acc_out) P.acc_out[static_cast<int64_t>(m) * P.N + n] = acc;
+                        mx = fmaxf(mx, fabsf(vf));
+                        ss.add_sq(vf);
+                    }
+                    if (P.act_out)
+                        st_cg_u64(P.act_out + static_cast<int64_t>(m) * (P.N / 2) + n0 / 2,
+                                       static_cast<unsigned long long>(vb[0] | (vb[1] << 16)) |
+                                           (static_cast<unsigned long long>(tag) << 32));
+                    if (w.r0 + rl == P.rg_base && rp == 0 && P.tok_scale_out) P.tok_scale_out[m] = S.ts[m];
                 }
-                if (P.act_out)
-                    st_relaxed_u64(P.act_out + static_cast<int64_t>(m) * (P.N / 2) + n0 / 2,
-                                   static_cast<unsigned long long>(vb[0] | (vb[1] << 16)) |
-                                       (static_cast<unsigned long long>(tag) << 32));
-                if (r == P.rg_base && rp == 0 && P.tok_scale_out) P.tok_scale_out[m] = S.ts[m];
+                reduce_stats(S, j, mx, ss, Mp, warp, lane);
             }
-            for (int j = 0; j < ph.nproj; ++j) reduce_stats(S, j, mx[j], ss[j], Mp, warp, lane);
             named_sync(1, kConsumers);
             if (tid < ph.nproj * Mp) {
                 const int j = tid / Mp, mm = tid % Mp;
-                const Proj &P = A.projs[ph.proj0 + j];
+                const Proj &P = MT.pj[j];
                 if (mm < M && P.stats_out) {
                     float cm;
-                    double cs;
+                    FF cs;
                     combine_stats(S, j, mm, cm, cs);
-                    st_relaxed_u64(P.stats_out + cta * Mp + mm, stats_word(cm, cs, tag));
+                    st_cg_u64(P.stats_out + cta * Mp + mm, stats_word(cm, cs, tag));
                 }
             }
         }
@@ -636,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const Args A) {
     if (threadIdx.x == 0) {
         *S.abort_flag = 0;
         *S.epoch = ld_relaxed_u32(A.ctl + 2);
-        for (int i = 0; i < kSlots; ++i) {
+        for (int i = 0; i < kDesc; ++i) {
             mbar_init(&S.full[i], 1);
             mbar_init(&S.empty[i], 1);
         }
@@ -667,7 +786,7 @@ struct HostPlan {
     std::vector<Phase> phases;
     std::vector<Proj> projs;
     int M = 0, Mp = 0, nCTA = 0, K0 = 0, NT = 1;
-    uint32_t q_bytes = 0, part_bytes = 0;
+    uint32_t ring_bytes = 0, q_bytes = 0, part_bytes = 0;
     size_t off_phases = 0, off_projs = 0, off_xstats = 0, off_partials = 0, bytes = 0;
     std::vector<size_t> off_act, off_stats;  // per projection, 0 if not consumed
 };
@@ -709,15 +828,28 @@ int choose_split(int RGT, int KT, int Mp, int nCTA, uint32_t limit) {
     return best;
 }
 
-// q cache + partial sums: what the 227 KB of shared memory leaves beside
-// the 128 KB weight ring and the small arrays.
-constexpr uint32_t kQPartLimit = 92 * 1024;
+// Shared memory: the q cache and partial sums get what the per-block limit
+// leaves beside the fixed arrays and a weight ring of at least kMinRing
+// bytes; the ring then takes the rest, up to kMaxRing.
+constexpr uint32_t kMinRing = 48 * 1024;
+constexpr uint32_t kMaxRing = 160 * 1024;
+
+int smem_optin() {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
+    return v;
+}
 
 bitlinear_status_t build_plan(int64_t M, int64_t K0, const bitlinear_chain_proj_t *projs, int32_t nproj,
                               int nCTA, HostPlan &H) {
     if (M < 1 || M > 16 || K0 < 16 || (K0 % 16) != 0 || K0 > 65536) return BITLINEAR_ERR_INVALID_ARG;
     if (!projs || nproj < 1 || nproj > 4096) return BITLINEAR_ERR_INVALID_ARG;
     if (nCTA < 1 || nCTA > kMaxCTA) return BITLINEAR_ERR_UNSUPPORTED;
+    if (nproj > kMaxProj) return BITLINEAR_ERR_UNSUPPORTED;
+    const int smax = smem_optin();
+    if (smax < static_cast<int>(smem_fixed_bytes() + kMinRing + 4096)) return BITLINEAR_ERR_UNSUPPORTED;
+    const uint32_t qpart_limit = static_cast<uint32_t>(smax) - smem_fixed_bytes() - kMinRing - 1024;
     H = HostPlan();
     H.M = static_cast<int>(M);
     H.Mp = 1;
@@ -781,7 +913,7 @@ bitlinear_status_t build_plan(int64_t M, int64_t K0, const bitlinear_chain_proj_
     // splits and limits
     uint64_t partial_words = 0;
     for (Phase &ph : H.phases) {
-        const int S = choose_split(ph.RGT, ph.KT, H.Mp, nCTA, kQPartLimit);
+        const int S = choose_split(ph.RGT, ph.KT, H.Mp, nCTA, qpart_limit);
         if (S == 0) return BITLINEAR_ERR_UNSUPPORTED;
         ph.S = S;
         ph.G = nCTA / S;
@@ -795,12 +927,16 @@ bitlinear_status_t build_plan(int64_t M, int64_t K0, const bitlinear_chain_proj_
     }
     H.q_bytes = (H.q_bytes + 127) & ~127u;
     H.part_bytes = (H.part_bytes + 127) & ~127u;
-    // workspace layout
-    size_t off = 256;  // control words
+    {
+        const uint32_t room = static_cast<uint32_t>(smax) - smem_fixed_bytes() - H.q_bytes - H.part_bytes - 1024;
+        H.ring_bytes = std::min(room, kMaxRing) & ~1023u;
+    }
+    // workspace layout: control words | phase metadata | gamma pointers | ...
+    size_t off = 256;
     H.off_phases = off;
-    off = align256(off + H.phases.size() * sizeof(Phase));
+    off = align256(off + H.phases.size() * sizeof(MetaImg));
     H.off_projs = off;
-    off = align256(off + H.projs.size() * sizeof(Proj));
+    off = align256(off + H.projs.size() * sizeof(float *));
     H.off_xstats = off;
     off = align256(off + static_cast<size_t>(nCTA) * H.Mp * 8);
     H.off_act.assign(nproj, 0);
@@ -884,7 +1020,7 @@ extern "C" bitlinear_status_t bitlinear_chain_prepare(int64_t M, int64_t K0, con
     const bitlinear_status_t st = build_plan(M, K0, projs, nproj, sm_count(), H);
     if (st != BITLINEAR_OK) return st;
     if (workspace_bytes < H.bytes) return BITLINEAR_ERR_INVALID_ARG;
-    const uint32_t smem = smem_bytes_for(H.q_bytes, H.part_bytes);
+    const uint32_t smem = smem_bytes_for(H.ring_bytes, H.q_bytes, H.part_bytes);
     int dev = 0, maxs = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&maxs, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
@@ -896,8 +1032,14 @@ extern "C" bitlinear_status_t bitlinear_chain_prepare(int64_t M, int64_t K0, con
     std::vector<uint8_t> img(H.off_xstats, 0);
     const uint32_t first_epoch = 1;  // tags of a cleared workspace (0) never match
     std::memcpy(img.data() + 8, &first_epoch, 4);
-    std::memcpy(img.data() + H.off_phases, H.phases.data(), H.phases.size() * sizeof(Phase));
-    std::memcpy(img.data() + H.off_projs, H.projs.data(), H.projs.size() * sizeof(Proj));
+    for (size_t p = 0; p < H.phases.size(); ++p) {
+        MetaImg mi{};
+        mi.ph = H.phases[p];
+        for (int j = 0; j < mi.ph.nproj; ++j) mi.pj[j] = H.projs[mi.ph.proj0 + j];
+        std::memcpy(img.data() + H.off_phases + p * sizeof(MetaImg), &mi, sizeof(MetaImg));
+    }
+    for (size_t j = 0; j < H.projs.size(); ++j)
+        std::memcpy(img.data() + H.off_projs + j * sizeof(float *), &H.projs[j].gamma, sizeof(float *));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(ws, 0, H.bytes, s) != cudaSuccess) return BITLINEAR_ERR_CUDA;
     if (cudaMemcpyAsync(ws, img.data(), img.size(), cudaMemcpyHostToDevice, s) != cudaSuccess)
@@ -912,6 +1054,7 @@ extern "C" bitlinear_status_t bitlinear_chain_prepare(int64_t M, int64_t K0, con
     plan->grid = H.nCTA;
     plan->threads = kThreads;
     plan->smem_bytes = static_cast<int32_t>(smem);
+    plan->ring_bytes = H.ring_bytes;
     plan->q_bytes = H.q_bytes;
     plan->part_bytes = H.part_bytes;
     plan->mp = H.Mp;
@@ -932,8 +1075,10 @@ extern "C" bitlinear_status_t bitlinear_chain_run(const bitlinear_chain_plan_t *
     if (bl::status_word(&status) != cudaSuccess) return BITLINEAR_ERR_CUDA;
     uint8_t *ws = static_cast<uint8_t *>(plan->workspace);
     Args A{};
-    A.phases = reinterpret_cast<const Phase *>(ws + plan->off_phases);
-    A.projs = reinterpret_cast<const Proj *>(ws + plan->off_projs);
+    A.metas = reinterpret_cast<const MetaImg *>(ws + plan->off_phases);
+    A.gammas = reinterpret_cast<const float *const *>(ws + plan->off_projs);
+    A.nproj = plan->nproj;
+    A.ring_bytes = plan->ring_bytes;
     A.x = static_cast<const __nv_bfloat16 *>(x_bf16);
     A.x_stats = reinterpret_cast<unsigned long long *>(ws + plan->off_xstats);
     A.partials = reinterpret_cast<unsigned long long *>(ws + plan->off_partials);

@@ -36,8 +36,7 @@ __device__ __forceinline__ uint32_t code_reg(uint32_t w, int p) {
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -59,6 +58,31 @@ __device__ __forceinline__ void build_b(const uint4 &q0, const uint4 &q1, uint32
         b[mu][0] = hfma2(lo, scale_c(2 * m), offset_c(2 * m));
         b[mu][1] = hfma2(hi, scale_c(2 * m + 1), offset_c(2 * m + 1));
         corr = __dp4a(static_cast<int>(qw[mu]), 0x01010101, corr);
+    }
+}
+
+// d[i][j] += (16 weight rows of row group i: one packed 16-byte lane chunk)
+// x (B fragments of token tile j), for i < nrg.  The loop order puts
+// independent accumulators next to each other so the MMAs overlap.
+template <int NT>
+__device__ __forceinline__ void mma_tile(const uint4 (&w)[4], int nrg, const uint32_t (&b)[NT][8][2],
+                                         float (&d)[4][NT][4]) {
+#pragma unroll
+    for (int P = 0; P < 2; ++P) {
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int mu = 4 * P + m;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (i < nrg) {
+                    const uint32_t X = P ? w[i].z : w[i].x, Y = P ? w[i].w : w[i].y;
+                    const uint32_t a0 = code_reg(X, 2 * m), a1 = code_reg(Y, 2 * m);
+                    const uint32_t a2 = code_reg(X, 2 * m + 1), a3 = code_reg(Y, 2 * m + 1);
+#pragma unroll
+                    for (int j = 0; j < NT; ++j) mma16816(d[i][j], a0, a1, a2, a3, b[j][mu][0], b[j][mu][1]);
+                }
+            }
+        }
     }
 }
 

@@ -245,7 +245,7 @@ typedef struct {
     uint32_t q_bytes, part_bytes;
     uint64_t off_phases, off_projs, off_xstats, off_partials;
     float eps;
-    int32_t reserved;
+    uint32_t ring_bytes;
     uint64_t magic;
 } bitlinear_chain_plan_t;
 
@@ -263,8 +263,8 @@ BITLINEAR_API size_t bitlinear_chain_workspace_bytes(int64_t M, int64_t K0,
  * plan tables on `stream` and synchronises it (a set-up call: not
  * capturable).  eps: the RMSNorm epsilon (1e-5 in the workloads).
  * Errors: INVALID_ARG (bad sizes, pointers, slot indices, workspace too
- * small), UNSUPPORTED (more than 1000 phases, more than 256 SMs, or a phase
- * that does not fit the kernel's shared memory), CUDA.
+ * small), UNSUPPORTED (more than 1024 projections or 1000 phases, more than
+ * 256 SMs, or a phase that does not fit the kernel's shared memory), CUDA.
  */
 BITLINEAR_API bitlinear_status_t bitlinear_chain_prepare(int64_t M, int64_t K0,
                                                          const bitlinear_chain_proj_t *projs,
