@@ -1,23 +1,26 @@
 """Benchmark of the BitLinear hot path on B300 (one JSON line on stdout).
 
-Workload (default): decode on 2B-shaped layers - hidden 2560, projections
-q/k/v/o 2560x2560, gate/up 2560->6912, down 6912->2560 - for M = 1, 4 and
-16 tokens.  One step runs, for each M, the seven projections of one layer
-chained through the fused RMSNorm+int8 quantiser:
-    h = quant(x); q,k,v = fwd(h); o = fwd(quant(v)); gate,up = fwd(quant(o));
-    down = fwd(quant(up))
-Every (M, projection) has its own packed weights, and steps rotate over
-ROT distinct weight sets (535 MB in total, more than 4x the 126 MB L2), so
-every weight byte is read from HBM.  Each step is one CUDA-graph replay of
-the library's calls (the kernels chain with programmatic dependent launch).
+Workload (default): one decode step of a stack of 2B-shaped layers, for
+M = 1, 4 and 16 tokens.  A layer has the seven projections q/k/v/o
+2560x2560, gate/up 2560->6912 and down 6912->2560, chained through the
+fused RMSNorm + absmax int8 quantiser:
+    h = x; q,k,v = f(h); o = f(v); gate,up = f(o); down = f(up); next x = down
+The stack has LAYERS = 20 layers: 396 MB of packed 2-bit weights, the
+0.4 GB the asi.tokyo write-up gives for the 2B model's weights, and more
+than 3x the 126 MB L2, so every weight byte is read from HBM.  Each M runs
+the whole stack as one fused decode-chain launch (bitlinear_chain_run); a
+step is the three launches, replayed as one CUDA graph.
 
-value  = algorithmic bytes of the whole step (packed weights, int8 and bf16
-         activations, scales, outputs) / device time, summed over ranks.
-e2e    = the same bytes / time of a step that also copies the step's inputs
-         from pinned host memory and reads its outputs back.
-roofline: the decode GEMV (dominant kernel) timed per launch with CUDA events.
+value  = algorithmic bytes of the step (packed weights, activations in and
+         out, scales; the same count as the unfused quant + forward calls)
+         / device time, summed over ranks.
+e2e    = the same bytes / wall time of steps that also copy each M's input
+         from pinned host memory and read the last projection's output back.
+roofline: the decode-chain kernel, bytes per launch / average launch time.
+unfused: the same stack through separate bitlinear_quant_act and
+         bitlinear_forward calls (PDL-chained, one graph), for comparison.
 prefill: the 2B prefill chain at M = 4096 (int8-exact tensor-core GEMM), TOPS.
-cpu_baseline: the CPU oracle on one full step (all three M), host cores.
+cpu_baseline: the CPU oracle on a bounded sample of the same workload.
 
 --impl reference times the CPU oracle (the reference arm of this build) on
 the same workload and prints the same kind of line.
@@ -40,7 +43,7 @@ if ROOT not in sys.path:
 METRIC = "BitLinear decode GB/s (% HBM peak) and prefill int8 TOPS, 2B-shape layers"
 WORKLOAD = "decode_2b"
 M_LIST = (1, 4, 16)
-ROT = 9
+LAYERS = 20
 FALLBACK_HBM_GBS = 6400.0
 FALLBACK_BF16_TFLOPS = 1800.0
 
@@ -140,83 +143,78 @@ def chain_plan(shapes):
     ], d
 
 
+# projection inputs within a layer (chain slots relative to the layer):
+# 0 = the layer input, i + 1 = output of the layer's projection i
+LAYER_INPUTS = [0, 0, 0, 3, 4, 4, 6]
+
+
+def layer_bytes(M, shapes):
+    """Algorithmic bytes of one layer at M tokens (unfused-path count)."""
+    plan, dims = chain_plan(shapes)
+    width = {"x": dims["q"][1]}
+    width.update({n: N for n, N, K in shapes})
+    b = 0
+    for kind, a, o in plan:
+        if kind == "quant":
+            b += algo_bytes_quant(M, width[a])
+        else:
+            N, K = dims[o]
+            b += algo_bytes_forward(M, N, K)
+    return b
+
+
 class DecodeBench:
-    def __init__(self, torch, bl, inputs, dev):
+    """The decode stack: LAYERS x 7 packed projections shared by every M."""
+
+    def __init__(self, torch, bl, inputs, dev, layers=LAYERS):
         self.torch, self.bl, self.inputs, self.dev = torch, bl, inputs, dev
         wl = inputs.WORKLOADS[WORKLOAD]
         self.shapes = wl["shapes"]
-        self.plan, self.dims = chain_plan(self.shapes)
+        self.layers = layers
         self.eps_w, self.eps_a = wl["eps_w"], wl["eps_a"]
-        hidden = self.dims["q"][1]
-        T = torch
-        # weights: ROT sets x M x projection
-        self.w = {}
-        for r in range(ROT):
-            for M in M_LIST:
-                for i, (name, N, K) in enumerate(self.shapes):
-                    seed = wl["seed"] * 100000 + r * 1000 + M * 10 + i
-                    W = inputs.weights_fp32(N, K, seed=seed, device=dev)
-                    self.w[(r, M, name)] = bl.pack_weights(W, self.eps_w)
-                    del W
-        # activation buffers per M
-        self.buf = {}
+        self.hidden = self.shapes[0][2]
+        self.w = []  # (packed, gamma, N) per projection, layer-major
+        for l in range(layers):
+            for i, (name, N, K) in enumerate(self.shapes):
+                W = inputs.weights_fp32(N, K, seed=wl["seed"] * 100000 + l * 10 + i, device=dev)
+                packed, gamma = bl.pack_weights(W, self.eps_w)
+                del W
+                self.w.append((packed, gamma, N))
+        self.packed_bytes = sum(p.numel() for p, _, _ in self.w)
+        self.x = {M: inputs.activations_bf16(M, self.hidden, seed=wl["seed"] * 7 + M, device=dev)
+                  for M in M_LIST}
+        self.chains = {}
         for M in M_LIST:
-            b = {"x": inputs.activations_bf16(M, hidden, seed=wl["seed"] * 7 + M, device=dev)}
-            for name, N, K in self.shapes:
-                b[name] = T.empty(M, N, dtype=T.bfloat16, device=dev)
-            for h, (src) in (("h0", "x"), ("h1", "v"), ("h2", "o"), ("h3", "up")):
-                K = b[src].shape[1]
-                b[h] = (T.empty(M, K, dtype=T.int8, device=dev), T.empty(M, dtype=T.float32, device=dev))
-            self.buf[M] = b
-        self.bytes_step = 0
-        self.gemv_bytes = 0
-        self.gemv_launches = 0
-        self.launches = 0
-        for M in M_LIST:
-            for kind, a, b_ in self.plan:
-                if kind == "quant":
-                    self.bytes_step += algo_bytes_quant(M, self.buf[M][a].shape[1])
-                else:
-                    N, K = self.dims[b_]
-                    self.bytes_step += algo_bytes_forward(M, N, K)
-                    self.gemv_bytes += algo_bytes_forward(M, N, K)
-                    self.gemv_launches += 1
-                self.launches += 1
+            projs = []
+            for l in range(layers):
+                base = 7 * l
+                for i, rel in enumerate(LAYER_INPUTS):
+                    slot = (base if l > 0 else 0) if rel == 0 else base + rel
+                    p, g, N = self.w[base + i]
+                    projs.append(dict(packed=p, gamma=g, N=N, input=slot))
+            self.chains[M] = bl.DecodeChain(M, self.hidden, projs, eps=self.eps_a)
+        self.bytes_per_M = {M: layer_bytes(M, self.shapes) * layers for M in M_LIST}
+        self.bytes_step = sum(self.bytes_per_M.values())
+        self.launches = len(M_LIST)
         torch.cuda.synchronize()
 
-    def run_step(self, r, kinds=("quant", "fwd")):
-        bl = self.bl
+    def run_step(self, stream, h2d=None, d2h=None):
         for M in M_LIST:
-            b = self.buf[M]
-            for kind, a, o in self.plan:
-                if kind == "quant" and "quant" in kinds:
-                    q, s = b[o]
-                    x = b[a]
-                    bl.bitlinear_quant_act(x, None, M, x.shape[1], self.eps_a, q, s)
-                elif kind == "fwd" and "fwd" in kinds:
-                    q, s = b[a]
-                    packed, gamma = self.w[(r, M, o)]
-                    N, K = self.dims[o]
-                    bl.bitlinear_forward(q, s, packed, gamma, M, N, K, b[o])
+            if h2d is not None:
+                self.x[M].copy_(h2d[M], non_blocking=True)
+            self.chains[M].run(self.x[M], stream)
+            if d2h is not None:
+                d2h[M].copy_(self.chains[M].out[-1], non_blocking=True)
 
     def capture(self, stream, h2d=None, d2h=None):
         torch = self.torch
         with torch.cuda.stream(stream):  # one eager step: host-side set-up happens outside capture
-            self.run_step(0)
+            self.run_step(stream)
         torch.cuda.synchronize()
-        graphs = []
-        for r in range(ROT):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                if h2d is not None:
-                    for M in M_LIST:
-                        self.buf[M]["x"].copy_(h2d[M], non_blocking=True)
-                self.run_step(r)
-                if d2h is not None:
-                    for M in M_LIST:
-                        d2h[M].copy_(self.buf[M]["down"], non_blocking=True)
-            graphs.append(g)
-        return graphs
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            self.run_step(stream, h2d, d2h)
+        return g
 
 
 def time_graphs(torch, graphs, steps, warmup, stream, barrier=None):
@@ -238,49 +236,46 @@ def time_graphs(torch, graphs, steps, warmup, stream, barrier=None):
     return e0.elapsed_time(e1)  # ms
 
 
-def per_kernel_times(torch, db, stream, reps=20):
-    """Average device duration of the decode GEMV and of the quantiser: each
-    is captured alone (same launches, same rotating weights, PDL between
-    kernels) and the replay time is divided by the number of launches."""
-    def graph_of(kind):
-        gs = []
-        for r in range(ROT):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                db.run_step(r, kinds=(kind,))
-            gs.append(g)
-        return gs
-
-    out = {}
-    for kind in ("fwd", "quant"):
-        gs = graph_of(kind)
-        ms = time_graphs(torch, gs, reps * ROT, ROT, stream)
-        n = sum(1 for M in M_LIST for k, _, _ in db.plan if k == kind) * reps * ROT
-        out[kind + "_avg_us"] = 1000.0 * ms / n
-        del gs
-    out["gemv_avg_bytes"] = db.gemv_bytes / db.gemv_launches
-    out["gemv_gbs"] = out["gemv_avg_bytes"] / (out["fwd_avg_us"] * 1e-6) / 1e9
-    # per shape: a graph of 9 rotating launches of one (M, projection)
-    per_shape = {}
+def unfused_step_ms(torch, bl, db, stream, reps=5):
+    """The same stack through the per-projection entry points: per layer
+    h0 = quant(x); q,k,v = fwd(h0); h1 = quant(v); o = fwd(h1);
+    h2 = quant(o); gate,up = fwd(h2); h3 = quant(up); down = fwd(h3),
+    chained with programmatic dependent launch in one CUDA graph.  Returns
+    ms per step (all M)."""
+    T = torch
+    bufs = {}
     for M in M_LIST:
-        b = db.buf[M]
-        for kind, a, o in db.plan:
-            if kind != "fwd" or o in ("k", "v", "up"):
-                continue
-            N, K = db.dims[o]
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for r in range(ROT):
-                    q, s = b[a]
-                    packed, gamma = db.w[(r, M, o)]
-                    db.bl.bitlinear_forward(q, s, packed, gamma, M, N, K, b[o])
-            ms = time_graphs(torch, [g], reps, 3, stream)
-            us = 1000.0 * ms / (reps * ROT)
-            per_shape[f"M{M}_{N}x{K}"] = {"us": round(us, 3),
-                                          "gbs": round(algo_bytes_forward(M, N, K) / (us * 1e-6) / 1e9, 1)}
-            del g
-    out["per_shape"] = per_shape
-    return out
+        outs = [T.empty(M, N, dtype=T.bfloat16, device=db.dev) for _, N, _ in db.shapes]
+        hs = [(T.empty(M, K, dtype=T.int8, device=db.dev), T.empty(M, dtype=T.float32, device=db.dev))
+              for K in (db.hidden, db.shapes[2][1], db.shapes[3][1], db.shapes[5][1])]
+        bufs[M] = (outs, hs)
+    # (projection index, quantised input index) per layer; quant steps before them
+    order = [("quant", 0, None), ("fwd", 0, 0), ("fwd", 1, 0), ("fwd", 2, 0), ("quant", 1, 2), ("fwd", 3, 1),
+             ("quant", 2, 3), ("fwd", 4, 2), ("fwd", 5, 2), ("quant", 3, 5), ("fwd", 6, 3)]
+
+    def step():
+        for M in M_LIST:
+            outs, hs = bufs[M]
+            for l in range(db.layers):
+                for kind, a, b in order:
+                    if kind == "quant":
+                        src = (db.x[M] if l == 0 else outs[6]) if a == 0 else outs[b]
+                        q, sc = hs[a]
+                        bl.bitlinear_quant_act(src, None, M, src.shape[1], db.eps_a, q, sc)
+                    else:
+                        packed, gamma, N = db.w[7 * l + a]
+                        q, sc = hs[b]
+                        bl.bitlinear_forward(q, sc, packed, gamma, M, N, q.shape[1], outs[a])
+
+    with T.cuda.stream(stream):
+        step()
+    T.cuda.synchronize()
+    g = T.cuda.CUDAGraph()
+    with T.cuda.graph(g, stream=stream):
+        step()
+    ms = time_graphs(T, [g], reps, 2, stream)
+    del g, bufs
+    return ms / reps
 
 
 def prefill_bench(torch, bl, inputs, dev, stream, steps=5, warmup=3, M=4096):
@@ -337,10 +332,11 @@ def prefill_bench(torch, bl, inputs, dev, stream, steps=5, warmup=3, M=4096):
 # ------------------------------------------------------------ CPU oracle --
 
 def oracle_step_sample(budget_s=20.0):
-    """The oracle on the decode workload: for each M, quantise, unpack the
-    packed weights, matmul and rescale, for the seven projections of one
-    layer.  Runs whole steps until `budget_s` is spent (at least one)."""
-    import numpy as np
+    """The oracle on a bounded sample of the decode workload: one layer of
+    the 2B-shape stack for each M (quantise, unpack the packed weights,
+    matmul, rescale, for the seven chained projections), repeated until
+    `budget_s` is spent (at least once).  Returns GB/s of the same
+    algorithmic bytes as the GPU line, steps, seconds, threads."""
     import oracle
     from bitlinear_02_b300 import inputs
     wl = inputs.WORKLOADS[WORKLOAD]
@@ -357,26 +353,25 @@ def oracle_step_sample(budget_s=20.0):
     xs = {M: inputs.bf16_bits(inputs.activations_bf16(M, hidden, seed=M)) for M in M_LIST}
     nbytes = 0
     t0 = time.perf_counter()
-    steps = 0
+    reps = 0
     while True:
         for M in M_LIST:
             acts = {"x": xs[M]}
             for kind, a, o in plan:
                 if kind == "quant":
                     acts[o] = oracle.quant_act(acts[a], None, wl["eps_a"])
-                    nbytes += algo_bytes_quant(M, acts[a].shape[1])
                 else:
                     q, s = acts[a]
                     N, K = dims[o]
                     wq, _ = oracle.unpack(packed[o], N, K)
                     acc = oracle.matmul(q, wq)
                     acts[o] = oracle.epilogue(acc, s, gam[o])
-                    nbytes += algo_bytes_forward(M, N, K)
-        steps += 1
+            nbytes += layer_bytes(M, shapes)
+        reps += 1
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    return nbytes / dt / 1e9, steps, dt, oracle.threads()
+    return nbytes / dt / 1e9, reps, dt, oracle.threads()
 
 
 # ------------------------------------------------------------ main --------
@@ -391,10 +386,11 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1000 * dt / steps, 2), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8/int32 (fp32 scales)", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "M": list(M_LIST), "hidden": 2560, "ffn": 6912,
-                   "projections": 7, "sample": f"{steps} whole step(s)"},
+        "config": {"workload": WORKLOAD, "M": list(M_LIST), "layers": LAYERS, "hidden": 2560, "ffn": 6912,
+                   "projections": 7, "sample": f"{steps} x one layer per M"},
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{steps} whole decode step(s) (M=1,4,16 x 7 projections) in {dt:.1f} s"},
+                         "sample": f"{steps} x one 2B-shape layer for each M=1,4,16 (7 chained projections) "
+                                   f"in {dt:.1f} s"},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -404,8 +400,8 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=6000)
-    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -432,42 +428,46 @@ def main():
     stream = torch.cuda.Stream()
 
     db = DecodeBench(torch, bl, inputs, dev)
-    graphs = db.capture(stream)
+    graph = db.capture(stream)
     sampler = ClockSampler(local)
     with sampler:
-        ms = time_graphs(torch, graphs, args.steps, args.warmup, stream, barrier)
+        ms = time_graphs(torch, [graph], args.steps, args.warmup, stream, barrier)
     clocks = sampler.summary()
     if ws > 1:
         import torch.distributed as dist
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
+    assert bl.bitlinear_check_status() == bl.OK, "a bounded wait expired during the timed steps"
     total_bytes = db.bytes_step * args.steps * ws
     value = total_bytes / (ms * 1e-3) / 1e9
-    del graphs
+    ms_step = ms / args.steps
+    del graph
 
-    # e2e: pinned host inputs copied in, outputs read back, every step
-    h2d = {M: db.buf[M]["x"].cpu().pin_memory() for M in M_LIST}
-    d2h = {M: torch.empty_like(db.buf[M]["down"], device="cpu").pin_memory() for M in M_LIST}
+    # e2e: each M's input copied from pinned host memory, the last output read back, every step
+    h2d = {M: db.x[M].cpu().pin_memory() for M in M_LIST}
+    d2h = {M: torch.empty_like(db.chains[M].out[-1], device="cpu").pin_memory() for M in M_LIST}
     g_e2e = db.capture(stream, h2d=h2d, d2h=d2h)
-    for i in range(args.warmup):
-        g_e2e[i % ROT].replay()
-    torch.cuda.synchronize()
-    n_e2e = max(10, args.steps // 2)
-    t0 = time.perf_counter()
-    for i in range(n_e2e):
-        g_e2e[i % ROT].replay()
-        torch.cuda.current_stream().synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            g_e2e.replay()
         stream.synchronize()
-        _ = float(d2h[16][0, 0])  # read the result on the host
-    e2e_s = time.perf_counter() - t0
+        n_e2e = max(10, args.steps // 4)
+        t0 = time.perf_counter()
+        for i in range(n_e2e):
+            g_e2e.replay()            # replays on `stream`, the current stream here
+            stream.synchronize()      # the step, copies included, has finished
+            _ = float(d2h[16][0, 0])  # read the result on the host
+        e2e_s = time.perf_counter() - t0
     e2e_val = db.bytes_step * n_e2e * ws / e2e_s / 1e9
     h2d_bytes = sum(t.numel() * t.element_size() for t in h2d.values())
     d2h_bytes = sum(t.numel() * t.element_size() for t in d2h.values())
     del g_e2e
 
-    kt = per_kernel_times(torch, db, stream)
-    gemv_frac = kt["gemv_gbs"] / hbm_peak
+    unf_ms = unfused_step_ms(torch, bl, db, stream)
+    launch_us = 1000.0 * ms_step / db.launches
+    bytes_launch = db.bytes_step / db.launches
+    chain_gbs = bytes_launch / (launch_us * 1e-6) / 1e9
     prefill = None
     if not args.no_prefill:
         prefill = prefill_bench(torch, bl, inputs, dev, stream)
@@ -478,31 +478,34 @@ def main():
                                             "sm_103a has no int8 tcgen05 MMA"}
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
-        gbs, steps, dt, cores = oracle_step_sample(budget_s=15.0)
+        gbs, reps, dt, cores = oracle_step_sample(budget_s=15.0)
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-               "sample": f"{steps} whole decode step(s) (M=1,4,16 x 7 projections, unpack+matmul+rescale) in {dt:.1f} s"}
+               "sample": f"{reps} x one 2B-shape layer for each M=1,4,16 (quantise, unpack, matmul, rescale; "
+                         f"7 chained projections) in {dt:.1f} s"}
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int8 x ternary -> int32 (f16 tensor-core operands, exact), bf16 out",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "M": list(M_LIST), "hidden": 2560, "ffn": 6912,
-                   "projections": "q,k,v,o 2560x2560; gate,up 2560->6912; down 6912->2560",
-                   "l2": f"inputs larger than L2: {ROT} rotating weight sets "
-                         f"({ROT * sum(db.w[(0, M, n)][0].numel() for M in M_LIST for n, _, _ in db.shapes) / 1e6:.0f} MB packed)",
-                   "bytes_per_step": db.bytes_step, "graph": "one CUDA graph per step, PDL between kernels",
+        "config": {"workload": WORKLOAD, "M": list(M_LIST), "layers": db.layers, "hidden": 2560,
+                   "ffn": 6912, "projections": "q,k,v,o 2560x2560; gate,up 2560->6912; down 6912->2560",
+                   "packed_mb": round(db.packed_bytes / 1e6, 1),
+                   "l2": "inputs larger than L2: the stack's packed weights are 3x the 126 MB L2",
+                   "bytes_per_step": db.bytes_step,
+                   "graph": "one CUDA graph per step: one fused decode-chain launch per M",
                    "parallelism": f"replicas x{ws}"},
         "hbm_frac_of_step": round(value / ws / hbm_peak, 4),
-        "roofline": {"bound": "hbm", "achieved": round(kt["gemv_gbs"], 1), "peak": round(hbm_peak, 1),
-                     "unit": "GB/s", "frac": round(gemv_frac, 4), "traffic": None,
-                     "kernel": "gemv_kernel (decode, M<=16)",
-                     "launch_avg_us": round(kt["fwd_avg_us"], 3),
-                     "algo_bytes_per_launch": round(kt["gemv_avg_bytes"]),
+        "roofline": {"bound": "hbm", "achieved": round(chain_gbs, 1), "peak": round(hbm_peak, 1),
+                     "unit": "GB/s", "frac": round(chain_gbs / hbm_peak, 4), "traffic": None,
+                     "kernel": "chain_kernel (fused decode chain, one launch = one M through the stack)",
+                     "launch_avg_us": round(launch_us, 2), "algo_bytes_per_launch": round(bytes_launch),
                      "peak_note": f"{peak_kind} HBM copy bandwidth",
-                     "method": "GEMV launches alone in CUDA graphs (PDL chained), replay time / launches"},
-        "kernels": {"quant_avg_us": round(kt["quant_avg_us"], 3), "gemv_per_shape": kt["per_shape"]},
+                     "method": "CUDA events around the timed graph replays / launches"},
+        "unfused": {"ms_per_step": round(unf_ms, 4),
+                    "value": round(db.bytes_step / (unf_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                    "mode": "bitlinear_quant_act + bitlinear_forward per projection, PDL-chained graph"},
         "prefill": prefill,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d_bytes,

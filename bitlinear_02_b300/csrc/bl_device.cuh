@@ -158,6 +158,11 @@ __device__ __forceinline__ unsigned long long ld_cg_u64(const unsigned long long
     asm volatile("ld.global.cg.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
+__device__ __forceinline__ ulonglong2 ld_cg_u64x2(const unsigned long long *p) {
+    ulonglong2 v;
+    asm volatile("ld.global.cg.v2.u64 {%0, %1}, [%2];" : "=l"(v.x), "=l"(v.y) : "l"(p) : "memory");
+    return v;
+}
 __device__ __forceinline__ void st_cg_u64(unsigned long long *p, unsigned long long v) {
     asm volatile("st.global.cg.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }

@@ -413,9 +413,8 @@ __device__ __forceinline__ void run_task(const Args &A, const Shared &S, const P
         const uint8_t *wt = chunk + (kt - t.tlo) * 512 + lane * 16;
         uint4 wv[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            wv[i] = i < nrg ? *reinterpret_cast<const uint4 *>(wt + i * per) : make_uint4(0, 0, 0, 0);
-        dm::mma_tile<NT>(wv, nrg, b, acc);
+        for (int i = 0; i < 4; ++i) wv[i] = *reinterpret_cast<const uint4 *>(wt + (i < nrg ? i : 0) * per);
+        dm::mma_tile<NT>(wv, b, acc);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.empty[d]);
@@ -596,33 +595,40 @@ __device__ void consumers(const Args &A, const Shared &S) {
                     }
                 }
             } else {
+                // pairs of tagged words (four values) per 16-byte load
                 const uint32_t in_tag = tag_of(epoch, ph.in_phase);
-                const int per = (khi - klo) / 2;
+                const int per = (khi - klo) / 4;
                 const int half = ph.K / 2;
                 const int n = M * per;
                 for (int e0 = tid; e0 < n; e0 += 8 * kConsumers) {
-                    unsigned long long v[8];
+                    ulonglong2 v[8];
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
                         const int e = e0 + u * kConsumers;
                         if (e < n)
-                            v[u] = ld_cg_u64(ph.act_in + static_cast<int64_t>(e / per) * half + klo / 2 + e % per);
+                            v[u] = ld_cg_u64x2(ph.act_in + static_cast<int64_t>(e / per) * half + klo / 2 + 2 * (e % per));
                     }
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
                         const int e = e0 + u * kConsumers;
                         if (e >= n) continue;
-                        const int m = e / per, k = klo + 2 * (e % per);
-                        if (!tag_ok(v[u], in_tag, 0xffffffffu, 32)) {
-                            v[u] = poll_tag(ph.act_in + static_cast<int64_t>(m) * half + k / 2, in_tag, 0xffffffffu, 32,
-                                            lim, A.status);
-                            ok = ok && tag_ok(v[u], in_tag, 0xffffffffu, 32);
+                        const int m = e / per, k = klo + 4 * (e % per);
+                        const unsigned long long *src = ph.act_in + static_cast<int64_t>(m) * half + k / 2;
+                        if (!tag_ok(v[u].x, in_tag, 0xffffffffu, 32)) {
+                            v[u].x = poll_tag(src, in_tag, 0xffffffffu, 32, lim, A.status);
+                            ok = ok && tag_ok(v[u].x, in_tag, 0xffffffffu, 32);
                         }
-                        const uint32_t bits = static_cast<uint32_t>(v[u]);
+                        if (!tag_ok(v[u].y, in_tag, 0xffffffffu, 32)) {
+                            v[u].y = poll_tag(src + 1, in_tag, 0xffffffffu, 32, lim, A.status);
+                            ok = ok && tag_ok(v[u].y, in_tag, 0xffffffffu, 32);
+                        }
+                        const uint32_t b0 = static_cast<uint32_t>(v[u].x), b1 = static_cast<uint32_t>(v[u].y);
                         const float c = S.c[m];
-                        const uint32_t lo = quant1(__uint_as_float(bits << 16), c);
-                        const uint32_t hi = quant1(__uint_as_float(bits & 0xffff0000u), c);
-                        *reinterpret_cast<uint16_t *>(S.qc + m * qs + (k - klo)) = static_cast<uint16_t>(lo | (hi << 8));
+                        const uint32_t q = quant1(__uint_as_float(b0 << 16), c) |
+                                           (quant1(__uint_as_float(b0 & 0xffff0000u), c) << 8) |
+                                           (quant1(__uint_as_float(b1 << 16), c) << 16) |
+                                           (quant1(__uint_as_float(b1 & 0xffff0000u), c) << 24);
+                        *reinterpret_cast<uint32_t *>(S.qc + m * qs + (k - klo)) = q;
                     }
                 }
             }

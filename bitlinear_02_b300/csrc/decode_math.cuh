@@ -62,10 +62,12 @@ __device__ __forceinline__ void build_b(const uint4 &q0, const uint4 &q1, uint32
 }
 
 // d[i][j] += (16 weight rows of row group i: one packed 16-byte lane chunk)
-// x (B fragments of token tile j), for i < nrg.  The loop order puts
-// independent accumulators next to each other so the MMAs overlap.
+// x (B fragments of token tile j), for all four row groups (a caller with
+// fewer passes a copy and discards the result: no branches in the loop).
+// The loop order puts independent accumulators next to each other so the
+// MMAs overlap.
 template <int NT>
-__device__ __forceinline__ void mma_tile(const uint4 (&w)[4], int nrg, const uint32_t (&b)[NT][8][2],
+__device__ __forceinline__ void mma_tile(const uint4 (&w)[4], const uint32_t (&b)[NT][8][2],
                                          float (&d)[4][NT][4]) {
 #pragma unroll
     for (int P = 0; P < 2; ++P) {
@@ -74,13 +76,11 @@ __device__ __forceinline__ void mma_tile(const uint4 (&w)[4], int nrg, const uin
             const int mu = 4 * P + m;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                if (i < nrg) {
-                    const uint32_t X = P ? w[i].z : w[i].x, Y = P ? w[i].w : w[i].y;
-                    const uint32_t a0 = code_reg(X, 2 * m), a1 = code_reg(Y, 2 * m);
-                    const uint32_t a2 = code_reg(X, 2 * m + 1), a3 = code_reg(Y, 2 * m + 1);
+                const uint32_t X = P ? w[i].z : w[i].x, Y = P ? w[i].w : w[i].y;
+                const uint32_t a0 = code_reg(X, 2 * m), a1 = code_reg(Y, 2 * m);
+                const uint32_t a2 = code_reg(X, 2 * m + 1), a3 = code_reg(Y, 2 * m + 1);
 #pragma unroll
-                    for (int j = 0; j < NT; ++j) mma16816(d[i][j], a0, a1, a2, a3, b[j][mu][0], b[j][mu][1]);
-                }
+                for (int j = 0; j < NT; ++j) mma16816(d[i][j], a0, a1, a2, a3, b[j][mu][0], b[j][mu][1]);
             }
         }
     }

@@ -23,7 +23,7 @@
 // distributed shared memory, and each CTA of the cluster finishes a slice
 // of the outputs.  Weight loads for the first tiles are issued before the
 // programmatic-dependent-launch wait, so they overlap the previous kernel.
-#include "bl_device.cuh"
+#include "decode_math.cuh"
 
 namespace bl {
 
@@ -32,32 +32,6 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kGroups = 4;  // 16-row groups per CTA
 constexpr int kRows = 16 * kGroups;
-
-// f16x2 constants: 2^-E(p) and -1152 * 2^-E(p) in both halves.
-__device__ __forceinline__ uint32_t scale_c(int p) {
-    constexpr uint32_t s[8] = {0x3C003C00u, 0x34003400u, 0x2C002C00u, 0x24002400u,
-                               0x1C001C00u, 0x14001400u, 0x2C002C00u, 0x24002400u};
-    return s[p];
-}
-__device__ __forceinline__ uint32_t offset_c(int p) {
-    constexpr uint32_t o[8] = {0xE480E480u, 0xDC80DC80u, 0xD480D480u, 0xCC80CC80u,
-                               0xC480C480u, 0xBC80BC80u, 0xD480D480u, 0xCC80CC80u};
-    return o[p];
-}
-// A operand register for bit pair p of a packed word (see header comment).
-__device__ __forceinline__ uint32_t code_reg(uint32_t w, int p) {
-    if (p < 6) return w & (0x00030003u << (2 * p));
-    return (w >> 8) & (0x00030003u << (2 * (p - 4)));
-}
-
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
 
 template <int NT>
 struct Stage {
@@ -117,39 +91,10 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
     for (int j = 0; j < NT; ++j) corr[j] = 0;
 
     auto compute = [&](const Stage<NT> &st) {
-        uint32_t b[8][NT][2];
+        uint32_t b[NT][8][2];
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            const uint32_t qw[8] = {st.q[j][0].x, st.q[j][0].y, st.q[j][0].z, st.q[j][0].w,
-                                    st.q[j][1].x, st.q[j][1].y, st.q[j][1].z, st.q[j][1].w};
-#pragma unroll
-            for (int mu = 0; mu < 8; ++mu) {
-                const int m = mu & 3;
-                const uint32_t x = qw[mu] ^ 0x80808080u;  // q + 128 per byte
-                const uint32_t lo = prmt(x, 0x64646464u, 0x4140u);  // f16 (1024 + u0, 1024 + u1)
-                const uint32_t hi = prmt(x, 0x64646464u, 0x4342u);
-                b[mu][j][0] = hfma2(lo, scale_c(2 * m), offset_c(2 * m));
-                b[mu][j][1] = hfma2(hi, scale_c(2 * m + 1), offset_c(2 * m + 1));
-                corr[j] = __dp4a(static_cast<int>(qw[mu]), 0x01010101, corr[j]);
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < kGroups; ++i) {
-            const uint32_t wr[4] = {st.w[i].x, st.w[i].y, st.w[i].z, st.w[i].w};
-#pragma unroll
-            for (int P = 0; P < 2; ++P) {
-                const uint32_t X = wr[2 * P], Y = wr[2 * P + 1];
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const int mu = 4 * P + m;
-                    const uint32_t a0 = code_reg(X, 2 * m), a1 = code_reg(Y, 2 * m);
-                    const uint32_t a2 = code_reg(X, 2 * m + 1), a3 = code_reg(Y, 2 * m + 1);
-#pragma unroll
-                    for (int j = 0; j < NT; ++j)
-                        mma16816(d[i][j], a0, a1, a2, a3, b[mu][j][0], b[mu][j][1]);
-                }
-            }
-        }
+        for (int j = 0; j < NT; ++j) dm::build_b(st.q[j][0], st.q[j][1], b[j], corr[j]);
+        dm::mma_tile<NT>(st.w, b, d);
     };
 
     // Two-deep software pipeline over this warp's tiles c, c+4, c+8, ...

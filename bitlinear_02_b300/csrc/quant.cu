@@ -6,12 +6,14 @@
 //
 // Per token (v_k = x_k * gain_k in fp32, exact for bf16 inputs):
 //   mx = max(max |v_k|, 1e-5f);  c = 127 / mx  (fp32);  q_k = rint(v_k * c)
-//   tok_scale = (float)(1/sqrt(sum v_k^2 / K + eps) * mx / 127)   (double)
+//   tok_scale = rms^-1 * mx / 127, rms = sqrt(sum v_k^2 / K + eps)
 // RMSNorm's positive factor cancels inside absmax, so q is decided by fp32
 // products of the raw inputs only: it is the same on every device and in
-// any reduction order.  The sum of squares is accumulated per thread as an
-// unevaluated pair of floats (two-sum plus the exact product residual),
-// then combined across threads in double.
+// any reduction order.  The sum of squares is accumulated as an unevaluated
+// pair of floats (two-sum plus the exact product residual) and combined
+// across threads the same way; the scale is then formed with correctly
+// rounded fp32 operations (B300's FP64 units are far too slow for this
+// path), within a few 1e-7 of the double-precision definition.
 #include "bl_device.cuh"
 
 namespace bl {
@@ -28,6 +30,27 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 &v, float (&f)[8]) {
     }
 }
 
+// Compensated fp32 sum: the squares of fp32 products get their exact
+// rounding residual, the additions an error-free two-sum.
+struct FF2 {
+    float hi = 0.0f, lo = 0.0f;
+    __device__ __forceinline__ void add(float p, float pe = 0.0f) {
+        const float s = __fadd_rn(hi, p);
+        const float bp = __fsub_rn(s, hi);
+        lo = __fadd_rn(lo, __fadd_rn(__fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(p, bp)), pe));
+        hi = s;
+    }
+    __device__ __forceinline__ void add(const FF2 &o) {
+        add(o.hi);
+        lo = __fadd_rn(lo, o.lo);
+    }
+    __device__ __forceinline__ void add_sq(float v) {
+        const float p = __fmul_rn(v, v);
+        add(p, __fmaf_rn(v, v, -p));
+    }
+    __device__ __forceinline__ float value() const { return __fadd_rn(hi, lo); }
+};
+
 template <bool kGain>
 __global__ void __launch_bounds__(kThreads)
     quant_act_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ gain, int64_t M,
@@ -35,7 +58,7 @@ __global__ void __launch_bounds__(kThreads)
                      int wpt) {
     pdl_launch_dependents();
     __shared__ float s_mx[kThreads / 32];
-    __shared__ double s_ss[kThreads / 32];
+    __shared__ float s_hi[kThreads / 32], s_lo[kThreads / 32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tpc = (kThreads / 32) / wpt;               // tokens per CTA
     const int64_t m = static_cast<int64_t>(blockIdx.x) * tpc + warp / wpt;
@@ -45,7 +68,8 @@ __global__ void __launch_bounds__(kThreads)
     const bool active = m < M;
     pdl_wait();
 
-    float mx = 0.0f, hi = 0.0f, lo = 0.0f;
+    float mx = 0.0f;
+    FF2 ss;
     if (active) {
         const uint4 *xr = x + m * chunks;
 #pragma unroll 4
@@ -61,34 +85,34 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 mx = fmaxf(mx, fabsf(v[j]));
-                const float p = __fmul_rn(v[j], v[j]);
-                const float e = __fmaf_rn(v[j], v[j], -p);   // exact residual of the product
-                const float s = __fadd_rn(hi, p);
-                const float bp = __fsub_rn(s, hi);
-                const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(p, bp));
-                hi = s;
-                lo = __fadd_rn(lo, __fadd_rn(err, e));
+                ss.add_sq(v[j]);
             }
         }
     }
-    double ss = static_cast<double>(hi) + static_cast<double>(lo);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        FF2 o;
+        o.hi = __shfl_xor_sync(0xffffffffu, ss.hi, off);
+        o.lo = __shfl_xor_sync(0xffffffffu, ss.lo, off);
+        ss.add(o);
     }
     if (lane == 0) {
         s_mx[warp] = mx;
-        s_ss[warp] = ss;
+        s_hi[warp] = ss.hi;
+        s_lo[warp] = ss.lo;
     }
     __syncthreads();
     if (wpt > 1) {
         const int base = (warp / wpt) * wpt;
         mx = 0.0f;
-        ss = 0.0;
+        ss = FF2();
         for (int w = 0; w < wpt; ++w) {
             mx = fmaxf(mx, s_mx[base + w]);
-            ss += s_ss[base + w];
+            FF2 o;
+            o.hi = s_hi[base + w];
+            o.lo = s_lo[base + w];
+            ss.add(o);
         }
     }
     if (!active) return;
@@ -116,8 +140,9 @@ __global__ void __launch_bounds__(kThreads)
         qr[i] = make_uint2(b[0], b[1]);
     }
     if (tid == 0) {
-        const double r = 1.0 / sqrt(ss / static_cast<double>(K) + static_cast<double>(eps));
-        tok_scale[m] = static_cast<float>(r * static_cast<double>(mx) / 127.0);
+        const float ms = __fadd_rn(__fdiv_rn(ss.value(), static_cast<float>(K)), eps);
+        const float r = __fdiv_rn(1.0f, __fsqrt_rn(ms));
+        tok_scale[m] = __fdiv_rn(__fmul_rn(r, mx), 127.0f);
     }
 }
 

@@ -156,8 +156,8 @@ BITLINEAR_API bitlinear_status_t bitlinear_pack_ternary(const int8_t *Wq, int64_
  *   q          device, int8 [M, K], 16-byte aligned.
  *   tok_scale  device, fp32 [M], 4-byte aligned.
  * q is bit-exact (no float reduction decides it); tok_scale is computed
- * with compensated sums and matches the double-precision definition to
- * about 1e-7 relative.
+ * with compensated fp32 sums and correctly rounded fp32 steps, within a few
+ * 1e-7 relative of the double-precision definition above.
  * Errors: INVALID_ARG (null/misaligned pointer, M < 0, K < 16, K % 16 != 0).
  */
 BITLINEAR_API bitlinear_status_t bitlinear_quant_act(const void *x_bf16, const void *gain_bf16, int64_t M,
