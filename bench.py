@@ -279,8 +279,10 @@ def unfused_step_ms(torch, bl, db, stream, reps=5):
 
 
 def prefill_bench(torch, bl, inputs, dev, stream, steps=5, warmup=3, M=4096):
-    """2B prefill chain at M tokens: TOPS of the tensor-core GEMM (2*M*N*K per
-    projection) and the whole chain."""
+    """2B prefill chain at M tokens (the seven projections chained through the
+    quantiser, f16-activation path: bitlinear_quant_act_f16 +
+    bitlinear_forward_f16): TOPS of the tensor-core GEMMs (2*M*N*K per
+    projection) and of the whole chain."""
     wl = inputs.WORKLOADS["prefill_2b"]
     shapes = wl["shapes"]
     plan, dims = chain_plan(shapes)
@@ -296,18 +298,18 @@ def prefill_bench(torch, bl, inputs, dev, stream, steps=5, warmup=3, M=4096):
         b[name] = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
     for h, src in (("h0", "x"), ("h1", "v"), ("h2", "o"), ("h3", "up")):
         K = b[src].shape[1]
-        b[h] = (torch.empty(M, K, dtype=torch.int8, device=dev), torch.empty(M, dtype=torch.float32, device=dev))
+        b[h] = (torch.empty(M, K, dtype=torch.float16, device=dev), torch.empty(M, dtype=torch.float32, device=dev))
     ops = sum(2 * M * dims[o][0] * dims[o][1] for k, _, o in plan if k == "fwd")
 
     def step(kinds=("quant", "fwd")):
         for kind, a, o in plan:
             if kind == "quant" and "quant" in kinds:
                 q, s = b[o]
-                bl.bitlinear_quant_act(b[a], None, M, b[a].shape[1], wl["eps_a"], q, s)
+                bl.bitlinear_quant_act_f16(b[a], None, M, b[a].shape[1], wl["eps_a"], q, s)
             elif kind == "fwd" and "fwd" in kinds:
                 q, s = b[a]
                 N, K = dims[o]
-                bl.bitlinear_forward(q, s, w[o][0], w[o][1], M, N, K, b[o])
+                bl.bitlinear_forward_f16(q, s, w[o][0], w[o][1], M, N, K, b[o])
 
     with torch.cuda.stream(stream):  # eager warm-up outside capture
         step()
@@ -317,15 +319,17 @@ def prefill_bench(torch, bl, inputs, dev, stream, steps=5, warmup=3, M=4096):
         step()
     ms = time_graphs(torch, [g], steps, warmup, stream)
     chain_tops = ops * steps / (ms * 1e-3) / 1e12
-    # GEMM alone (quantised activations already in place)
+    # GEMMs alone (quantised activations already in place)
     g2 = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g2, stream=stream):
         step(kinds=("fwd",))
     ms2 = time_graphs(torch, [g2], steps, warmup, stream)
     gemm_tops = ops * steps / (ms2 * 1e-3) / 1e12
     del w, b, g, g2
-    return {"workload": f"prefill_2b M={M}", "chain_tops": round(chain_tops, 1),
-            "gemm_tops": round(gemm_tops, 1), "gemm_ms_per_chain": round(ms2 / steps, 4),
+    return {"workload": f"prefill_2b M={M}", "path": "quant_act_f16 + forward_f16 (tensor-map activations)",
+            "chain_tops": round(chain_tops, 1), "gemm_tops": round(gemm_tops, 1),
+            "gemm_ms_per_chain": round(ms2 / steps, 4), "gemm_launches_per_chain": 7,
+            "gemm_us_per_launch": round(1000 * ms2 / steps / 7, 2),
             "tokens_per_s": round(M * steps / (ms * 1e-3), 1)}
 
 

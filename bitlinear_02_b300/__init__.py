@@ -21,6 +21,7 @@ __all__ = [
     "bitlinear_packed_bytes", "bitlinear_pack_weights", "bitlinear_pack_weights_noalloc",
     "bitlinear_pack_ternary",
     "bitlinear_quant_act", "bitlinear_forward", "bitlinear_check_status",
+    "bitlinear_quant_act_f16", "bitlinear_forward_f16", "quant_act_f16", "forward_f16",
     "bitlinear_set_wait_limit", "bitlinear_status_string", "bitlinear_version",
     "pack_weights", "pack_ternary", "quant_act", "forward", "bitlinear",
     "ChainProj", "ChainPlan", "bitlinear_chain_workspace_bytes", "bitlinear_chain_prepare",
@@ -94,6 +95,8 @@ def load_library():
     L.bitlinear_check_status.argtypes = [P]
     L.bitlinear_set_wait_limit.argtypes = [ctypes.c_uint32]
     L.bitlinear_set_wait_limit.restype = None
+    L.bitlinear_quant_act_f16.argtypes = [P, P, I64, I64, F, P, P, P]
+    L.bitlinear_forward_f16.argtypes = [P, P, P, P, I64, I64, I64, P, P, P]
     L.bitlinear_chain_workspace_bytes.argtypes = [I64, I64, ctypes.POINTER(ChainProj), ctypes.c_int32]
     L.bitlinear_chain_workspace_bytes.restype = ctypes.c_size_t
     L.bitlinear_chain_prepare.argtypes = [I64, I64, ctypes.POINTER(ChainProj), ctypes.c_int32, F, P,
@@ -103,6 +106,7 @@ def load_library():
     L.bitlinear_chain_set_split.restype = None
     for name in ("bitlinear_pack_weights", "bitlinear_pack_weights_noalloc", "bitlinear_pack_ternary", "bitlinear_quant_act",
                  "bitlinear_forward", "bitlinear_check_status", "bitlinear_chain_prepare",
+                 "bitlinear_quant_act_f16", "bitlinear_forward_f16",
                  "bitlinear_chain_run"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -181,6 +185,20 @@ def bitlinear_forward(q, tok_scale, packed, gamma, M: int, N: int, K: int, out, 
                                             int(M), int(N), int(K), _ptr(out), _ptr(acc_out),
                                             _stream(stream)),
            "bitlinear_forward")
+
+
+def bitlinear_quant_act_f16(x, gain, M: int, K: int, eps: float, q_f16, tok_scale, stream=None) -> None:
+    _check(load_library().bitlinear_quant_act_f16(_ptr(x), _ptr(gain), int(M), int(K), float(eps),
+                                                  _ptr(q_f16), _ptr(tok_scale), _stream(stream)),
+           "bitlinear_quant_act_f16")
+
+
+def bitlinear_forward_f16(q_f16, tok_scale, packed, gamma, M: int, N: int, K: int, out, acc_out=None,
+                          stream=None) -> None:
+    _check(load_library().bitlinear_forward_f16(_ptr(q_f16), _ptr(tok_scale), _ptr(packed), _ptr(gamma),
+                                                int(M), int(N), int(K), _ptr(out), _ptr(acc_out),
+                                                _stream(stream)),
+           "bitlinear_forward_f16")
 
 
 def bitlinear_check_status(stream=None) -> int:
@@ -288,6 +306,24 @@ def quant_act(x: torch.Tensor, gain: torch.Tensor | None = None, eps: float = 1e
     s = torch.empty(M, dtype=torch.float32, device=x.device)
     bitlinear_quant_act(x, gain, M, K, eps, q, s)
     return q, s
+
+
+def quant_act_f16(x: torch.Tensor, gain: torch.Tensor | None = None, eps: float = 1e-5):
+    """bf16 [M, K] -> (q as f16 [M, K], tok_scale float32 [M])."""
+    M, K = x.shape
+    q = torch.empty(M, K, dtype=torch.float16, device=x.device)
+    s = torch.empty(M, dtype=torch.float32, device=x.device)
+    bitlinear_quant_act_f16(x, gain, M, K, eps, q, s)
+    return q, s
+
+
+def forward_f16(q: torch.Tensor, tok_scale: torch.Tensor, packed: torch.Tensor, gamma: torch.Tensor,
+                N: int, out: torch.Tensor | None = None, acc_out: torch.Tensor | None = None):
+    M, K = q.shape
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=q.device)
+    bitlinear_forward_f16(q, tok_scale, packed, gamma, M, N, K, out, acc_out)
+    return out
 
 
 def forward(q: torch.Tensor, tok_scale: torch.Tensor, packed: torch.Tensor, gamma: torch.Tensor,

@@ -12,6 +12,9 @@ cudaError_t launch_gemv(const int8_t *q, const float *tok_scale, const uint8_t *
 cudaError_t launch_gemm(const int8_t *q, const float *tok_scale, const uint8_t *packed,
                         const float *gamma, int M, int N, int K, __nv_bfloat16 *out,
                         int32_t *acc_out, cudaStream_t st, uint32_t wait_limit);
+cudaError_t launch_gemm16(const void *q16, const float *tok_scale, const uint8_t *packed,
+                          const float *gamma, int M, int N, int K, __nv_bfloat16 *out,
+                          int32_t *acc_out, cudaStream_t st, uint32_t wait_limit);
 cudaError_t gemm_status(unsigned int *out, cudaStream_t st);
 
 namespace {
@@ -77,6 +80,26 @@ extern "C" bitlinear_status_t bitlinear_forward(const int8_t *q, const float *to
     else
         e = launch_gemm(q, tok_scale, packed, gamma, static_cast<int>(M), static_cast<int>(N),
                         static_cast<int>(K), out, acc_out, st, g_wait_limit.load());
+    return e == cudaSuccess ? BITLINEAR_OK : BITLINEAR_ERR_CUDA;
+}
+
+extern "C" bitlinear_status_t bitlinear_forward_f16(const void *q_f16, const float *tok_scale,
+                                                    const uint8_t *packed, const float *gamma,
+                                                    int64_t M, int64_t N, int64_t K, void *out_bf16,
+                                                    int32_t *acc_out, void *stream) {
+    using namespace bl;
+    if (M < 0 || N < 1 || K < 16 || (K % 16) != 0 || K > 65536 || N > (1ll << 30) || M > (1ll << 30))
+        return BITLINEAR_ERR_INVALID_ARG;
+    if (M == 0) return BITLINEAR_OK;
+    if (!q_f16 || !tok_scale || !packed || !gamma || !out_bf16) return BITLINEAR_ERR_INVALID_ARG;
+    if (!aligned16(q_f16) || !aligned4(tok_scale) || !aligned16(packed) || !aligned4(gamma) ||
+        !aligned16(out_bf16) || (acc_out && !aligned16(acc_out)))
+        return BITLINEAR_ERR_INVALID_ARG;
+    if ((M + 63) / 64 > 65535 || M > 0x7fffffffll) return BITLINEAR_ERR_UNSUPPORTED;
+    const cudaError_t e =
+        launch_gemm16(q_f16, tok_scale, packed, gamma, static_cast<int>(M), static_cast<int>(N),
+                      static_cast<int>(K), static_cast<__nv_bfloat16 *>(out_bf16), acc_out,
+                      static_cast<cudaStream_t>(stream), g_wait_limit.load());
     return e == cudaSuccess ? BITLINEAR_OK : BITLINEAR_ERR_CUDA;
 }
 

@@ -51,10 +51,12 @@ struct FF2 {
     __device__ __forceinline__ float value() const { return __fadd_rn(hi, lo); }
 };
 
-template <bool kGain>
+// kF16: store the quantised values as f16 (their exact integer values)
+// instead of int8, for the prefill engine's tensor-map loads.
+template <bool kGain, bool kF16>
 __global__ void __launch_bounds__(kThreads)
     quant_act_kernel(const uint4 *__restrict__ x, const uint4 *__restrict__ gain, int64_t M,
-                     int64_t K, float eps, int8_t *__restrict__ q, float *__restrict__ tok_scale,
+                     int64_t K, float eps, void *__restrict__ qout, float *__restrict__ tok_scale,
                      int wpt) {
     pdl_launch_dependents();
     __shared__ float s_mx[kThreads / 32];
@@ -119,7 +121,8 @@ __global__ void __launch_bounds__(kThreads)
     if (!(mx >= 1e-5f)) mx = 1e-5f;
     const float c = __fdiv_rn(127.0f, mx);
     const uint4 *xr = x + m * chunks;
-    uint2 *qr = reinterpret_cast<uint2 *>(q + m * K);
+    uint2 *qr = reinterpret_cast<uint2 *>(static_cast<int8_t *>(qout) + m * K);
+    uint4 *qh = reinterpret_cast<uint4 *>(static_cast<__half *>(qout) + m * K);
 #pragma unroll 4
     for (int64_t i = tid; i < chunks; i += nthr) {
         float v[8];
@@ -131,13 +134,18 @@ __global__ void __launch_bounds__(kThreads)
             for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], gv[j]);
         }
         uint32_t b[2] = {0u, 0u};
+        uint32_t h[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             int iv = __float2int_rn(__fmul_rn(v[j], c));
             iv = iv > 127 ? 127 : (iv < -128 ? -128 : iv);
             b[j >> 2] |= (static_cast<uint32_t>(iv) & 0xffu) << (8 * (j & 3));
+            h[j >> 1] |= static_cast<uint32_t>(__half_as_ushort(__int2half_rn(iv))) << (16 * (j & 1));
         }
-        qr[i] = make_uint2(b[0], b[1]);
+        if (kF16)
+            qh[i] = make_uint4(h[0], h[1], h[2], h[3]);
+        else
+            qr[i] = make_uint2(b[0], b[1]);
     }
     if (tid == 0) {
         const float ms = __fadd_rn(__fdiv_rn(ss.value(), static_cast<float>(K)), eps);
@@ -149,10 +157,10 @@ __global__ void __launch_bounds__(kThreads)
 }  // namespace
 }  // namespace bl
 
-extern "C" bitlinear_status_t bitlinear_quant_act(const void *x_bf16, const void *gain_bf16,
-                                                  int64_t M, int64_t K, float eps, int8_t *q,
-                                                  float *tok_scale, void *stream) {
-    using namespace bl;
+namespace bl {
+namespace {
+bitlinear_status_t quant_entry(const void *x_bf16, const void *gain_bf16, int64_t M, int64_t K, float eps,
+                               void *q, float *tok_scale, void *stream, bool f16) {
     if (M < 0 || K < 16 || (K % 16) != 0 || K > (1ll << 30)) return BITLINEAR_ERR_INVALID_ARG;
     if (M == 0) return BITLINEAR_OK;
     if (!x_bf16 || !q || !tok_scale) return BITLINEAR_ERR_INVALID_ARG;
@@ -165,14 +173,29 @@ extern "C" bitlinear_status_t bitlinear_quant_act(const void *x_bf16, const void
     const int64_t blocks = (M + tpc - 1) / tpc;
     if (blocks > 0x7fffffffll) return BITLINEAR_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint4 *xv = static_cast<const uint4 *>(x_bf16);
+    const uint4 *gv = static_cast<const uint4 *>(gain_bf16);
+    const dim3 grid(static_cast<unsigned>(blocks)), block(kThreads);
     cudaError_t e;
     if (gain_bf16)
-        e = launch_pdl(quant_act_kernel<true>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0,
-                       st, 1, static_cast<const uint4 *>(x_bf16),
-                       static_cast<const uint4 *>(gain_bf16), M, K, eps, q, tok_scale, wpt);
+        e = f16 ? launch_pdl(quant_act_kernel<true, true>, grid, block, 0, st, 1, xv, gv, M, K, eps, q, tok_scale, wpt)
+                : launch_pdl(quant_act_kernel<true, false>, grid, block, 0, st, 1, xv, gv, M, K, eps, q, tok_scale, wpt);
     else
-        e = launch_pdl(quant_act_kernel<false>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0,
-                       st, 1, static_cast<const uint4 *>(x_bf16),
-                       static_cast<const uint4 *>(nullptr), M, K, eps, q, tok_scale, wpt);
+        e = f16 ? launch_pdl(quant_act_kernel<false, true>, grid, block, 0, st, 1, xv, gv, M, K, eps, q, tok_scale, wpt)
+                : launch_pdl(quant_act_kernel<false, false>, grid, block, 0, st, 1, xv, gv, M, K, eps, q, tok_scale, wpt);
     return e == cudaSuccess ? BITLINEAR_OK : BITLINEAR_ERR_CUDA;
+}
+}  // namespace
+}  // namespace bl
+
+extern "C" bitlinear_status_t bitlinear_quant_act(const void *x_bf16, const void *gain_bf16,
+                                                  int64_t M, int64_t K, float eps, int8_t *q,
+                                                  float *tok_scale, void *stream) {
+    return bl::quant_entry(x_bf16, gain_bf16, M, K, eps, q, tok_scale, stream, false);
+}
+
+extern "C" bitlinear_status_t bitlinear_quant_act_f16(const void *x_bf16, const void *gain_bf16,
+                                                      int64_t M, int64_t K, float eps, void *q_f16,
+                                                      float *tok_scale, void *stream) {
+    return bl::quant_entry(x_bf16, gain_bf16, M, K, eps, q_f16, tok_scale, stream, true);
 }

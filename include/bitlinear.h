@@ -204,6 +204,30 @@ BITLINEAR_API bitlinear_status_t bitlinear_forward(const int8_t *q, const float 
                                      void *stream);
 
 /*
+ * bitlinear_quant_act with the quantised activations stored as f16 (their
+ * exact integer values, -128..127) instead of int8, for
+ * bitlinear_forward_f16.  Same q values and token scales as
+ * bitlinear_quant_act; q_f16: device f16 [M, K], 16-byte aligned.
+ * Errors as bitlinear_quant_act.
+ */
+BITLINEAR_API bitlinear_status_t bitlinear_quant_act_f16(const void *x_bf16, const void *gain_bf16,
+                                                         int64_t M, int64_t K, float eps, void *q_f16,
+                                                         float *tok_scale, void *stream);
+
+/*
+ * bitlinear_forward for f16 activations from bitlinear_quant_act_f16, any
+ * M >= 1: always the tensor-core GEMM, which then loads the activation
+ * tiles by tensor-map copy straight into the layout its MMAs read (the
+ * int8 path converts them on the fly).  Identical results to
+ * bitlinear_forward on the same values; the same weight contract.
+ * Errors: as bitlinear_forward.
+ */
+BITLINEAR_API bitlinear_status_t bitlinear_forward_f16(const void *q_f16, const float *tok_scale,
+                                                       const uint8_t *packed, const float *gamma,
+                                                       int64_t M, int64_t N, int64_t K, void *out_bf16,
+                                                       int32_t *acc_out, void *stream);
+
+/*
  * Fused decode chain: a sequence of BitLinear projections for M <= 16
  * tokens, each one quantising its input (RMSNorm + per-token absmax int8,
  * as bitlinear_quant_act with no gain) and multiplying it with its ternary

@@ -171,6 +171,56 @@ def test_prefill_gemm_parity(M, N, K):
     check_full(w, x)
 
 
+@pytest.mark.parametrize("M", [1, 17, 64, 65, 200, 300])
+@pytest.mark.parametrize("N,K", [(512, 256), (200, 8640), (144, 144), (1040, 1280)])
+def test_prefill_f16_path_parity(M, N, K):
+    """quant_act_f16 + forward_f16: the same q values, bit-exact accumulators
+    and outputs as the oracle (and the int8 path)."""
+    w = inputs.weights_fp32(N, K, seed=17 * N + K)
+    x = inputs.activations_bf16(M, K, seed=19 * M + K, outlier_frac=0.01)
+    wn = w.numpy()
+    g_ref = oracle.gamma(wn)
+    wq = oracle.ternarize(wn, g_ref, 1e-5)
+    q_ref, s_ref = oracle.quant_act(inputs.bf16_bits(x), None, 1e-5)
+    packed, gamma = gpu_pack(w)
+    q16, s = bl.quant_act_f16(x.to(DEV))
+    acc = torch.empty(M, N, dtype=torch.int32, device=DEV)
+    out = bl.forward_f16(q16, s, packed, gamma, N, acc_out=acc)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(q16.cpu().to(torch.int32).numpy(), q_ref.astype(np.int32))
+    np.testing.assert_allclose(s.cpu().numpy(), s_ref, rtol=S_TOK_RTOL, atol=0)
+    acc_ref = oracle.matmul(q_ref, wq)
+    np.testing.assert_array_equal(acc.cpu().numpy(), acc_ref)
+    np.testing.assert_array_equal(bits16(out), oracle.epilogue(acc_ref, s.cpu().numpy(), g_ref))
+
+
+def test_prefill_f16_2b_full_size_sampled():
+    M = 4096
+    wl = inputs.WORKLOADS["prefill_2b"]
+    for i, (name, N, K) in enumerate(wl["shapes"]):
+        if name not in ("gate", "down"):
+            continue
+        w = inputs.weights_fp32(N, K, seed=wl["seed"] * 100 + i)
+        x = inputs.activations_bf16(M, K, seed=wl["seed"] * 1000 + M + i, outlier_frac=0.01,
+                                    outlier_scale=20.0)
+        wn = w.numpy()
+        g_ref = oracle.gamma(wn)
+        wq = oracle.ternarize(wn, g_ref, 1e-5)
+        packed, gamma = gpu_pack(w)
+        q16, s = bl.quant_act_f16(x.to(DEV))
+        acc = torch.empty(M, N, dtype=torch.int32, device=DEV)
+        out = bl.forward_f16(q16, s, packed, gamma, N, acc_out=acc)
+        torch.cuda.synchronize()
+        q_ref, _ = oracle.quant_act(inputs.bf16_bits(x), None, 1e-5)
+        np.testing.assert_array_equal(q16.cpu().to(torch.int32).numpy(), q_ref.astype(np.int32))
+        rng = np.random.default_rng(i)
+        ms = rng.integers(0, M, 4096)
+        ns = rng.integers(0, N, 4096)
+        accn = acc.cpu().numpy()
+        np.testing.assert_array_equal(accn[ms, ns], oracle.matmul_pairs(q_ref, wq, ms, ns))
+        np.testing.assert_array_equal(bits16(out), oracle.epilogue(accn, s.cpu().numpy(), g_ref))
+
+
 def test_layer_small_workload():
     wl = inputs.WORKLOADS["layer_small"]
     _, N, K = wl["shapes"][0]
