@@ -401,6 +401,75 @@ def run_reference(args):
     return 0
 
 
+def profile_gemm(spec):
+    """--profile-gemm N,K,M[,int8]: one prefill GEMM shape, 3 warm-up + 20
+    timed calls (the driver for ncu captures of the GEMM kernels)."""
+    import torch
+    import bitlinear_02_b300 as bl
+    from bitlinear_02_b300 import inputs
+    parts = spec.split(",")
+    N, K, M = (int(v) for v in parts[:3])
+    f16 = not (len(parts) > 3 and parts[3] == "int8")
+    dev = torch.device("cuda:0")
+    w = inputs.weights_fp32(N, K, seed=1, device=dev)
+    packed, gamma = bl.pack_weights(w, 1e-5)
+    x = inputs.activations_bf16(M, K, seed=2, device=dev)
+    q, s = bl.quant_act_f16(x) if f16 else bl.quant_act(x)
+    fwd = bl.forward_f16 if f16 else bl.forward
+    out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    for _ in range(3):
+        fwd(q, s, packed, gamma, N, out=out)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(20):
+        fwd(q, s, packed, gamma, N, out=out)
+    e1.record()
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / 20
+    assert bl.bitlinear_check_status() == bl.OK
+    print(json.dumps({"profile": "gemm", "N": N, "K": K, "M": M, "activations": "f16" if f16 else "int8",
+                      "us": round(ms * 1000, 2), "tflops": round(2 * M * N * K / ms / 1e9, 1)}))
+    return 0
+
+
+def profile_chain(spec):
+    """--profile-chain L,M: the decode chain on an L-layer 2B-shape stack at
+    M tokens, 3 warm-up + 10 timed runs (driver for ncu captures)."""
+    import torch
+    import bitlinear_02_b300 as bl
+    from bitlinear_02_b300 import inputs
+    L, M = (int(v) for v in spec.split(","))
+    dev = torch.device("cuda:0")
+    shapes = inputs.WORKLOADS[WORKLOAD]["shapes"]
+    hidden = shapes[0][2]
+    projs = []
+    for l in range(L):
+        for i, rel in enumerate(LAYER_INPUTS):
+            _, N, K = shapes[i]
+            wq = inputs.ternary(N, K, seed=l * 10 + i, device=dev)
+            packed = bl.pack_ternary(wq)
+            slot = (7 * l if l > 0 else 0) if rel == 0 else 7 * l + rel
+            projs.append(dict(packed=packed, gamma=torch.tensor([0.02], device=dev), N=N, input=slot))
+    dc = bl.DecodeChain(M, hidden, projs)
+    x = inputs.activations_bf16(M, hidden, seed=M, device=dev)
+    for _ in range(3):
+        dc.run(x)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(10):
+        dc.run(x)
+    e1.record()
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / 10
+    assert bl.bitlinear_check_status() == bl.OK
+    wb = sum(p["packed"].numel() for p in projs)
+    print(json.dumps({"profile": "chain", "layers": L, "M": M, "us": round(ms * 1000, 2),
+                      "weight_gbs": round(wb / (ms * 1e-3) / 1e9, 1)}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -409,7 +478,13 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--profile-gemm", default=None, help="N,K,M[,int8]: time one GEMM shape (ncu driver)")
+    ap.add_argument("--profile-chain", default=None, help="L,M: time the decode chain (ncu driver)")
     args = ap.parse_args()
+    if args.profile_gemm:
+        return profile_gemm(args.profile_gemm)
+    if args.profile_chain:
+        return profile_chain(args.profile_chain)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
