@@ -8,17 +8,22 @@ fused RMSNorm + absmax int8 quantiser:
 The stack has LAYERS = 20 layers: 396 MB of packed 2-bit weights, the
 0.4 GB the asi.tokyo write-up gives for the 2B model's weights, and more
 than 3x the 126 MB L2, so every weight byte is read from HBM.  Each M runs
-the whole stack as one fused decode-chain launch (bitlinear_chain_run); a
-step is the three launches, replayed as one CUDA graph.
+the whole stack; a step is all of it for the three M, replayed as one CUDA
+graph.
+
+The step runs the fused decode path: per M one bitlinear_act_stats of the
+stack input, then per layer four bitlinear_forward_fused launches
+(q,k,v | o | gate,up | down), each quantising its input on the fly.
 
 value  = algorithmic bytes of the step (packed weights, activations in and
          out, scales; the same count as the unfused quant + forward calls)
          / device time, summed over ranks.
 e2e    = the same bytes / wall time of steps that also copy each M's input
          from pinned host memory and read the last projection's output back.
-roofline: the decode-chain kernel, bytes per launch / average launch time.
-unfused: the same stack through separate bitlinear_quant_act and
-         bitlinear_forward calls (PDL-chained, one graph), for comparison.
+roofline: the fused decode GEMV, bytes per launch / average launch time.
+chain, unfused: the same stack through the persistent fused-chain kernel
+         (bitlinear_chain_run, one launch per M) and through separate
+         bitlinear_quant_act + bitlinear_forward calls, for comparison.
 prefill: the 2B prefill chain at M = 4096 (int8-exact tensor-core GEMM), TOPS.
 cpu_baseline: the CPU oracle on a bounded sample of the same workload.
 
@@ -278,6 +283,61 @@ def unfused_step_ms(torch, bl, db, stream, reps=5):
     return ms / reps
 
 
+class FusedDecode:
+    """The decode stack through the fused path: per M one bitlinear_act_stats
+    of the stack input, then per layer four bitlinear_forward_fused launches
+    (q,k,v | o | gate,up | down), each quantising its input on the fly."""
+
+    def __init__(self, torch, bl, db):
+        self.torch, self.bl, self.db = torch, bl, db
+        T = torch
+        self.bufs = {}
+        for M in M_LIST:
+            outs = [[T.empty(M, N, dtype=T.bfloat16, device=db.dev) for _, N, _ in db.shapes]
+                    for _ in range(db.layers)]
+            stats = [[bl.new_stats(db.dev) for _ in range(4)] for _ in range(db.layers)]  # v, o, up, down
+            x_stats = bl.new_stats(db.dev)
+            self.bufs[M] = (outs, stats, x_stats)
+
+    def run_step(self, stream, h2d=None, d2h=None):
+        bl, db = self.bl, self.db
+        for M in M_LIST:
+            outs, stats, x_stats = self.bufs[M]
+            if h2d is not None:
+                db.x[M].copy_(h2d[M], non_blocking=True)
+            bl.bitlinear_act_stats(db.x[M], M, db.hidden, db.eps_a, x_stats, stream)
+            for l in range(db.layers):
+                o = outs[l]
+                st_v, st_o, st_up, st_down = stats[l]
+                x = db.x[M] if l == 0 else outs[l - 1][6]
+                xs = x_stats if l == 0 else stats[l - 1][3]
+
+                def fp(i, st=None):
+                    packed, gamma, N = db.w[7 * l + i]
+                    return bl.FusedProj(packed.data_ptr(), gamma.data_ptr(), N, o[i].data_ptr(), None,
+                                        st.data_ptr() if st is not None else None)
+
+                K = db.hidden
+                bl.bitlinear_forward_fused(x, xs, M, K, [fp(0), fp(1), fp(2, st_v)], db.eps_a, stream)
+                bl.bitlinear_forward_fused(o[2], st_v, M, o[2].shape[1], [fp(3, st_o)], db.eps_a, stream)
+                bl.bitlinear_forward_fused(o[3], st_o, M, o[3].shape[1], [fp(4), fp(5, st_up)], db.eps_a, stream)
+                bl.bitlinear_forward_fused(o[5], st_up, M, o[5].shape[1], [fp(6, st_down)], db.eps_a, stream)
+            if d2h is not None:
+                d2h[M].copy_(outs[-1][6], non_blocking=True)
+
+    def capture(self, stream, h2d=None, d2h=None):
+        torch = self.torch
+        with torch.cuda.stream(stream):
+            self.run_step(stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            self.run_step(stream, h2d, d2h)
+        return g
+
+    launches = len(M_LIST) * (1 + 4 * LAYERS)
+
+
 def prefill_bench(torch, bl, inputs, dev, stream, steps=5, warmup=3, M=4096):
     """2B prefill chain at M tokens (the seven projections chained through the
     quantiser, f16-activation path: bitlinear_quant_act_f16 +
@@ -507,7 +567,8 @@ def main():
     stream = torch.cuda.Stream()
 
     db = DecodeBench(torch, bl, inputs, dev)
-    graph = db.capture(stream)
+    fd = FusedDecode(torch, bl, db)
+    graph = fd.capture(stream)
     sampler = ClockSampler(local)
     with sampler:
         ms = time_graphs(torch, [graph], args.steps, args.warmup, stream, barrier)
@@ -526,7 +587,7 @@ def main():
     # e2e: each M's input copied from pinned host memory, the last output read back, every step
     h2d = {M: db.x[M].cpu().pin_memory() for M in M_LIST}
     d2h = {M: torch.empty_like(db.chains[M].out[-1], device="cpu").pin_memory() for M in M_LIST}
-    g_e2e = db.capture(stream, h2d=h2d, d2h=d2h)
+    g_e2e = fd.capture(stream, h2d=h2d, d2h=d2h)
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
             g_e2e.replay()
@@ -543,10 +604,14 @@ def main():
     d2h_bytes = sum(t.numel() * t.element_size() for t in d2h.values())
     del g_e2e
 
+    g_chain = db.capture(stream)
+    chain_ms = time_graphs(torch, [g_chain], max(20, args.steps // 10), 3, stream) / max(20, args.steps // 10)
+    del g_chain
     unf_ms = unfused_step_ms(torch, bl, db, stream)
-    launch_us = 1000.0 * ms_step / db.launches
-    bytes_launch = db.bytes_step / db.launches
-    chain_gbs = bytes_launch / (launch_us * 1e-6) / 1e9
+    n_fused = FusedDecode.launches  # act_stats + 4 fused GEMVs per layer, per M
+    launch_us = 1000.0 * ms_step / n_fused
+    bytes_launch = db.bytes_step / n_fused
+    fused_gbs = bytes_launch / (launch_us * 1e-6) / 1e9
     prefill = None
     if not args.no_prefill:
         prefill = prefill_bench(torch, bl, inputs, dev, stream)
@@ -573,15 +638,18 @@ def main():
                    "packed_mb": round(db.packed_bytes / 1e6, 1),
                    "l2": "inputs larger than L2: the stack's packed weights are 3x the 126 MB L2",
                    "bytes_per_step": db.bytes_step,
-                   "graph": "one CUDA graph per step: one fused decode-chain launch per M",
+                   "graph": "one CUDA graph per step: per M one act_stats + 4 fused GEMV launches per layer",
                    "parallelism": f"replicas x{ws}"},
         "hbm_frac_of_step": round(value / ws / hbm_peak, 4),
-        "roofline": {"bound": "hbm", "achieved": round(chain_gbs, 1), "peak": round(hbm_peak, 1),
-                     "unit": "GB/s", "frac": round(chain_gbs / hbm_peak, 4), "traffic": None,
-                     "kernel": "chain_kernel (fused decode chain, one launch = one M through the stack)",
+        "roofline": {"bound": "hbm", "achieved": round(fused_gbs, 1), "peak": round(hbm_peak, 1),
+                     "unit": "GB/s", "frac": round(fused_gbs / hbm_peak, 4), "traffic": None,
+                     "kernel": "fused_gemv_kernel (decode GEMV with the quantiser folded in)",
                      "launch_avg_us": round(launch_us, 2), "algo_bytes_per_launch": round(bytes_launch),
                      "peak_note": f"{peak_kind} HBM copy bandwidth",
-                     "method": "CUDA events around the timed graph replays / launches"},
+                     "method": "CUDA events around the timed graph replays / launches in the step"},
+        "chain": {"ms_per_step": round(chain_ms, 4),
+                  "value": round(db.bytes_step / (chain_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                  "mode": "persistent fused-chain kernel, one launch per M through the whole stack"},
         "unfused": {"ms_per_step": round(unf_ms, 4),
                     "value": round(db.bytes_step / (unf_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                     "mode": "bitlinear_quant_act + bitlinear_forward per projection, PDL-chained graph"},
@@ -590,7 +658,7 @@ def main():
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d_bytes,
                 "d2h_bytes_per_step": d2h_bytes,
                 "mode": "graph replay of the public API calls incl. pinned H2D/D2H copies, host sync per step"},
-        "gpu_launches": db.launches * args.steps,
+        "gpu_launches": n_fused * args.steps,
         "clocks": clocks,
     }
     if rank == 0:

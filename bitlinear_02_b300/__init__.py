@@ -24,6 +24,7 @@ __all__ = [
     "bitlinear_quant_act_f16", "bitlinear_forward_f16", "quant_act_f16", "forward_f16",
     "bitlinear_set_wait_limit", "bitlinear_status_string", "bitlinear_version",
     "pack_weights", "pack_ternary", "quant_act", "forward", "bitlinear",
+    "FusedProj", "bitlinear_fused_stats_bytes", "bitlinear_act_stats", "bitlinear_forward_fused",
     "ChainProj", "ChainPlan", "bitlinear_chain_workspace_bytes", "bitlinear_chain_prepare",
     "bitlinear_chain_run", "bitlinear_chain_set_split", "DecodeChain",
 ]
@@ -36,6 +37,12 @@ ERR_INVALID_ARG = 1
 ERR_UNSUPPORTED = 2
 ERR_CUDA = 3
 ERR_TIMEOUT = 4
+
+
+class FusedProj(ctypes.Structure):
+    """bitlinear_fused_proj_t: one projection of a fused decode GEMV launch."""
+    _fields_ = [("packed", ctypes.c_void_p), ("gamma", ctypes.c_void_p), ("N", ctypes.c_int64),
+                ("out_bf16", ctypes.c_void_p), ("acc_out", ctypes.c_void_p), ("stats", ctypes.c_void_p)]
 
 
 class ChainProj(ctypes.Structure):
@@ -96,6 +103,10 @@ def load_library():
     L.bitlinear_set_wait_limit.argtypes = [ctypes.c_uint32]
     L.bitlinear_set_wait_limit.restype = None
     L.bitlinear_quant_act_f16.argtypes = [P, P, I64, I64, F, P, P, P]
+    L.bitlinear_fused_stats_bytes.argtypes = []
+    L.bitlinear_fused_stats_bytes.restype = ctypes.c_size_t
+    L.bitlinear_act_stats.argtypes = [P, I64, I64, F, P, P]
+    L.bitlinear_forward_fused.argtypes = [P, P, I64, I64, ctypes.c_int32, ctypes.POINTER(FusedProj), F, P]
     L.bitlinear_forward_f16.argtypes = [P, P, P, P, I64, I64, I64, P, P, P]
     L.bitlinear_chain_workspace_bytes.argtypes = [I64, I64, ctypes.POINTER(ChainProj), ctypes.c_int32]
     L.bitlinear_chain_workspace_bytes.restype = ctypes.c_size_t
@@ -106,7 +117,8 @@ def load_library():
     L.bitlinear_chain_set_split.restype = None
     for name in ("bitlinear_pack_weights", "bitlinear_pack_weights_noalloc", "bitlinear_pack_ternary", "bitlinear_quant_act",
                  "bitlinear_forward", "bitlinear_check_status", "bitlinear_chain_prepare",
-                 "bitlinear_quant_act_f16", "bitlinear_forward_f16",
+                 "bitlinear_quant_act_f16", "bitlinear_forward_f16", "bitlinear_act_stats",
+                 "bitlinear_forward_fused",
                  "bitlinear_chain_run"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -199,6 +211,29 @@ def bitlinear_forward_f16(q_f16, tok_scale, packed, gamma, M: int, N: int, K: in
                                                 int(M), int(N), int(K), _ptr(out), _ptr(acc_out),
                                                 _stream(stream)),
            "bitlinear_forward_f16")
+
+
+def bitlinear_fused_stats_bytes() -> int:
+    return int(load_library().bitlinear_fused_stats_bytes())
+
+
+def bitlinear_act_stats(x, M: int, K: int, eps: float, stats, stream=None) -> None:
+    _check(load_library().bitlinear_act_stats(_ptr(x), int(M), int(K), float(eps), _ptr(stats),
+                                              _stream(stream)),
+           "bitlinear_act_stats")
+
+
+def bitlinear_forward_fused(x, x_stats, M: int, K: int, projs, eps: float = 1e-5, stream=None) -> None:
+    """projs: list of FusedProj (up to 4) sharing the input x."""
+    arr = (FusedProj * len(projs))(*projs)
+    _check(load_library().bitlinear_forward_fused(_ptr(x), _ptr(x_stats), int(M), int(K), len(projs), arr,
+                                                  float(eps), _stream(stream)),
+           "bitlinear_forward_fused")
+
+
+def new_stats(device="cuda"):
+    """A zeroed factor buffer for the fused decode path."""
+    return torch.zeros(bitlinear_fused_stats_bytes(), dtype=torch.uint8, device=device)
 
 
 def bitlinear_check_status(stream=None) -> int:

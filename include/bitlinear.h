@@ -228,6 +228,51 @@ BITLINEAR_API bitlinear_status_t bitlinear_forward_f16(const void *q_f16, const 
                                                        int32_t *acc_out, void *stream);
 
 /*
+ * Fused decode path (M <= 16): the activation quantiser folded into the
+ * decode GEMV (cheatsheet.md "BitNet b1.58とは？": every BitLinear input is
+ * quantised per token by its absolute maximum and rescaled by its RMS).
+ *
+ * A "factor buffer" (bitlinear_fused_stats_bytes() bytes, device, 16-byte
+ * aligned) carries, for an activation matrix [M, K] in bf16, each token's
+ * c = 127 / max(max_k |v|, 1e-5) and tok_scale = rms^-1 * max / 127 (rms =
+ * sqrt(sum v^2 / K + eps)), plus an accumulator that its producer reduces
+ * through.  Zero a factor buffer once (cudaMemset) before its first use;
+ * every call leaves it ready for the next.
+ *
+ *   bitlinear_act_stats       factors of an input x (bf16 [M, K]) into stats.
+ *   bitlinear_forward_fused   for up to 4 projections j sharing the input x
+ *                             (with its factors x_stats): q = clamp(rint(
+ *                             x * c), -128, 127) (bit-identical to
+ *                             bitlinear_quant_act), acc = sum q * Wq (exact
+ *                             int32), out_j = bf16(acc * (gamma_j *
+ *                             tok_scale)); and, if stats_j is given, out_j's
+ *                             own factors for the next projection.  The
+ *                             token scales of stats_j sum squares with fp32
+ *                             atomics (order varies): they agree with the
+ *                             definition to about 1e-7, not bit for bit.
+ * x_stats must not be one of the stats_j.  Weights follow the static-weight
+ * contract of bitlinear_forward.  1 <= M <= 16, K % 16 == 0, K <= 65536.
+ * Errors: INVALID_ARG (sizes, pointers, alignment), UNSUPPORTED (too many
+ * row blocks), CUDA.
+ */
+typedef struct {
+    const uint8_t *packed;  /* device: packed weights of an [N, K] matrix */
+    const float *gamma;     /* device: its scale (one float) */
+    int64_t N;              /* output features, 1 <= N <= 2^24 */
+    void *out_bf16;         /* device bf16 [M, N], 16-byte aligned */
+    int32_t *acc_out;       /* device int32 [M, N] or NULL (exact accumulators) */
+    void *stats;            /* device factor buffer for out, or NULL */
+} bitlinear_fused_proj_t;
+
+BITLINEAR_API size_t bitlinear_fused_stats_bytes(void);
+BITLINEAR_API bitlinear_status_t bitlinear_act_stats(const void *x_bf16, int64_t M, int64_t K, float eps,
+                                                     void *stats, void *stream);
+BITLINEAR_API bitlinear_status_t bitlinear_forward_fused(const void *x_bf16, const void *x_stats,
+                                                         int64_t M, int64_t K, int32_t nproj,
+                                                         const bitlinear_fused_proj_t *projs, float eps,
+                                                         void *stream);
+
+/*
  * Fused decode chain: a sequence of BitLinear projections for M <= 16
  * tokens, each one quantising its input (RMSNorm + per-token absmax int8,
  * as bitlinear_quant_act with no gain) and multiplying it with its ternary
