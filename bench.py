@@ -321,7 +321,10 @@ class FusedDecode:
                 bl.bitlinear_forward_fused(x, xs, M, K, [fp(0), fp(1), fp(2, st_v)], db.eps_a, stream)
                 bl.bitlinear_forward_fused(o[2], st_v, M, o[2].shape[1], [fp(3, st_o)], db.eps_a, stream)
                 bl.bitlinear_forward_fused(o[3], st_o, M, o[3].shape[1], [fp(4), fp(5, st_up)], db.eps_a, stream)
-                bl.bitlinear_forward_fused(o[5], st_up, M, o[5].shape[1], [fp(6, st_down)], db.eps_a, stream)
+                # the last layer's output feeds nothing here: no factors for it
+                last = l == db.layers - 1
+                bl.bitlinear_forward_fused(o[5], st_up, M, o[5].shape[1], [fp(6, None if last else st_down)],
+                                           db.eps_a, stream)
             if d2h is not None:
                 d2h[M].copy_(outs[-1][6], non_blocking=True)
 

@@ -25,6 +25,7 @@ __all__ = [
     "bitlinear_set_wait_limit", "bitlinear_status_string", "bitlinear_version",
     "pack_weights", "pack_ternary", "quant_act", "forward", "bitlinear",
     "FusedProj", "bitlinear_fused_stats_bytes", "bitlinear_act_stats", "bitlinear_forward_fused",
+    "bitlinear_fused_factors", "fused_factors", "new_stats",
     "ChainProj", "ChainPlan", "bitlinear_chain_workspace_bytes", "bitlinear_chain_prepare",
     "bitlinear_chain_run", "bitlinear_chain_set_split", "DecodeChain",
 ]
@@ -37,6 +38,7 @@ ERR_INVALID_ARG = 1
 ERR_UNSUPPORTED = 2
 ERR_CUDA = 3
 ERR_TIMEOUT = 4
+ERR_STATE = 5
 
 
 class FusedProj(ctypes.Structure):
@@ -107,6 +109,7 @@ def load_library():
     L.bitlinear_fused_stats_bytes.restype = ctypes.c_size_t
     L.bitlinear_act_stats.argtypes = [P, I64, I64, F, P, P]
     L.bitlinear_forward_fused.argtypes = [P, P, I64, I64, ctypes.c_int32, ctypes.POINTER(FusedProj), F, P]
+    L.bitlinear_fused_factors.argtypes = [P, I64, I64, F, ctypes.c_int32, P, P, P]
     L.bitlinear_forward_f16.argtypes = [P, P, P, P, I64, I64, I64, P, P, P]
     L.bitlinear_chain_workspace_bytes.argtypes = [I64, I64, ctypes.POINTER(ChainProj), ctypes.c_int32]
     L.bitlinear_chain_workspace_bytes.restype = ctypes.c_size_t
@@ -118,7 +121,7 @@ def load_library():
     for name in ("bitlinear_pack_weights", "bitlinear_pack_weights_noalloc", "bitlinear_pack_ternary", "bitlinear_quant_act",
                  "bitlinear_forward", "bitlinear_check_status", "bitlinear_chain_prepare",
                  "bitlinear_quant_act_f16", "bitlinear_forward_f16", "bitlinear_act_stats",
-                 "bitlinear_forward_fused",
+                 "bitlinear_forward_fused", "bitlinear_fused_factors",
                  "bitlinear_chain_run"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -231,13 +234,28 @@ def bitlinear_forward_fused(x, x_stats, M: int, K: int, projs, eps: float = 1e-5
            "bitlinear_forward_fused")
 
 
+def bitlinear_fused_factors(stats, M: int, K: int, eps: float, consume: bool, c_out, ts_out,
+                            stream=None) -> None:
+    _check(load_library().bitlinear_fused_factors(_ptr(stats), int(M), int(K), float(eps), 1 if consume else 0,
+                                                  _ptr(c_out), _ptr(ts_out), _stream(stream)),
+           "bitlinear_fused_factors")
+
+
+def fused_factors(stats, M: int, K: int, eps: float = 1e-5, consume: bool = False, stream=None):
+    """(c, tok_scale) of a factor buffer as device fp32 [M] tensors."""
+    c = torch.empty(M, dtype=torch.float32, device=stats.device)
+    ts = torch.empty(M, dtype=torch.float32, device=stats.device)
+    bitlinear_fused_factors(stats, M, K, eps, consume, c, ts, stream)
+    return c, ts
+
+
 def new_stats(device="cuda"):
     """A zeroed factor buffer for the fused decode path."""
     return torch.zeros(bitlinear_fused_stats_bytes(), dtype=torch.uint8, device=device)
 
 
 def bitlinear_check_status(stream=None) -> int:
-    """Returns the status code (OK or ERR_TIMEOUT); does not raise."""
+    """Returns the status code (OK, ERR_STATE or ERR_TIMEOUT); does not raise."""
     return int(load_library().bitlinear_check_status(_stream(stream)))
 
 

@@ -42,6 +42,7 @@ extern "C" const char *bitlinear_status_string(int status) {
         case BITLINEAR_ERR_UNSUPPORTED: return "unsupported device or shape";
         case BITLINEAR_ERR_CUDA: return "CUDA runtime error";
         case BITLINEAR_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
+        case BITLINEAR_ERR_STATE: return "a pending factor buffer was produced into again";
         default: return "unknown status";
     }
 }
@@ -106,5 +107,7 @@ extern "C" bitlinear_status_t bitlinear_forward_f16(const void *q_f16, const flo
 extern "C" bitlinear_status_t bitlinear_check_status(void *stream) {
     unsigned int v = 0;
     if (bl::gemm_status(&v, static_cast<cudaStream_t>(stream)) != cudaSuccess) return BITLINEAR_ERR_CUDA;
-    return v ? BITLINEAR_ERR_TIMEOUT : BITLINEAR_OK;
+    // bit 0: a bounded wait gave up; bit 1: a pending factor buffer was produced into
+    if (v & 1u) return BITLINEAR_ERR_TIMEOUT;
+    return v ? BITLINEAR_ERR_STATE : BITLINEAR_OK;
 }

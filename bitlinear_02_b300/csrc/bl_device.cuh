@@ -163,6 +163,16 @@ __device__ __forceinline__ ulonglong2 ld_cg_u64x2(const unsigned long long *p) {
     asm volatile("ld.global.cg.v2.u64 {%0, %1}, [%2];" : "=l"(v.x), "=l"(v.y) : "l"(p) : "memory");
     return v;
 }
+// Bulk prefetch of a global range into L2 (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ unsigned ld_cg_u32(const void *p) {
+    unsigned v;
+    asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ float ld_cg_f32(const void *p) { return __uint_as_float(ld_cg_u32(p)); }
 __device__ __forceinline__ void st_cg_u64(unsigned long long *p, unsigned long long v) {
     asm volatile("st.global.cg.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }

@@ -213,7 +213,7 @@ __device__ __noinline__ unsigned long long poll_tag(const unsigned long long *p,
         __nanosleep(32);
         const unsigned long long v = ld_cg_u64(p);
         if (static_cast<uint32_t>(v >> shift & mask) == want) return v;
-        if ((i & 63u) == 63u && ld_relaxed_u32(status) != 0u) break;
+        if ((i & 63u) == 63u && (ld_relaxed_u32(status) & 1u) != 0u) break;  // another CTA gave up
     }
     return 0ull;
 }
@@ -504,7 +504,7 @@ __device__ void consumers(const Args &A, const Shared &S) {
                     ok = true;
                     break;
                 }
-                if ((i & 63u) == 63u && ld_relaxed_u32(A.status) != 0u) break;
+                if ((i & 63u) == 63u && (ld_relaxed_u32(A.status) & 1u) != 0u) break;
             }
             if (!ok) raise_abort(S, A.status);
         }

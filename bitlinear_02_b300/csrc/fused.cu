@@ -6,38 +6,46 @@
 // dependent launches (four quantisers, seven GEMVs), each bound by launch
 // latency.  Here the quantiser disappears into the GEMVs:
 //   - the producer of an activation (a fused GEMV, or bitlinear_act_stats
-//     for the layer input) leaves, next to it, the per-token quantisation
-//     factors c = 127/max|v| and tok_scale = rms^-1 * max / 127;
-//   - a fused GEMV reads its bf16 input and those factors, quantises its
-//     K-slice in registers while loading it (q = rint(v * c), exactly as
-//     bitlinear_quant_act), and runs the decode GEMV arithmetic
-//     (decode_math.cuh) on up to four projections that share the input in
-//     one launch (q/k/v, gate/up);
-//   - its epilogue folds the outputs' per-token max |v| (atomicMax on the bit
-//     pattern: exact) and sum v^2 (fp32 atomics: order varies, so the token
-//     scale may vary in its last bits, well inside 1e-6) into a small
-//     accumulator; the last CTA of the projection (fence + counter) turns it
-//     into the next factors and clears it.
+//     for the layer input) leaves, next to it, what its consumer needs to
+//     quantise it: a fused GEMV folds its outputs' per-token max |v|
+//     (atomicMax on the bit pattern: exact) and sum v^2 (fp32 atomics) into
+//     a small accumulator of 16 copies and marks it pending; nothing else
+//     waits at the end of the producer;
+//   - a fused GEMV, right after its dependency wait, reduces the input's 16
+//     accumulator copies in a fixed shuffle tree (every CTA computes the
+//     same bits) to c = 127/max|x| and tok_scale = rms^-1 * max / 127,
+//     reads its bf16 input, quantises its K-slice in registers (q =
+//     rint(x * c), exactly as bitlinear_quant_act) and runs the decode GEMV
+//     arithmetic (decode_math.cuh) for up to four projections that share the
+//     input (q/k/v, gate/up);
+//   - each consuming CTA takes a ticket once it has read the accumulator;
+//     the last one writes the factors into the buffer and clears the
+//     accumulator for the next production.  Later launches reading the same
+//     buffer use those factors.
 // A decode layer becomes four launches, chained with programmatic dependent
 // launch.  q and the int32 accumulators are bit-identical to the unfused
 // path; the token scale agrees to about 1e-7.
 #include "decode_math.cuh"
 
 namespace bl {
+cudaError_t status_word(unsigned int **dev_ptr);  // gemm.cu: the library's device status word
 namespace {
 
 constexpr int kWarps = 4;
 constexpr int kGroups = 4;  // 16-row groups per CTA
 constexpr int kRows = 16 * kGroups;
 constexpr int kMaxFused = 4;
+static_assert(kWarps == 4, "cta_factors covers 16 tokens with 4 warps");
 
-// Factor buffer (floats / words): c[16] | tok_scale[16] | counter (u32) |
-// pad | acc_max[kCopies][16] (u32) | acc_sum[kCopies][16].  The accumulator
-// has kCopies copies (a CTA uses copy rowblock % kCopies), so the atomics of
-// many CTAs do not all meet on the same words.
+// Factor buffer (floats / words): c[16] | tok_scale[16] | state (u32) |
+// ticket counter (u32) | pad | acc_max[kCopies][16] (u32) |
+// acc_sum[kCopies][16].  A CTA of a producer folds into copy
+// (row block * S + slice) % kCopies, so the atomics spread over many words.
 constexpr int kCopies = 16;
-constexpr int kOffC = 0, kOffTs = 16, kOffCount = 32, kOffMax = 64, kOffSum = 64 + 16 * kCopies;
+constexpr int kOffC = 0, kOffTs = 16, kOffState = 32, kOffTicket = 33, kOffMax = 64, kOffSum = 64 + 16 * kCopies;
 constexpr size_t kStatsBytes = (64 + 32 * kCopies) * 4;
+constexpr unsigned kPending = 1u;     // state: the accumulator holds an unconsumed production
+constexpr unsigned kStateError = 2u;  // status bit: a factor buffer was produced twice unconsumed
 
 struct FProj {
     const uint8_t *packed;
@@ -50,22 +58,29 @@ struct FProj {
 
 struct FArgs {
     const __nv_bfloat16 *x;
-    const float *xs;  // factor buffer of the input
+    float *xs;  // factor buffer of the input (consumed)
+    unsigned int *status;
     FProj p[kMaxFused];
     int nproj, M, K, KT, tiles_per_cta;
     float eps;
 };
 
+// Register stage of a warp: one 128-k tile of packed weights for its 4 row
+// groups, and the raw bf16 input of that tile for the lane's tokens (32
+// values of token 8j+g at k = 128c + 32t, quantised just before the MMAs).
 template <int NT>
 struct Stage {
     uint4 w[kGroups];
-    uint4 q[NT][2];
+    uint4 x[NT][4];
 };
 
-__device__ __forceinline__ uint32_t quant_byte(float v, float c) {
-    int iv = __float2int_rn(__fmul_rn(v, c));
-    iv = iv > 127 ? 127 : (iv < -128 ? -128 : iv);
-    return static_cast<uint32_t>(iv) & 0xffu;
+// q = rint(v * c) (ties to even) in the low byte of the result: adding
+// 1.5 * 2^23 to fl(v * c) rounds it to an integer, as rint does.  No clamp:
+// c = 127 / max|x| comes from these very values, so |v * c| <= 127 (the
+// clamp of the definition never acts), and |v * c| < 2^22 keeps the trick
+// exact.
+__device__ __forceinline__ uint32_t qbits(float v, float c) {
+    return __float_as_uint(__fadd_rn(__fmul_rn(v, c), 12582912.0f));
 }
 // 16 bf16 -> 16 int8 (one uint4)
 __device__ __forceinline__ uint4 quant16(const uint4 &a, const uint4 &b, float c) {
@@ -74,21 +89,84 @@ __device__ __forceinline__ uint4 quant16(const uint4 &a, const uint4 &b, float c
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const uint32_t w0 = w[2 * i], w1 = w[2 * i + 1];
-        o[i] = quant_byte(__uint_as_float(w0 << 16), c) | (quant_byte(__uint_as_float(w0 & 0xffff0000u), c) << 8) |
-               (quant_byte(__uint_as_float(w1 << 16), c) << 16) |
-               (quant_byte(__uint_as_float(w1 & 0xffff0000u), c) << 24);
+        const uint32_t lo = prmt(qbits(__uint_as_float(w0 << 16), c), qbits(__uint_as_float(w0 & 0xffff0000u), c),
+                                 0x0040u);
+        const uint32_t hi = prmt(qbits(__uint_as_float(w1 << 16), c), qbits(__uint_as_float(w1 & 0xffff0000u), c),
+                                 0x0040u);
+        o[i] = prmt(lo, hi, 0x5410u);
     }
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// (hi, lo) += (bh, bl): compensated fp32 sum (two-sum of the high parts).
+// Symmetric in its operands, so both lanes of a shuffle pair get the same bits.
+__device__ __forceinline__ void ff_add(float &hi, float &lo, float bh, float bl_) {
+    const float s = __fadd_rn(hi, bh), bp = __fsub_rn(s, hi);
+    const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(bh, bp));
+    lo = __fadd_rn(__fadd_rn(lo, bl_), err);
+    hi = s;
+}
+
+// c and tok_scale of one token from max |v| and sum v^2 over K values.
+__device__ __forceinline__ void token_factors(float mx, float ss, int K, float eps, float &c, float &ts) {
+    if (!(mx >= 1e-5f)) mx = 1e-5f;
+    const float ms = __fadd_rn(__fdiv_rn(ss, static_cast<float>(K)), eps);
+    const float r = __fdiv_rn(1.0f, __fsqrt_rn(ms));
+    c = __fdiv_rn(127.0f, mx);
+    ts = __fdiv_rn(__fmul_rn(r, mx), 127.0f);
+}
+
+// Factors of tokens [0, M) of a factor buffer, by a CTA of 4 warps, into
+// c_out / ts_out (shared memory).  Every load is issued at once, whether the
+// buffer is pending or published (one round trip): the state word, the
+// published factors, and the 16 copies of each token's accumulator.  Warp w
+// takes token pairs w and w + 4: lanes 0-15 hold the copies of token 2p,
+// lanes 16-31 those of token 2p+1; max and the compensated sum are reduced in
+// a fixed butterfly, so every CTA and every caller gets the same bits.
+// Returns whether the buffer was pending.
+__device__ __forceinline__ bool cta_factors(const float *xs, int M, int K, float eps, float *c_out,
+                                            float *ts_out) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cp = lane & 15;
+    float mx[2], hi[2], lo[2] = {0.0f, 0.0f};
+    int tk[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        tk[r] = 2 * (warp + 4 * r) + (lane >> 4);
+        const bool ok = tk[r] < M;
+        mx[r] = ok ? ld_cg_f32(xs + kOffMax + cp * 16 + tk[r]) : 0.0f;
+        hi[r] = ok ? ld_cg_f32(xs + kOffSum + cp * 16 + tk[r]) : 0.0f;
+    }
+    const bool pend = ld_cg_u32(xs + kOffState) == kPending;
+    const float pub_c = lane < 16 ? ld_cg_f32(xs + kOffC + lane) : 0.0f;
+    const float pub_ts = lane < 16 ? ld_cg_f32(xs + kOffTs + lane) : 0.0f;
+    if (pend) {
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) {
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], off));
+                const float oh = __shfl_xor_sync(0xffffffffu, hi[r], off);
+                const float ol = __shfl_xor_sync(0xffffffffu, lo[r], off);
+                ff_add(hi[r], lo[r], oh, ol);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+            if (cp == 0 && tk[r] < M) token_factors(mx[r], __fadd_rn(hi[r], lo[r]), K, eps, c_out[tk[r]], ts_out[tk[r]]);
+    } else if (warp == 0 && lane < 16) {
+        c_out[lane] = pub_c;
+        ts_out[lane] = pub_ts;
+    }
+    return pend;
+}
+
 template <int NT>
-__global__ void __launch_bounds__(kWarps * 32, 3) fused_gemv_kernel(const FArgs A) {
+__global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 3) fused_gemv_kernel(const FArgs A) {
     __shared__ int32_t part[kWarps][NT * 8][kRows];
     __shared__ int32_t total[NT * 8 * kRows];
-    __shared__ float s_max[16], s_sum[16];
-    __shared__ int s_last;
+    __shared__ float s_c[16], s_ts[16];
 
-    pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const int rb = blockIdx.y;
@@ -114,25 +192,19 @@ __global__ void __launch_bounds__(kWarps * 32, 3) fused_gemv_kernel(const FArgs 
                 st.w[i] = make_uint4(0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u);
         }
     };
-    float cq[NT];  // 127 / max|x| of this lane's tokens
-    auto load_q = [&](Stage<NT> &st, int c) {
+    auto load_x = [&](Stage<NT> &st, int c) {
         if (c >= c_end) return;
         const int k0 = c * 128 + t * 32;
 #pragma unroll
         for (int jj = 0; jj < NT; ++jj) {
             const int tok = 8 * jj + g;
             const __nv_bfloat16 *src = A.x + static_cast<int64_t>(tok) * K + k0;
-            uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0, v2 = v0, v3 = v0;
-            if (tok < M && k0 < K) {
-                v0 = ld_ro16(src);
-                v1 = ld_ro16(src + 8);
-            }
-            if (tok < M && k0 + 16 < K) {
-                v2 = ld_ro16(src + 16);
-                v3 = ld_ro16(src + 24);
-            }
-            st.q[jj][0] = quant16(v0, v1, cq[jj]);
-            st.q[jj][1] = quant16(v2, v3, cq[jj]);
+            const uint4 z = make_uint4(0, 0, 0, 0);
+            const bool lo_ok = tok < M && k0 < K, hi_ok = tok < M && k0 + 16 < K;
+            st.x[jj][0] = lo_ok ? ld_ro16(src) : z;
+            st.x[jj][1] = lo_ok ? ld_ro16(src + 8) : z;
+            st.x[jj][2] = hi_ok ? ld_ro16(src + 16) : z;
+            st.x[jj][3] = hi_ok ? ld_ro16(src + 24) : z;
         }
     };
 
@@ -146,10 +218,13 @@ __global__ void __launch_bounds__(kWarps * 32, 3) fused_gemv_kernel(const FArgs 
     int corr[NT];
 #pragma unroll
     for (int jj = 0; jj < NT; ++jj) corr[jj] = 0;
+    float cq[NT];  // 127 / max|x| of this lane's tokens
     auto compute = [&](const Stage<NT> &st) {
         uint32_t b[NT][8][2];
 #pragma unroll
-        for (int jj = 0; jj < NT; ++jj) dm::build_b(st.q[jj][0], st.q[jj][1], b[jj], corr[jj]);
+        for (int jj = 0; jj < NT; ++jj)
+            dm::build_b(quant16(st.x[jj][0], st.x[jj][1], cq[jj]), quant16(st.x[jj][2], st.x[jj][3], cq[jj]), b[jj],
+                        corr[jj]);
         dm::mma_tile<NT>(st.w, b, d);
     };
 
@@ -157,22 +232,44 @@ __global__ void __launch_bounds__(kWarps * 32, 3) fused_gemv_kernel(const FArgs 
     int c = c_begin + warp;
     load_w(SA, c);
     load_w(SB, c + kWarps);
+    // tiles past the two register stages: into L2 now, one bulk prefetch per row group
+    if (threadIdx.x < kGroups && c_end > c_begin + 2 * kWarps) {
+        const int rg = rbl * kGroups + static_cast<int>(threadIdx.x);
+        if (rg < P.RGN)
+            bulk_prefetch_l2(P.packed + (static_cast<int64_t>(rg) * KT + c_begin + 2 * kWarps) * 512,
+                             static_cast<uint32_t>(c_end - c_begin - 2 * kWarps) * 512u);
+    }
+    const float gam = *P.gamma;  // static, like the weights
     pdl_wait();  // the input and its factors come from earlier kernels
+    load_x(SA, c);
+    load_x(SB, c + kWarps);
+
+    // The input's factors: from its pending accumulator, or as published.
+    unsigned *const xs_u = reinterpret_cast<unsigned *>(A.xs);
+    const bool pend = cta_factors(A.xs, M, K, A.eps, s_c, s_ts);
+    // This launch produces into P.stats: mark it pending (once per buffer).
+    if (P.stats != nullptr && rbl == 0 && s == 0 && threadIdx.x == 0) {
+        unsigned *const st = reinterpret_cast<unsigned *>(P.stats) + kOffState;
+        if (ld_cg_u32(st) == kPending) atomicOr(A.status, kStateError);
+        *st = kPending;
+    }
+    __syncthreads();
+    unsigned ticket = 0u;  // taken once every thread's reads of the accumulator are done
+    if (pend && threadIdx.x == 0) ticket = atomicAdd(xs_u + kOffTicket, 1u);
 #pragma unroll
     for (int jj = 0; jj < NT; ++jj) {
         const int tok = 8 * jj + g;
-        cq[jj] = tok < M ? A.xs[kOffC + tok] : 0.0f;
+        cq[jj] = tok < M ? s_c[tok] : 0.0f;
     }
-    load_q(SA, c);
-    load_q(SB, c + kWarps);
+
     for (; c < c_end; c += 2 * kWarps) {
         compute(SA);
         load_w(SA, c + 2 * kWarps);
-        load_q(SA, c + 2 * kWarps);
+        load_x(SA, c + 2 * kWarps);
         if (c + kWarps < c_end) {
             compute(SB);
             load_w(SB, c + 3 * kWarps);
-            load_q(SB, c + 3 * kWarps);
+            load_x(SB, c + 3 * kWarps);
         }
     }
 
@@ -198,7 +295,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3) fused_gemv_kernel(const FArgs 
         }
     }
     __syncthreads();
-    constexpr int E = NT * 8 * kRows;
+    const int E = M * kRows;  // entries e = token * kRows + row of the real tokens
     for (int e = threadIdx.x; e < E; e += kWarps * 32) {
         const int tk = e / kRows, rr = e % kRows;
         int v = 0;
@@ -210,32 +307,29 @@ __global__ void __launch_bounds__(kWarps * 32, 3) fused_gemv_kernel(const FArgs 
     if (S > 1) {
         cluster_sync();
         const int per = (E + S - 1) / S;
-        e0 = s * per;
+        e0 = min(E, s * per);
         e1 = min(E, e0 + per);
     } else {
         __syncthreads();
     }
-    if (threadIdx.x < 16) {
-        s_max[threadIdx.x] = 0.0f;
-        s_sum[threadIdx.x] = 0.0f;
-    }
-    __syncthreads();
-    const float gam = *P.gamma;
     float *vals = reinterpret_cast<float *>(&part[0][0][0]);  // bf16 outputs as floats, by entry
     for (int e = e0 + static_cast<int>(threadIdx.x); e < e1; e += kWarps * 32) {
-        int v;
+        int v = total[e];
         if (S > 1) {
-            v = 0;
+            // every slice's total (this CTA's own included), all loads in flight at once
             const uint32_t la = smem_addr(&total[e]);
-            for (int r = 0; r < S; ++r) v += ld_cluster_s32(cluster_map(la, r));
-        } else {
-            v = total[e];
+            int pv[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) pv[r] = r < S ? ld_cluster_s32(cluster_map(la, r)) : 0;
+            v = 0;
+#pragma unroll
+            for (int r = 0; r < 8; ++r) v += pv[r];
         }
         const int tk = e / kRows, rr = e % kRows;
         const int n = rbl * kRows + rr;
         float vf = 0.0f;
-        if (tk < M && n < P.N) {
-            const float f = __fmul_rn(gam, A.xs[kOffTs + tk]);
+        if (n < P.N) {
+            const float f = __fmul_rn(gam, s_ts[tk]);
             const __nv_bfloat16 o = __float2bfloat16_rn(__fmul_rn(static_cast<float>(v), f));
             P.out[static_cast<int64_t>(tk) * P.N + n] = o;
             if (P.acc_out) P.acc_out[static_cast<int64_t>(tk) * P.N + n] = v;
@@ -243,64 +337,56 @@ __global__ void __launch_bounds__(kWarps * 32, 3) fused_gemv_kernel(const FArgs 
         }
         vals[e] = vf;
     }
-    if (S > 1) cluster_sync();  // peers have read this CTA's totals
+    if (S > 1) cluster_sync();  // peers have read this CTA's totals; vals complete
     else __syncthreads();
-    if (P.stats == nullptr) return;
 
-    // Fold this CTA's outputs into the per-token accumulator of the projection.
-    if (threadIdx.x < M) {
-        const int tk = threadIdx.x;
-        float mx = 0.0f, hi = 0.0f, lo = 0.0f;
-        const int lo_e = max(e0, tk * kRows), hi_e = min(e1, (tk + 1) * kRows);
-        for (int e = lo_e; e < hi_e; ++e) {
-            const float v = vals[e];
-            mx = fmaxf(mx, fabsf(v));
-            const float p = __fmul_rn(v, v);  // exact: v is a bf16 value
-            const float sm = __fadd_rn(hi, p), bp = __fsub_rn(sm, hi);
-            lo = __fadd_rn(lo, __fadd_rn(__fsub_rn(hi, __fsub_rn(sm, bp)), __fsub_rn(p, bp)));
-            hi = sm;
-        }
-        if (hi_e > lo_e) {
-            const int cp = (rbl % kCopies) * 16 + tk;
-            atomicMax(reinterpret_cast<unsigned int *>(P.stats + kOffMax) + cp, __float_as_uint(mx));
-            atomicAdd(P.stats + kOffSum + cp, __fadd_rn(hi, lo));
-        }
-    }
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const unsigned nblk = static_cast<unsigned>((P.rb1 - P.rb0) * S);
-        const unsigned old = atomicAdd(reinterpret_cast<unsigned int *>(P.stats + kOffCount), 1u);
-        s_last = old == nblk - 1u;
-    }
-    __syncthreads();
-    if (!s_last) return;
-    // Last CTA of the projection: the next input's factors, then a clean
-    // accumulator for the next use of this buffer.
-    __threadfence();
-    if (threadIdx.x < M) {
-        const int tk = threadIdx.x;
-        volatile float *vs = P.stats;
-        float mx = 0.0f, hi = 0.0f, lo = 0.0f;
-        for (int cpy = 0; cpy < kCopies; ++cpy) {  // fixed order
-            mx = fmaxf(mx, __uint_as_float(reinterpret_cast<volatile unsigned int *>(vs)[kOffMax + cpy * 16 + tk]));
-            const float p = vs[kOffSum + cpy * 16 + tk];
-            const float sm = __fadd_rn(hi, p), bp = __fsub_rn(sm, hi);
-            lo = __fadd_rn(lo, __fadd_rn(__fsub_rn(hi, __fsub_rn(sm, bp)), __fsub_rn(p, bp)));
-            hi = sm;
-        }
-        const float ss = __fadd_rn(hi, lo);
-        if (!(mx >= 1e-5f)) mx = 1e-5f;
-        const float ms = __fadd_rn(__fdiv_rn(ss, static_cast<float>(P.N)), A.eps);
-        const float r = __fdiv_rn(1.0f, __fsqrt_rn(ms));
-        P.stats[kOffC + tk] = __fdiv_rn(127.0f, mx);
-        P.stats[kOffTs + tk] = __fdiv_rn(__fmul_rn(r, mx), 127.0f);
-        for (int cpy = 0; cpy < kCopies; ++cpy) {
-            reinterpret_cast<unsigned int *>(P.stats)[kOffMax + cpy * 16 + tk] = 0u;
-            P.stats[kOffSum + cpy * 16 + tk] = 0.0f;
+    // Fold this CTA's outputs into the per-token accumulator of the output:
+    // one warp per token, two entries per lane, a compensated butterfly.
+    if (P.stats != nullptr) {
+        const int cp = (rbl * S + s) % kCopies;
+        for (int tk = warp; tk < M; tk += kWarps) {
+            const int b0 = tk * kRows;
+            if (min(e1, b0 + kRows) <= max(e0, b0)) continue;  // no entry of this token here
+            const int ea = b0 + lane, eb = b0 + lane + 32;
+            const float va = (ea >= e0 && ea < e1) ? vals[ea] : 0.0f;
+            const float vb = (eb >= e0 && eb < e1) ? vals[eb] : 0.0f;
+            float mx = fmaxf(fabsf(va), fabsf(vb));
+            float hi = __fmul_rn(va, va), lo = 0.0f;  // exact: va is a bf16 value
+            ff_add(hi, lo, __fmul_rn(vb, vb), 0.0f);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                const float oh = __shfl_xor_sync(0xffffffffu, hi, off), ol = __shfl_xor_sync(0xffffffffu, lo, off);
+                ff_add(hi, lo, oh, ol);
+            }
+            if (lane == 0) {
+                atomicMax(reinterpret_cast<unsigned int *>(P.stats + kOffMax) + cp * 16 + tk, __float_as_uint(mx));
+                atomicAdd(P.stats + kOffSum + cp * 16 + tk, __fadd_rn(hi, lo));
+            }
         }
     }
-    if (threadIdx.x == 0) reinterpret_cast<unsigned int *>(P.stats)[kOffCount] = 0u;
+
+    // The last CTA to take a ticket publishes the input's factors and
+    // clears its accumulator (every CTA has read it by then).
+    if (pend && warp == 0) {
+        const unsigned tk0 = __shfl_sync(0xffffffffu, ticket, 0);
+        if (tk0 == gridDim.x * gridDim.y - 1u) {
+            if (lane < M) {
+                A.xs[kOffC + lane] = s_c[lane];
+                A.xs[kOffTs + lane] = s_ts[lane];
+            }
+            for (int i = lane; i < 2 * 16 * kCopies; i += 32) xs_u[kOffMax + i] = 0u;
+            if (lane == 0) {
+                xs_u[kOffTicket] = 0u;
+                xs_u[kOffState] = 0u;
+            }
+        }
+    }
+    // Only now may the next launch's CTAs start: they then find the SMs
+    // empty and spread evenly (started earlier, they land wherever this
+    // launch left room, several to an SM), and their weight loads overlap
+    // this launch's completion.
+    pdl_launch_dependents();
 }
 
 // Factors of an external input x [M, K]: one CTA per token.
@@ -310,6 +396,14 @@ __global__ void __launch_bounds__(256) act_stats_kernel(const uint4 *__restrict_
     __shared__ float s_mx[8], s_hi[8], s_lo[8];
     const int m = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_wait();
+    if (m == 0) {  // a fresh buffer: clear the accumulator and any pending state
+        unsigned *const su = reinterpret_cast<unsigned *>(stats);
+        for (int i = threadIdx.x; i < 2 * 16 * kCopies; i += 256) su[kOffMax + i] = 0u;
+        if (threadIdx.x == 0) {
+            su[kOffTicket] = 0u;
+            su[kOffState] = 0u;
+        }
+    }
     float mx = 0.0f, hi = 0.0f, lo = 0.0f;
     auto add = [&](float p) {
         const float sm = __fadd_rn(hi, p), bp = __fsub_rn(sm, hi);
@@ -350,11 +444,33 @@ __global__ void __launch_bounds__(256) act_stats_kernel(const uint4 *__restrict_
             add(s_hi[w]);
             lo = __fadd_rn(lo, s_lo[w]);
         }
-        if (!(mx >= 1e-5f)) mx = 1e-5f;
-        const float ms = __fadd_rn(__fdiv_rn(__fadd_rn(hi, lo), static_cast<float>(K)), eps);
-        const float r = __fdiv_rn(1.0f, __fsqrt_rn(ms));
-        stats[kOffC + m] = __fdiv_rn(127.0f, mx);
-        stats[kOffTs + m] = __fdiv_rn(__fmul_rn(r, mx), 127.0f);
+        token_factors(mx, __fadd_rn(hi, lo), K, eps, stats[kOffC + m], stats[kOffTs + m]);
+    }
+}
+
+// Reads (and, if `consume`, publishes and clears) a factor buffer's factors.
+__global__ void __launch_bounds__(128) read_factors_kernel(float *stats, int M, int K, float eps, int consume,
+                                                           float *c_out, float *ts_out) {
+    __shared__ float s_c[16], s_ts[16];
+    pdl_launch_dependents();
+    pdl_wait();
+    unsigned *const su = reinterpret_cast<unsigned *>(stats);
+    const bool pend = cta_factors(stats, M, K, eps, s_c, s_ts);
+    __syncthreads();
+    if (threadIdx.x < M) {
+        if (c_out) c_out[threadIdx.x] = s_c[threadIdx.x];
+        if (ts_out) ts_out[threadIdx.x] = s_ts[threadIdx.x];
+    }
+    if (pend && consume) {
+        if (threadIdx.x < M) {
+            stats[kOffC + threadIdx.x] = s_c[threadIdx.x];
+            stats[kOffTs + threadIdx.x] = s_ts[threadIdx.x];
+        }
+        for (int i = threadIdx.x; i < 2 * 16 * kCopies; i += 128) su[kOffMax + i] = 0u;
+        if (threadIdx.x == 0) {
+            su[kOffTicket] = 0u;
+            su[kOffState] = 0u;
+        }
     }
 }
 
@@ -374,7 +490,19 @@ extern "C" bitlinear_status_t bitlinear_act_stats(const void *x_bf16, int64_t M,
     return e == cudaSuccess ? BITLINEAR_OK : BITLINEAR_ERR_CUDA;
 }
 
-extern "C" bitlinear_status_t bitlinear_forward_fused(const void *x_bf16, const void *x_stats, int64_t M,
+extern "C" bitlinear_status_t bitlinear_fused_factors(void *stats, int64_t M, int64_t K, float eps,
+                                                      int32_t consume, float *c_out, float *ts_out,
+                                                      void *stream) {
+    using namespace bl;
+    if (M < 1 || M > 16 || K < 1 || !stats || !aligned16(stats)) return BITLINEAR_ERR_INVALID_ARG;
+    if ((c_out && !aligned4(c_out)) || (ts_out && !aligned4(ts_out))) return BITLINEAR_ERR_INVALID_ARG;
+    const cudaError_t e = launch_pdl(read_factors_kernel, dim3(1), dim3(128), 0, static_cast<cudaStream_t>(stream),
+                                     1, static_cast<float *>(stats), static_cast<int>(M), static_cast<int>(K), eps,
+                                     consume ? 1 : 0, c_out, ts_out);
+    return e == cudaSuccess ? BITLINEAR_OK : BITLINEAR_ERR_CUDA;
+}
+
+extern "C" bitlinear_status_t bitlinear_forward_fused(const void *x_bf16, void *x_stats, int64_t M,
                                                       int64_t K, int32_t nproj,
                                                       const bitlinear_fused_proj_t *projs, float eps,
                                                       void *stream) {
@@ -384,7 +512,8 @@ extern "C" bitlinear_status_t bitlinear_forward_fused(const void *x_bf16, const 
     if (nproj < 1 || nproj > kMaxFused || !projs) return BITLINEAR_ERR_INVALID_ARG;
     FArgs A{};
     A.x = static_cast<const __nv_bfloat16 *>(x_bf16);
-    A.xs = static_cast<const float *>(x_stats);
+    A.xs = static_cast<float *>(x_stats);
+    if (status_word(&A.status) != cudaSuccess) return BITLINEAR_ERR_CUDA;
     A.nproj = nproj;
     A.M = static_cast<int>(M);
     A.K = static_cast<int>(K);
@@ -397,6 +526,9 @@ extern "C" bitlinear_status_t bitlinear_forward_fused(const void *x_bf16, const 
         if (!aligned16(q.packed) || !aligned4(q.gamma) || !aligned16(q.out_bf16) ||
             (q.acc_out && !aligned16(q.acc_out)) || (q.stats && !aligned16(q.stats)))
             return BITLINEAR_ERR_INVALID_ARG;
+        if (q.stats && q.stats == x_stats) return BITLINEAR_ERR_INVALID_ARG;  // reads and writes one buffer
+        for (int i = 0; i < j; ++i)
+            if (q.stats && projs[i].stats == q.stats) return BITLINEAR_ERR_INVALID_ARG;
         FProj &P = A.p[j];
         P.packed = q.packed;
         P.gamma = q.gamma;

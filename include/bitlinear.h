@@ -64,7 +64,8 @@ typedef enum {
     BITLINEAR_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment or stream */
     BITLINEAR_ERR_UNSUPPORTED = 2, /* no sm_103a device / shape beyond limits */
     BITLINEAR_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
-    BITLINEAR_ERR_TIMEOUT = 4      /* a kernel gave up a bounded wait */
+    BITLINEAR_ERR_TIMEOUT = 4,     /* a kernel gave up a bounded wait */
+    BITLINEAR_ERR_STATE = 5        /* a pending factor buffer was produced into again */
 } bitlinear_status_t;
 
 /* Static, NUL-terminated description of a status code (never NULL). */
@@ -233,27 +234,44 @@ BITLINEAR_API bitlinear_status_t bitlinear_forward_f16(const void *q_f16, const 
  * quantised per token by its absolute maximum and rescaled by its RMS).
  *
  * A "factor buffer" (bitlinear_fused_stats_bytes() bytes, device, 16-byte
- * aligned) carries, for an activation matrix [M, K] in bf16, each token's
- * c = 127 / max(max_k |v|, 1e-5) and tok_scale = rms^-1 * max / 127 (rms =
- * sqrt(sum v^2 / K + eps)), plus an accumulator that its producer reduces
- * through.  Zero a factor buffer once (cudaMemset) before its first use;
- * every call leaves it ready for the next.
+ * aligned) travels with an activation matrix [M, K] in bf16.  It yields each
+ * token's c = 127 / max(max_k |v|, 1e-5) and tok_scale = rms^-1 * max / 127
+ * (rms = sqrt(sum v^2 / K + eps)), either as published values or as a
+ * pending accumulator filled by the launch that produced the activation.
+ * Zero a factor buffer once (cudaMemset) before its first use.
  *
- *   bitlinear_act_stats       factors of an input x (bf16 [M, K]) into stats.
- *   bitlinear_forward_fused   for up to 4 projections j sharing the input x
- *                             (with its factors x_stats): q = clamp(rint(
+ *   bitlinear_act_stats       publishes the factors of an input x (bf16
+ *                             [M, K]) into stats, resetting any pending
+ *                             state.
+ *   bitlinear_forward_fused   for up to 4 projections j sharing the input x:
+ *                             c and tok_scale from x_stats, q = clamp(rint(
  *                             x * c), -128, 127) (bit-identical to
  *                             bitlinear_quant_act), acc = sum q * Wq (exact
  *                             int32), out_j = bf16(acc * (gamma_j *
  *                             tok_scale)); and, if stats_j is given, out_j's
- *                             own factors for the next projection.  The
- *                             token scales of stats_j sum squares with fp32
- *                             atomics (order varies): they agree with the
- *                             definition to about 1e-7, not bit for bit.
- * x_stats must not be one of the stats_j.  Weights follow the static-weight
- * contract of bitlinear_forward.  1 <= M <= 16, K % 16 == 0, K <= 65536.
- * Errors: INVALID_ARG (sizes, pointers, alignment), UNSUPPORTED (too many
- * row blocks), CUDA.
+ *                             max |v| and sum v^2 per token accumulated into
+ *                             stats_j, which becomes pending.  The launch
+ *                             consumes x_stats: if it was pending, its
+ *                             factors are published and its accumulator
+ *                             cleared by the time the launch ends.  The sums
+ *                             of squares use fp32 atomics (order varies):
+ *                             token scales agree with the definition to about
+ *                             1e-7, and every CTA of the consuming launch
+ *                             uses the same bits.
+ *   bitlinear_fused_factors   copies the factors of a factor buffer for
+ *                             [M, K] to c_out / ts_out (device fp32 [M] each,
+ *                             either may be NULL); with consume != 0 it also
+ *                             publishes them and clears a pending
+ *                             accumulator, like a consuming launch.
+ * A pending factor buffer must be consumed (by bitlinear_forward_fused or
+ * bitlinear_fused_factors with consume) or reset (bitlinear_act_stats)
+ * before it is produced into again; producing into a pending buffer sets the
+ * status word, which bitlinear_check_status reports as
+ * BITLINEAR_ERR_STATE.  x_stats must not be one of the stats_j, and the
+ * stats_j must be distinct.  Weights follow the static-weight contract of
+ * bitlinear_forward.  1 <= M <= 16, K % 16 == 0, K <= 65536.
+ * Errors: INVALID_ARG (sizes, pointers, alignment, shared buffers),
+ * UNSUPPORTED (too many row blocks), CUDA.
  */
 typedef struct {
     const uint8_t *packed;  /* device: packed weights of an [N, K] matrix */
@@ -267,9 +285,12 @@ typedef struct {
 BITLINEAR_API size_t bitlinear_fused_stats_bytes(void);
 BITLINEAR_API bitlinear_status_t bitlinear_act_stats(const void *x_bf16, int64_t M, int64_t K, float eps,
                                                      void *stats, void *stream);
-BITLINEAR_API bitlinear_status_t bitlinear_forward_fused(const void *x_bf16, const void *x_stats,
+BITLINEAR_API bitlinear_status_t bitlinear_forward_fused(const void *x_bf16, void *x_stats,
                                                          int64_t M, int64_t K, int32_t nproj,
                                                          const bitlinear_fused_proj_t *projs, float eps,
+                                                         void *stream);
+BITLINEAR_API bitlinear_status_t bitlinear_fused_factors(void *stats, int64_t M, int64_t K, float eps,
+                                                         int32_t consume, float *c_out, float *ts_out,
                                                          void *stream);
 
 /*
@@ -358,9 +379,11 @@ BITLINEAR_API bitlinear_status_t bitlinear_chain_run(const bitlinear_chain_plan_
 BITLINEAR_API void bitlinear_chain_set_split(int32_t split);
 
 /*
- * Reads and clears the current device's kernel status word (a bounded wait
- * that gave up) after synchronising `stream`.  Returns BITLINEAR_OK or
- * BITLINEAR_ERR_TIMEOUT; BITLINEAR_ERR_CUDA if the stream reports an error.
+ * Reads and clears the current device's kernel status word after
+ * synchronising `stream`.  Returns BITLINEAR_OK, BITLINEAR_ERR_STATE (a
+ * pending factor buffer was produced into again), BITLINEAR_ERR_TIMEOUT (a
+ * bounded wait gave up), or BITLINEAR_ERR_CUDA if the stream reports an
+ * error.
  */
 BITLINEAR_API bitlinear_status_t bitlinear_check_status(void *stream);
 

@@ -7,7 +7,10 @@ multiplies with the ternary weights and rescales.  Bit-exact: the int32
 accumulators (which pins the int8 activations), and the bf16 outputs when the
 oracle's epilogue is fed the token scales the GPU used (read back from the
 input's factor buffer).  The token scales and the factors c = 127/max are
-held to the oracle's within 1e-6 and bit for bit respectively.
+held to the oracle's within 1e-6 and bit for bit respectively.  Also the
+factor buffer's protocol: pending until consumed, published by the consumer,
+a second production into a pending buffer reported, a reset by
+bitlinear_act_stats.
 """
 import numpy as np
 import pytest
@@ -36,9 +39,9 @@ def bits16(t):
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def factors(stats, M):
-    f = stats.view(torch.float32).cpu().numpy()
-    return f[0:M].copy(), f[16:16 + M].copy()
+def factors(stats, M, K):
+    c, ts = bl.fused_factors(stats, M, K)
+    return c.cpu().numpy(), ts.cpu().numpy()
 
 
 def make_weights(shapes, seed):
@@ -55,7 +58,7 @@ def make_weights(shapes, seed):
 def check_proj(x_bits, stats_in, M, w, acc, out):
     """One projection: the oracle on the GPU's input bits and token scales."""
     q_ref, s_ref = oracle.quant_act(x_bits, None, 1e-5)
-    c, ts = factors(stats_in, M)
+    c, ts = factors(stats_in, M, x_bits.shape[1])
     mx = np.maximum(np.abs(x_bits_to_f32(x_bits)).max(axis=1), np.float32(1e-5))
     np.testing.assert_array_equal(c, np.float32(127.0) / mx.astype(np.float32))
     np.testing.assert_allclose(ts, s_ref, rtol=S_TOK_RTOL, atol=0)
@@ -100,14 +103,18 @@ def run_layer(M, hidden, ffn, kv, w, x, stats, check=True):
         for name in ("gate", "up"):
             check_proj(ob, stats["o"], M, W[name], dev_out[name][1], dev_out[name][0])
         check_proj(bits16(dev_out["up"][0]), stats["up"], M, W["down"], dev_out["down"][1], dev_out["down"][0])
-        # the down projection's factors, for the next layer
+        # the down projection's factors, for the next layer (still pending)
         check_factors(bits16(dev_out["down"][0]), stats["down"], M)
+    # nothing consumes them here: consume them so the buffer can be produced again
+    bl.fused_factors(stats["down"], M, hidden, consume=True)
+    torch.cuda.synchronize()
+    assert bl.bitlinear_check_status() == bl.OK
     return dev_out
 
 
 def check_factors(x_bits, stats, M):
     _, s_ref = oracle.quant_act(x_bits, None, 1e-5)
-    c, ts = factors(stats, M)
+    c, ts = factors(stats, M, x_bits.shape[1])
     mx = np.maximum(np.abs(x_bits_to_f32(x_bits)).max(axis=1), np.float32(1e-5))
     np.testing.assert_array_equal(c, np.float32(127.0) / mx.astype(np.float32))
     np.testing.assert_allclose(ts, s_ref, rtol=S_TOK_RTOL, atol=0)
@@ -157,8 +164,67 @@ def test_fused_matches_unfused_path():
     bl.forward(q, s, w[0], w[1], N, acc_out=acc2)
     torch.cuda.synchronize()
     np.testing.assert_array_equal(acc.cpu().numpy(), acc2.cpu().numpy())
-    _, ts = factors(st, M)
+    _, ts = factors(st, M, K)
     np.testing.assert_allclose(ts, s.cpu().numpy(), rtol=S_TOK_RTOL)
+
+
+def test_factor_buffer_protocol():
+    """Pending until consumed; every consumer sees the same factors; a second
+    production into a pending buffer is reported; act_stats resets."""
+    M, K, N, N2 = 7, 512, 640, 384
+    w1 = make_weights([(N, K)], seed=9800)[0]
+    w2 = make_weights([(N2, N)], seed=9801)[0]
+    x = inputs.activations_bf16(M, K, seed=9802).to(DEV)
+    sx, sh = bl.new_stats(DEV), bl.new_stats(DEV)
+    h = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+
+    def produce():
+        bl.bitlinear_act_stats(x, M, K, 1e-5, sx)
+        bl.bitlinear_forward_fused(x, sx, M, K, [bl.FusedProj(w1[0].data_ptr(), w1[1].data_ptr(), N, h.data_ptr(),
+                                                              None, sh.data_ptr())])
+
+    def consume():
+        out = torch.empty(M, N2, dtype=torch.bfloat16, device=DEV)
+        acc = torch.empty(M, N2, dtype=torch.int32, device=DEV)
+        bl.bitlinear_forward_fused(h, sh, M, N, [bl.FusedProj(w2[0].data_ptr(), w2[1].data_ptr(), N2,
+                                                              out.data_ptr(), acc.data_ptr(), None)])
+        return out, acc
+
+    produce()
+    torch.cuda.synchronize()
+    assert bl.bitlinear_check_status() == bl.OK
+    state = lambda: int(sh.view(torch.int32)[32].item())
+    assert state() == 1                                   # pending
+    c0, ts0 = factors(sh, M, N)                           # read without consuming
+    assert state() == 1
+    out1, acc1 = consume()
+    torch.cuda.synchronize()
+    assert state() == 0                                   # published, accumulator cleared
+    f = sh.view(torch.float32).cpu().numpy()
+    np.testing.assert_array_equal(f[0:M], c0)
+    np.testing.assert_array_equal(f[16:16 + M], ts0)
+    assert not sh.view(torch.int32)[64:64 + 512].any().item()
+    out2, acc2 = consume()                                # a second consumer: the published factors
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(acc1.cpu().numpy(), acc2.cpu().numpy())
+    np.testing.assert_array_equal(bits16(out1), bits16(out2))
+    check_proj(bits16(h), sh, M, w2, acc1, out1)
+    assert bl.bitlinear_check_status() == bl.OK
+    # produce twice without consuming: reported, and act_stats makes it usable again
+    produce()
+    produce()
+    torch.cuda.synchronize()
+    assert bl.bitlinear_check_status() == bl.ERR_STATE
+    assert bl.bitlinear_check_status() == bl.OK           # the status word was cleared
+    bl.bitlinear_act_stats(h, M, N, 1e-5, sh)
+    torch.cuda.synchronize()
+    assert state() == 0
+    produce()
+    out3, acc3 = consume()
+    torch.cuda.synchronize()
+    assert bl.bitlinear_check_status() == bl.OK
+    np.testing.assert_array_equal(acc1.cpu().numpy(), acc3.cpu().numpy())
+    check_proj(bits16(h), sh, M, w2, acc3, out3)   # the sum order of the token scale may differ
 
 
 def test_fused_rejects_bad_arguments():
@@ -175,3 +241,10 @@ def test_fused_rejects_bad_arguments():
         bl.bitlinear_forward_fused(x, st, 2, 256, [p] * 5)       # more than 4 projections
     with pytest.raises(bl.BitLinearError):
         bl.bitlinear_act_stats(x, 0, 256, 1e-5, st)
+    ps = bl.FusedProj(w[0].data_ptr(), w[1].data_ptr(), 64, out.data_ptr(), None, st.data_ptr())
+    with pytest.raises(bl.BitLinearError):
+        bl.bitlinear_forward_fused(x, st, 2, 256, [ps])          # reads and writes one factor buffer
+    st2 = bl.new_stats(DEV)
+    ps2 = bl.FusedProj(w[0].data_ptr(), w[1].data_ptr(), 64, out.data_ptr(), None, st2.data_ptr())
+    with pytest.raises(bl.BitLinearError):
+        bl.bitlinear_forward_fused(x, st, 2, 256, [ps2, ps2])    # two outputs into one factor buffer
