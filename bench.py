@@ -24,6 +24,9 @@ roofline: the fused decode GEMV, bytes per launch / average launch time.
 chain, unfused: the same stack through the persistent fused-chain kernel
          (bitlinear_chain_run, one launch per M) and through separate
          bitlinear_quant_act + bitlinear_forward calls, for comparison.
+sweep: the decode GEMV shape by shape (bitlinear_forward on a pre-quantised
+         input, every launch reading its weights from HBM after an L2 flush),
+         and bitlinear_quant_act on its own.
 prefill: the 2B prefill chain at M = 4096 (int8-exact tensor-core GEMM), TOPS.
 cpu_baseline: the CPU oracle on a bounded sample of the same workload.
 
@@ -49,6 +52,11 @@ METRIC = "BitLinear decode GB/s (% HBM peak) and prefill int8 TOPS, 2B-shape lay
 WORKLOAD = "decode_2b"
 M_LIST = (1, 4, 16)
 LAYERS = 20
+# DRAM bytes read per packed-weight byte by fused_gemv_kernel, from one ncu
+# capture (profiles/fused_gemv_decode_2b_M16_full.md: 15.826 MB read over
+# three launches holding 15.400 MB of packed weights).  Re-measure when the
+# kernel changes.
+FUSED_DRAM_PER_PACKED_BYTE = 1.0277
 FALLBACK_HBM_GBS = 6400.0
 FALLBACK_BF16_TFLOPS = 1800.0
 
@@ -288,11 +296,12 @@ class FusedDecode:
     of the stack input, then per layer four bitlinear_forward_fused launches
     (q,k,v | o | gate,up | down), each quantising its input on the fly."""
 
-    def __init__(self, torch, bl, db):
+    def __init__(self, torch, bl, db, m_list=M_LIST):
         self.torch, self.bl, self.db = torch, bl, db
         T = torch
         self.bufs = {}
-        for M in M_LIST:
+        self.m_list = tuple(m_list)
+        for M in self.m_list:
             outs = [[T.empty(M, N, dtype=T.bfloat16, device=db.dev) for _, N, _ in db.shapes]
                     for _ in range(db.layers)]
             stats = [[bl.new_stats(db.dev) for _ in range(4)] for _ in range(db.layers)]  # v, o, up, down
@@ -301,7 +310,7 @@ class FusedDecode:
 
     def run_step(self, stream, h2d=None, d2h=None):
         bl, db = self.bl, self.db
-        for M in M_LIST:
+        for M in self.m_list:
             outs, stats, x_stats = self.bufs[M]
             if h2d is not None:
                 db.x[M].copy_(h2d[M], non_blocking=True)
@@ -496,6 +505,35 @@ def profile_gemm(spec):
     return 0
 
 
+def profile_fused(spec):
+    """--profile-fused L,M: the fused decode path (act_stats + 4 fused GEMV
+    launches per layer) on an L-layer 2B-shape stack at M tokens, eagerly
+    launched: 3 warm-up + 5 timed passes (driver for ncu captures)."""
+    import torch
+    import bitlinear_02_b300 as bl
+    from bitlinear_02_b300 import inputs
+    L, M = (int(v) for v in spec.split(","))
+    dev = torch.device("cuda:0")
+    bl.load_library()
+    db = DecodeBench(torch, bl, inputs, dev, layers=L)
+    fd = FusedDecode(torch, bl, db, m_list=(M,))
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        fd.run_step(stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(5):
+        fd.run_step(stream)
+    e1.record()
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / 5
+    assert bl.bitlinear_check_status() == bl.OK
+    print(json.dumps({"profile": "fused", "layers": L, "M": M, "ms_per_pass": round(ms, 4),
+                      "launches_per_pass": 1 + 4 * L}))
+    return 0
+
+
 def profile_chain(spec):
     """--profile-chain L,M: the decode chain on an L-layer 2B-shape stack at
     M tokens, 3 warm-up + 10 timed runs (driver for ncu captures)."""
@@ -533,6 +571,87 @@ def profile_chain(spec):
     return 0
 
 
+def gemv_sweep(torch, bl, db, stream, reps=9):
+    """The 2B decode GEMV sweep, shape by shape: bitlinear_forward on a
+    pre-quantised input (the GEMV with its rescale epilogue), and
+    bitlinear_quant_act reported on its own.  Per (M, shape) one CUDA graph
+    of back-to-back launches over the stack's copies of that projection (20
+    layers x the projections of that shape), replayed right after an L2
+    flush (a 256 MB write, outside the timed events), so every launch reads
+    its weights from HBM.  Per-launch time = median replay time / launches;
+    GB/s = algorithmic bytes per launch / that time."""
+    T = torch
+    flush = T.empty(256 << 20, dtype=T.uint8, device=db.dev)
+    kinds = [("q,k,v,o", [0, 1, 2, 3]), ("gate,up", [4, 5]), ("down", [6])]
+    e0, e1 = T.cuda.Event(enable_timing=True), T.cuda.Event(enable_timing=True)
+
+    def timed(graph, n):
+        ts = []
+        with T.cuda.stream(stream):
+            for _ in range(reps):
+                flush.zero_()
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+                e1.synchronize()
+                ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts) / n  # ms per launch
+
+    gemv, quant = [], []
+    tot_b, tot_ms = 0, 0.0
+    for M in M_LIST:
+        for name, idxs in kinds:
+            _, N, K = db.shapes[idxs[0]]
+            x = db.inputs.activations_bf16(M, K, seed=900 + M, device=db.dev)
+            q, sc = bl.quant_act(x, None, db.eps_a)
+            out = T.empty(M, N, dtype=T.bfloat16, device=db.dev)
+            mats = [db.w[7 * l + j] for l in range(db.layers) for j in idxs]
+
+            def run():
+                for packed, gamma, n in mats:
+                    bl.bitlinear_forward(q, sc, packed, gamma, M, n, K, out)
+
+            with T.cuda.stream(stream):
+                run()
+            T.cuda.synchronize()
+            g = T.cuda.CUDAGraph()
+            with T.cuda.graph(g, stream=stream):
+                run()
+            ms = timed(g, len(mats))
+            b = algo_bytes_forward(M, N, K)
+            gemv.append({"M": M, "proj": name, "N": N, "K": K, "us": round(ms * 1e3, 3),
+                         "GB/s": round(b / (ms * 1e-3) / 1e9, 1), "launches": len(mats)})
+            tot_b += b * len(mats)
+            tot_ms += ms * len(mats)
+            del g
+        for K in sorted({k for _, _, k in db.shapes}):
+            xs = [db.inputs.activations_bf16(M, K, seed=950 + M + i, device=db.dev) for i in range(20)]
+            qo = T.empty(M, K, dtype=T.int8, device=db.dev)
+            so = T.empty(M, dtype=T.float32, device=db.dev)
+
+            def runq():
+                for x in xs:
+                    bl.bitlinear_quant_act(x, None, M, K, db.eps_a, qo, so)
+
+            with T.cuda.stream(stream):
+                runq()
+            T.cuda.synchronize()
+            g = T.cuda.CUDAGraph()
+            with T.cuda.graph(g, stream=stream):
+                runq()
+            ms = timed(g, len(xs))
+            quant.append({"M": M, "K": K, "us": round(ms * 1e3, 3),
+                          "GB/s": round(algo_bytes_quant(M, K) / (ms * 1e-3) / 1e9, 2)})
+            del g
+    del flush
+    return {"mode": "per (M, shape): a graph of bitlinear_forward launches over the stack's copies of that "
+                    "projection on a pre-quantised input, replayed after a 256 MB L2 flush; median of "
+                    f"{reps} replays / launches",
+            "gemv": gemv, "quant_act": quant,
+            "gemv_all": {"GB/s": round(tot_b / (tot_ms * 1e-3) / 1e9, 1),
+                         "note": "all shapes and M: algorithmic bytes / summed launch times"}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -543,9 +662,12 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--profile-gemm", default=None, help="N,K,M[,int8]: time one GEMM shape (ncu driver)")
     ap.add_argument("--profile-chain", default=None, help="L,M: time the decode chain (ncu driver)")
+    ap.add_argument("--profile-fused", default=None, help="L,M: time the fused decode path (ncu driver)")
     args = ap.parse_args()
     if args.profile_gemm:
         return profile_gemm(args.profile_gemm)
+    if args.profile_fused:
+        return profile_fused(args.profile_fused)
     if args.profile_chain:
         return profile_chain(args.profile_chain)
     if args.warmup < 3:
@@ -611,6 +733,9 @@ def main():
     chain_ms = time_graphs(torch, [g_chain], max(20, args.steps // 10), 3, stream) / max(20, args.steps // 10)
     del g_chain
     unf_ms = unfused_step_ms(torch, bl, db, stream)
+    sweep = gemv_sweep(torch, bl, db, stream)
+    for r in sweep["gemv"]:
+        r["frac"] = round(r["GB/s"] / hbm_peak, 4)
     n_fused = FusedDecode.launches  # act_stats + 4 fused GEMVs per layer, per M
     launch_us = 1000.0 * ms_step / n_fused
     bytes_launch = db.bytes_step / n_fused
@@ -645,17 +770,22 @@ def main():
                    "parallelism": f"replicas x{ws}"},
         "hbm_frac_of_step": round(value / ws / hbm_peak, 4),
         "roofline": {"bound": "hbm", "achieved": round(fused_gbs, 1), "peak": round(hbm_peak, 1),
-                     "unit": "GB/s", "frac": round(fused_gbs / hbm_peak, 4), "traffic": None,
+                     "unit": "GB/s", "frac": round(fused_gbs / hbm_peak, 4),
+                     "traffic": round(FUSED_DRAM_PER_PACKED_BYTE * db.packed_bytes * len(M_LIST) / n_fused),
+                     "traffic_note": "bytes per average launch: ncu DRAM bytes per packed-weight byte "
+                                     "(profiles/fused_gemv_decode_2b_M16_full.md) x packed bytes per launch",
                      "kernel": "fused_gemv_kernel (decode GEMV with the quantiser folded in)",
                      "launch_avg_us": round(launch_us, 2), "algo_bytes_per_launch": round(bytes_launch),
                      "peak_note": f"{peak_kind} HBM copy bandwidth",
-                     "method": "CUDA events around the timed graph replays / launches in the step"},
+                     "method": "CUDA events around the timed graph replays; launch time = step time / "
+                               "launches in the step (3 of the 243 are act_stats)"},
         "chain": {"ms_per_step": round(chain_ms, 4),
                   "value": round(db.bytes_step / (chain_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                   "mode": "persistent fused-chain kernel, one launch per M through the whole stack"},
         "unfused": {"ms_per_step": round(unf_ms, 4),
                     "value": round(db.bytes_step / (unf_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                     "mode": "bitlinear_quant_act + bitlinear_forward per projection, PDL-chained graph"},
+        "sweep": sweep,
         "prefill": prefill,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d_bytes,

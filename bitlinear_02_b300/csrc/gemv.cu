@@ -48,7 +48,6 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
     __shared__ int32_t part[kWarps][NT * 8][kRows];
     __shared__ int32_t total[NT * 8 * kRows];
 
-    pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const int rb = blockIdx.y;
@@ -176,6 +175,9 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
         }
     }
     if (S > 1) cluster_sync();  // keep this CTA's shared memory alive for its peers
+    // The next launch's CTAs start only now, on SMs this launch is leaving:
+    // they spread evenly instead of piling into the room left beside it.
+    pdl_launch_dependents();
 }
 
 }  // namespace
