@@ -65,9 +65,23 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+// Packed weights of 8 row groups at one 128-k tile, by one tensor-map copy:
+// the packed buffer seen as u64 [row group][k-tile][64], box 64 x 1 x 8
+// (4 KB, row group major, so the 512-byte tiles land back to back).  One
+// copy instead of eight 512-byte bulk copies: the copy instructions, issued
+// by one loader thread, set the pace of the pipeline.
+__device__ __forceinline__ void tma_load_w8(void *dst, const CUtensorMap *map, int c, int rg0, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(c), "r"(rg0), "r"(smem_addr(bar))
+        : "memory");
+}
+
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap qmap, const float *__restrict__ tok_scale,
+    gemm_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap wmap,
+                const float *__restrict__ tok_scale,
                 const uint8_t *__restrict__ packed, const float *__restrict__ gamma, int M, int N,
                 int K, int KT, int RGN, __nv_bfloat16 *__restrict__ out,
                 int32_t *__restrict__ acc_out, uint32_t wait_limit) {
@@ -114,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 9) {
         // ---------------- loader ----------------
         if (lane == 0) {
-            const uint32_t bytes = static_cast<uint32_t>(nrg) * 512u + L::kRawB;
+            const uint32_t bytes = kRawA + L::kRawB;  // a full box: rows past N arrive zero-filled (unread)
             // the packed weights are static: their copies may start before the
             // previous kernel finished; the activations may not
             bool waited = false;
@@ -126,10 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 uint8_t *raw = smem + L::kRawBase + rs * L::kRawStage;
                 mbar_arrive_expect_tx(&raw_full[rs], bytes);
-                const int c = st >> 1;
-                for (int i = 0; i < nrg; ++i)
-                    bulk_g2s(raw + 512 * i, packed + (static_cast<int64_t>(rg0 + i) * KT + c) * 512, 512u,
-                             &raw_full[rs]);
+                tma_load_w8(raw, &wmap, st >> 1, rg0, &raw_full[rs]);
                 if (!waited) {
                     pdl_wait();
                     waited = true;
@@ -258,30 +269,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 // layout the MMA reads, so the converter warps only expand the weight codes
 // into tensor memory.  Stage = swizzled f16 tile | packed codes.
 // ---------------------------------------------------------------------------
-constexpr int kS16 = 6;
-
-template <int BN>
+// NSTG stages; MINB CTAs per SM (2: each CTA's prologue and epilogue run
+// under the other's main loop, so the tensor pipe keeps working across tile
+// boundaries; that needs the TMEM columns of both to fit in 512).
+template <int BN, int NSTG>
 struct Smem16 {
     static constexpr uint32_t kTileB = BN * 128;
     static constexpr uint32_t kStage = kTileB + kRawA;  // multiple of 1024
-    static constexpr uint32_t kBytes = kS16 * kStage + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr uint32_t kBytes = NSTG * kStage + 1024 /*align*/ + 256 /*barriers*/;
     static constexpr uint32_t kACol = BN;
-    static constexpr uint32_t kCols = BN + 32 * kS16 <= 256 ? 256 : 512;
+    static constexpr uint32_t kCols = BN + 32 * NSTG <= 128 ? 128 : (BN + 32 * NSTG <= 256 ? 256 : 512);
 };
 
-template <int BN>
-__global__ void __launch_bounds__(kThreads, 1)
-    gemm16_kernel(const __grid_constant__ CUtensorMap qmap, const float *__restrict__ tok_scale,
+template <int BN, int NSTG, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB)
+    gemm16_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap wmap,
+                  const float *__restrict__ tok_scale,
                   const uint8_t *__restrict__ packed, const float *__restrict__ gamma, int M, int N,
                   int K, int KT, int RGN, __nv_bfloat16 *__restrict__ out,
                   int32_t *__restrict__ acc_out, uint32_t wait_limit) {
-    using L = Smem16<BN>;
+    using L = Smem16<BN, NSTG>;
+    static_assert(MINB * L::kCols <= 512, "the CTAs of an SM share 512 TMEM columns");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kS16 * L::kStage);
-    uint64_t *full = bars, *a_ready = bars + kS16, *empty = bars + 2 * kS16;
-    uint64_t *accum = bars + 3 * kS16;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NSTG * L::kStage);
+    uint64_t *full = bars, *a_ready = bars + NSTG, *empty = bars + 2 * NSTG;
+    uint64_t *accum = bars + 3 * NSTG;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum + 1);
     int *issued = reinterpret_cast<int *>(tmem_slot + 1);
 
@@ -291,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool timed_out = false;
     if (tid == 0) {
         *issued = 0;
-        for (int i = 0; i < kS16; ++i) {
+        for (int i = 0; i < NSTG; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&a_ready[i], kConverters / 2);
             mbar_init(&empty[i], 1);
@@ -313,20 +327,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 9) {
         // ---------------- loader ----------------
         if (lane == 0) {
-            const uint32_t bytes = static_cast<uint32_t>(nrg) * 512u + L::kTileB;
+            const uint32_t bytes = kRawA + L::kTileB;  // a full box: rows past N arrive zero-filled (unread)
             bool waited = false;
             for (int st = 0; st < NS; ++st) {
-                const int s = st % kS16;
-                if (!mbar_wait_bounded(&empty[s], ((st / kS16) & 1) ^ 1, wait_limit)) {
+                const int s = st % NSTG;
+                if (!mbar_wait_bounded(&empty[s], ((st / NSTG) & 1) ^ 1, wait_limit)) {
                     timed_out = true;
                     break;
                 }
                 uint8_t *stage = smem + s * L::kStage;
                 mbar_arrive_expect_tx(&full[s], bytes);
-                const int c = st >> 1;
-                for (int i = 0; i < nrg; ++i)
-                    bulk_g2s(stage + L::kTileB + 512 * i, packed + (static_cast<int64_t>(rg0 + i) * KT + c) * 512,
-                             512u, &full[s]);
+                tma_load_w8(stage + L::kTileB, &wmap, st >> 1, rg0, &full[s]);
                 if (!waited) {  // the weights are static; the activations come from earlier kernels
                     pdl_wait();
                     waited = true;
@@ -345,22 +356,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a_off = 512 * rgl + 16 * 4 * (ri & 7) + 4 * (ri >> 3);
         const uint32_t a_lane = static_cast<uint32_t>(32 * (warp & 3)) << 16;
         for (int st = warp >> 2; st < NS; st += 2) {
-            const int s = st % kS16;
-            if (!mbar_wait_bounded(&full[s], (st / kS16) & 1, wait_limit)) timed_out = true;
+            const int s = st % NSTG;
+            if (!mbar_wait_bounded(&full[s], (st / NSTG) & 1, wait_limit)) timed_out = true;
             const uint8_t *codes = smem + s * L::kStage + L::kTileB;
             const int hf = st & 1;
-            uint32_t f[32];
 #pragma unroll
-            for (int t2 = 0; t2 < 2; ++t2)
+            for (int t2 = 0; t2 < 2; ++t2) {  // two 16-column halves (fewer live registers)
+                uint32_t f[16];
 #pragma unroll
                 for (int P = 0; P < 2; ++P) {
                     const uint32_t w = row_ok ? *reinterpret_cast<const uint32_t *>(codes + a_off + 16 * (2 * hf + t2) + 8 * P)
                                               : 0x55555555u;
 #pragma unroll
                     for (int p = 0; p < 8; ++p)
-                        f[16 * t2 + 8 * P + p] = hadd2(((w >> (2 * p)) & 0x00030003u) | 0x64006400u, 0xE401E401u);
+                        f[8 * P + p] = hadd2(((w >> (2 * p)) & 0x00030003u) | 0x64006400u, 0xE401E401u);
                 }
-            tc_st32(tmem + a_lane + L::kACol + 32 * s, f);
+                tc_st16(tmem + a_lane + L::kACol + 32 * s + 16 * t2, f);
+            }
             tc_wait_st();
             tc_fence_before();
             mbar_arrive(&a_ready[s]);
@@ -370,9 +382,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t idesc = idesc_f16_f32(128, BN);
         const uint32_t base = smem_addr(smem);
         for (int st = 0; st < NS; ++st) {
-            const int s = st % kS16;
-            if (!mbar_wait_bounded(&full[s], (st / kS16) & 1, wait_limit)) timed_out = true;
-            if (!mbar_wait_bounded(&a_ready[s], (st / kS16) & 1, wait_limit)) timed_out = true;
+            const int s = st % NSTG;
+            if (!mbar_wait_bounded(&full[s], (st / NSTG) & 1, wait_limit)) timed_out = true;
+            if (!mbar_wait_bounded(&a_ready[s], (st / NSTG) & 1, wait_limit)) timed_out = true;
             tc_fence_after();
             const uint64_t bd = sw128_desc(base + s * L::kStage);
             const uint32_t at = tmem + L::kACol + 32 * s;
@@ -416,8 +428,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             mbar_wait_bounded(accum, 0, kDrainLimit);
             const int n = *issued;  // only copies that were issued can be in flight
-            for (int st = n > kS16 ? n - kS16 : 0; st < n; ++st)
-                mbar_wait_bounded(&full[st % kS16], (st / kS16) & 1, kDrainLimit);
+            for (int st = n > NSTG ? n - NSTG : 0; st < n; ++st)
+                mbar_wait_bounded(&full[st % NSTG], (st / NSTG) & 1, kDrainLimit);
         }
         __syncwarp();
         tc_fence_after();
@@ -429,17 +441,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 std::mutex g_encode_mutex;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-cudaError_t make_qmap(CUtensorMap *map, const void *q, int M, int K, int BN, bool f16) {
-    {
-        std::lock_guard<std::mutex> lock(g_encode_mutex);
-        if (!g_encode) {
-            cudaDriverEntryPointQueryResult qr;
-            void *fn = nullptr;
-            cudaError_t e = cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &fn, cudaEnableDefault, &qr);
-            if (e != cudaSuccess || qr != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
-            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-        }
+// The driver's tensor-map encoder, looked up once.
+cudaError_t tensor_map_encoder() {
+    std::lock_guard<std::mutex> lock(g_encode_mutex);
+    if (!g_encode) {
+        cudaDriverEntryPointQueryResult qr;
+        void *fn = nullptr;
+        cudaError_t e = cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &fn, cudaEnableDefault, &qr);
+        if (e != cudaSuccess || qr != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
+    return cudaSuccess;
+}
+
+cudaError_t make_qmap(CUtensorMap *map, const void *q, int M, int K, int BN, bool f16) {
+    cudaError_t e0 = tensor_map_encoder();
+    if (e0 != cudaSuccess) return e0;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * (f16 ? 2u : 1u)};
     const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(BN)};
@@ -451,29 +468,46 @@ cudaError_t make_qmap(CUtensorMap *map, const void *q, int M, int K, int BN, boo
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int BN>
+// Tensor map of the packed weights (layout of bitlinear_packed_bytes): u64
+// [RGN][KT][64], boxes of 64 x 1 x 8.
+cudaError_t make_wmap(CUtensorMap *map, const uint8_t *packed, int RGN, int KT) {
+    cudaError_t e = tensor_map_encoder();
+    if (e != cudaSuccess) return e;
+    const cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(KT), static_cast<cuuint64_t>(RGN)};
+    const cuuint64_t strides[2] = {512u, static_cast<cuuint64_t>(KT) * 512u};
+    const cuuint32_t box[3] = {64u, 1u, 8u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<uint8_t *>(packed), dims, strides,
+                                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int BN, int NSTG, int MINB>
 cudaError_t launch16_bn(const void *q16, const float *tok_scale, const uint8_t *packed, const float *gamma,
                         int M, int N, int K, __nv_bfloat16 *out, int32_t *acc_out, cudaStream_t st,
                         uint32_t wait_limit) {
     const int KT = (K + 127) / 128;
     const int RGN = (N + 15) / 16;
-    const uint32_t smem = Smem16<BN>::kBytes;
+    const uint32_t smem = Smem16<BN, NSTG>::kBytes;
     static bool configured[64] = {false};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        e = cudaFuncSetAttribute(gemm16_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(gemm16_kernel<BN, NSTG, MINB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    CUtensorMap qmap;
+    CUtensorMap qmap, wmap;
     e = make_qmap(&qmap, q16, M, K, BN, true);
     if (e != cudaSuccess) return e;
+    e = make_wmap(&wmap, packed, RGN, KT);
+    if (e != cudaSuccess) return e;
     const dim3 grid((RGN + 7) / 8, (M + BN - 1) / BN);
-    return launch_pdl(gemm16_kernel<BN>, grid, dim3(kThreads), smem, st, 1, qmap, tok_scale, packed, gamma,
+    return launch_pdl(gemm16_kernel<BN, NSTG, MINB>, grid, dim3(kThreads), smem, st, 1, qmap, wmap, tok_scale, packed, gamma,
                       M, N, K, KT, RGN, out, acc_out, wait_limit);
 }
 
@@ -495,11 +529,13 @@ cudaError_t launch_bn(const int8_t *q, const float *tok_scale, const uint8_t *pa
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    CUtensorMap qmap;
+    CUtensorMap qmap, wmap;
     e = make_qmap(&qmap, q, M, K, BN, false);
     if (e != cudaSuccess) return e;
+    e = make_wmap(&wmap, packed, RGN, KT);
+    if (e != cudaSuccess) return e;
     const dim3 grid((RGN + 7) / 8, (M + BN - 1) / BN);
-    return launch_pdl(gemm_kernel<BN>, grid, dim3(kThreads), smem, st, 1, qmap, tok_scale, packed, gamma,
+    return launch_pdl(gemm_kernel<BN>, grid, dim3(kThreads), smem, st, 1, qmap, wmap, tok_scale, packed, gamma,
                       M, N, K, KT, RGN, out, acc_out, wait_limit);
 }
 
@@ -508,9 +544,9 @@ cudaError_t launch_bn(const int8_t *q, const float *tok_scale, const uint8_t *pa
 cudaError_t launch_gemm16(const void *q16, const float *tok_scale, const uint8_t *packed,
                           const float *gamma, int M, int N, int K, __nv_bfloat16 *out,
                           int32_t *acc_out, cudaStream_t st, uint32_t wait_limit) {
-    if (M <= 64) return launch16_bn<64>(q16, tok_scale, packed, gamma, M, N, K, out, acc_out, st, wait_limit);
-    if (M <= 128) return launch16_bn<128>(q16, tok_scale, packed, gamma, M, N, K, out, acc_out, st, wait_limit);
-    return launch16_bn<256>(q16, tok_scale, packed, gamma, M, N, K, out, acc_out, st, wait_limit);
+    if (M <= 64) return launch16_bn<64, 6, 1>(q16, tok_scale, packed, gamma, M, N, K, out, acc_out, st, wait_limit);
+    if (M <= 128) return launch16_bn<128, 6, 1>(q16, tok_scale, packed, gamma, M, N, K, out, acc_out, st, wait_limit);
+    return launch16_bn<256, 6, 1>(q16, tok_scale, packed, gamma, M, N, K, out, acc_out, st, wait_limit);
 }
 
 cudaError_t launch_gemm(const int8_t *q, const float *tok_scale, const uint8_t *packed,
