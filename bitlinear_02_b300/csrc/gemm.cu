@@ -541,11 +541,30 @@ cudaError_t launch_bn(const int8_t *q, const float *tok_scale, const uint8_t *pa
 
 }  // namespace
 
+// Token tile (MMA N) of the f16 GEMM for M > 128, one CTA per SM holding a
+// 128-row x BN tile: 256, or 192 where that takes fewer whole waves.  A 64-k
+// stage costs about the same down to BN = 192 (its copies and weight
+// conversion set a floor), so a narrower tile pays only where the wave count
+// drops: e.g. N = 2560 (20 row tiles) at M = 4096 gives 320 tiles with
+// BN = 256 (2.2 waves, three paid) and 440 with BN = 192 (three full waves).
+int token_tile(int M, int N) {
+    int sms = 148, dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t row_tiles = (N + 127) / 128;
+    auto cost = [&](int bn) {  // whole waves x a per-tile time with a large fixed part
+        const int64_t tiles = row_tiles * ((M + bn - 1) / bn);
+        return (tiles + sms - 1) / sms * (bn + 64);
+    };
+    return cost(192) < cost(256) ? 192 : 256;
+}
+
 cudaError_t launch_gemm16(const void *q16, const float *tok_scale, const uint8_t *packed,
                           const float *gamma, int M, int N, int K, __nv_bfloat16 *out,
                           int32_t *acc_out, cudaStream_t st, uint32_t wait_limit) {
     if (M <= 64) return launch16_bn<64, 6, 1>(q16, tok_scale, packed, gamma, M, N, K, out, acc_out, st, wait_limit);
     if (M <= 128) return launch16_bn<128, 6, 1>(q16, tok_scale, packed, gamma, M, N, K, out, acc_out, st, wait_limit);
+    if (token_tile(M, N) == 192)
+        return launch16_bn<192, 6, 1>(q16, tok_scale, packed, gamma, M, N, K, out, acc_out, st, wait_limit);
     return launch16_bn<256, 6, 1>(q16, tok_scale, packed, gamma, M, N, K, out, acc_out, st, wait_limit);
 }
 
