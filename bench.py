@@ -77,6 +77,37 @@ def dist_info():
     return ws, rank, local
 
 
+def replica_group(backend="nccl", device=None):
+    """N > 1 (one process per GPU, torchrun environment): join the process
+    group and return torch.distributed; None at N = 1.  The group carries
+    only the barrier around the timed region and the max over ranks of its
+    time: every rank runs its own replica of the whole workload."""
+    ws, _, _ = dist_info()
+    if ws == 1:
+        return None
+    import torch.distributed as dist
+    if backend == "nccl" and device is not None:
+        dist.init_process_group(backend, device_id=device)
+    else:
+        dist.init_process_group(backend)
+    return dist
+
+
+def max_over_ranks(torch, ms, device, dist):
+    """The slowest rank's time of the timed region (ms)."""
+    if dist is None:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(bytes_step, steps, ws, ms):
+    """Whole-job GB/s: ws replicas each ran `steps` steps of bytes_step
+    algorithmic bytes within the slowest rank's ms (weak scaling)."""
+    return bytes_step * steps * ws / (ms * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------ clocks ------
 
 class ClockSampler:
@@ -682,11 +713,8 @@ def main():
     ws, rank, local = dist_info()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    barrier = None
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-        barrier = lambda: dist.barrier()
+    dist = replica_group("nccl", dev)
+    barrier = (lambda: dist.barrier()) if dist is not None else None
     bl.load_library()
     hbm_peak, bf16_peak, bf16_sust, peak_kind = peaks()
     stream = torch.cuda.Stream()
@@ -698,14 +726,9 @@ def main():
     with sampler:
         ms = time_graphs(torch, [graph], args.steps, args.warmup, stream, barrier)
     clocks = sampler.summary()
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(torch, ms, dev, dist)
     assert bl.bitlinear_check_status() == bl.OK, "a bounded wait expired during the timed steps"
-    total_bytes = db.bytes_step * args.steps * ws
-    value = total_bytes / (ms * 1e-3) / 1e9
+    value = job_value(db.bytes_step, args.steps, ws, ms)
     ms_step = ms / args.steps
     del graph
 
@@ -796,8 +819,7 @@ def main():
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
-    if ws > 1:
-        import torch.distributed as dist
+    if dist is not None:
         dist.destroy_process_group()
     return 0
 
