@@ -254,7 +254,15 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 3) fused_gemv_kerne
         *st = kPending;
     }
     __syncthreads();
-    unsigned ticket = 0u;  // taken once every thread's reads of the accumulator are done
+    // Ticket: taken after the barrier, so after every thread of this CTA has
+    // consumed the values it loaded from the accumulator.  The last CTA's
+    // clearing stores are issued only after its own atomic has returned the
+    // final count, which includes this increment.  By then no CTA's load of
+    // the accumulator is still pending.  The atomic is relaxed and its result
+    // is needed only at the CTA's end, so it stays off the critical path.
+    // (A release here would first wait for this thread's weight loads still in
+    // flight.)
+    unsigned ticket = 0u;
     if (pend && threadIdx.x == 0) ticket = atomicAdd(xs_u + kOffTicket, 1u);
 #pragma unroll
     for (int jj = 0; jj < NT; ++jj) {
