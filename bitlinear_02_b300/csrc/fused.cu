@@ -521,7 +521,6 @@ extern "C" bitlinear_status_t bitlinear_forward_fused(const void *x_bf16, void *
     FArgs A{};
     A.x = static_cast<const __nv_bfloat16 *>(x_bf16);
     A.xs = static_cast<float *>(x_stats);
-    if (status_word(&A.status) != cudaSuccess) return BITLINEAR_ERR_CUDA;
     A.nproj = nproj;
     A.M = static_cast<int>(M);
     A.K = static_cast<int>(K);
@@ -550,6 +549,8 @@ extern "C" bitlinear_status_t bitlinear_forward_fused(const void *x_bf16, void *
         rbs = P.rb1;
     }
     if (rbs > 65535) return BITLINEAR_ERR_UNSUPPORTED;
+    // every argument is checked: only now the first CUDA call
+    if (status_word(&A.status) != cudaSuccess) return BITLINEAR_ERR_CUDA;
     // K split over a cluster of S CTAs (combined in distributed shared memory)
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

@@ -99,6 +99,47 @@ def test_quant_and_pack_reject_bad_arguments(lib):
     assert L.bitlinear_pack_ternary(P(FAKE), 4, 32, P(FAKE + 4), None) == bl.ERR_INVALID_ARG
 
 
+def test_fused_entry_points_reject_bad_arguments(lib):
+    L = lib
+    P = ctypes.c_void_p
+    assert L.bitlinear_fused_stats_bytes() == 2304
+    assert "pending factor buffer" in bl.bitlinear_status_string(bl.ERR_STATE)
+    # bitlinear_act_stats(x, M, K, eps, stats, stream)
+    assert L.bitlinear_act_stats(P(FAKE), 0, 64, 1e-5, P(FAKE), None) == bl.ERR_INVALID_ARG
+    assert L.bitlinear_act_stats(P(FAKE), 17, 64, 1e-5, P(FAKE), None) == bl.ERR_INVALID_ARG
+    assert L.bitlinear_act_stats(P(FAKE), 4, 72 + 4, 1e-5, P(FAKE), None) == bl.ERR_INVALID_ARG
+    assert L.bitlinear_act_stats(None, 4, 64, 1e-5, P(FAKE), None) == bl.ERR_INVALID_ARG
+    assert L.bitlinear_act_stats(P(FAKE), 4, 64, 1e-5, P(FAKE + 4), None) == bl.ERR_INVALID_ARG
+    # bitlinear_fused_factors(stats, M, K, eps, consume, c_out, ts_out, stream)
+    assert L.bitlinear_fused_factors(P(FAKE), 0, 64, 1e-5, 0, None, None, None) == bl.ERR_INVALID_ARG
+    assert L.bitlinear_fused_factors(P(FAKE), 17, 64, 1e-5, 0, None, None, None) == bl.ERR_INVALID_ARG
+    assert L.bitlinear_fused_factors(None, 4, 64, 1e-5, 0, None, None, None) == bl.ERR_INVALID_ARG
+    assert L.bitlinear_fused_factors(P(FAKE), 4, 64, 1e-5, 0, P(FAKE + 2), None, None) == bl.ERR_INVALID_ARG
+
+    # bitlinear_forward_fused(x, x_stats, M, K, nproj, projs, eps, stream)
+    def proj(N=64, packed=FAKE, gamma=FAKE, out=FAKE, acc=None, stats=None):
+        return bl.FusedProj(packed, gamma, N, out, acc, stats)
+
+    def call(projs, M=4, K=256, x=FAKE, xs=FAKE + 4096):
+        arr = (bl.FusedProj * max(1, len(projs)))(*projs)
+        return L.bitlinear_forward_fused(P(x) if x else None, P(xs) if xs else None, M, K, len(projs), arr,
+                                         1e-5, None)
+
+    good = proj(stats=FAKE + 8192)
+    assert call([good], M=0) == bl.ERR_INVALID_ARG
+    assert call([good], M=17) == bl.ERR_INVALID_ARG
+    assert call([good], K=250) == bl.ERR_INVALID_ARG
+    assert call([good], x=0) == bl.ERR_INVALID_ARG
+    assert call([good], xs=FAKE + 8) == bl.ERR_INVALID_ARG                  # misaligned factor buffer
+    assert call([]) == bl.ERR_INVALID_ARG                                   # no projection
+    assert call([good] * 5) == bl.ERR_INVALID_ARG                           # more than four
+    assert call([proj(N=0)]) == bl.ERR_INVALID_ARG
+    assert call([proj(packed=0)]) == bl.ERR_INVALID_ARG
+    assert call([proj(out=FAKE + 2)]) == bl.ERR_INVALID_ARG                 # misaligned output
+    assert call([proj(stats=FAKE + 4096)]) == bl.ERR_INVALID_ARG            # output factors = input factors
+    assert call([good, good]) == bl.ERR_INVALID_ARG                         # two outputs, one factor buffer
+
+
 def test_python_binding_raises_on_error(lib):
     with pytest.raises(bl.BitLinearError) as ei:
         bl._check(bl.ERR_INVALID_ARG, "bitlinear_forward")
