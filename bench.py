@@ -30,6 +30,8 @@ chain, unfused: the same stack through the persistent fused-chain kernel
 sweep: the decode GEMV shape by shape (bitlinear_forward on a pre-quantised
          input, every launch reading its weights from HBM after an L2 flush),
          and bitlinear_quant_act on its own.
+mid_m: batches of 32-256 tokens through the tensor-core GEMM, shape by shape
+         (the crossover with the decode GEMV).
 prefill: the 2B prefill chain at M = 4096 (int8-exact tensor-core GEMM), TOPS.
 cpu_baseline: the CPU oracle on a bounded sample of the same workload.
 
@@ -718,6 +720,57 @@ def gemv_sweep(torch, bl, db, stream, reps=9):
                          "note": "all shapes and M: algorithmic bytes / summed launch times"}}
 
 
+def midm_sweep(torch, bl, db, stream, reps=7, m_values=(32, 64, 128, 256)):
+    """Mid-size batches (16 < M < 512) through the tensor-core GEMM
+    (bitlinear_quant_act_f16 + bitlinear_forward_f16), measured like the
+    GEMV sweep: per (M, shape) a graph of back-to-back launches over the
+    stack's copies of that projection, replayed after an L2 flush.  Reports
+    per launch us, TFLOP/s and packed-weight GB/s, to place the crossover
+    with the decode GEMV (M <= 16)."""
+    T = torch
+    flush = T.empty(256 << 20, dtype=T.uint8, device=db.dev)
+    kinds = [("q,k,v,o", [0, 1, 2, 3]), ("gate,up", [4, 5]), ("down", [6])]
+    e0, e1 = T.cuda.Event(enable_timing=True), T.cuda.Event(enable_timing=True)
+    rows = []
+    for M in m_values:
+        for name, idxs in kinds:
+            _, N, K = db.shapes[idxs[0]]
+            x = db.inputs.activations_bf16(M, K, seed=700 + M, device=db.dev)
+            q, sc = bl.quant_act_f16(x, None, db.eps_a)
+            out = T.empty(M, N, dtype=T.bfloat16, device=db.dev)
+            mats = [db.w[7 * l + j] for l in range(db.layers) for j in idxs]
+
+            def run():
+                for packed, gamma, n in mats:
+                    bl.forward_f16(q, sc, packed, gamma, n, out=out)
+
+            with T.cuda.stream(stream):
+                run()
+            T.cuda.synchronize()
+            g = T.cuda.CUDAGraph()
+            with T.cuda.graph(g, stream=stream):
+                run()
+            ts = []
+            with T.cuda.stream(stream):
+                for _ in range(reps):
+                    flush.zero_()
+                    e0.record(stream)
+                    g.replay()
+                    e1.record(stream)
+                    e1.synchronize()
+                    ts.append(e0.elapsed_time(e1))
+            ms = statistics.median(ts) / len(mats)
+            wbytes = (-(-N // 16) * 16) * (-(-K // 128) * 128) // 4
+            rows.append({"M": M, "proj": name, "N": N, "K": K, "us": round(ms * 1e3, 3),
+                         "TFLOP/s": round(2 * M * N * K / (ms * 1e-3) / 1e12, 1),
+                         "weight_GB/s": round(wbytes / (ms * 1e-3) / 1e9, 1)})
+            del g
+    del flush
+    return {"mode": "bitlinear_quant_act_f16 + bitlinear_forward_f16 (tcgen05 GEMM), per (M, shape) a graph of "
+                    "launches over the stack's copies after a 256 MB L2 flush; median of "
+                    f"{reps} replays / launches", "rows": rows}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -793,6 +846,7 @@ def main():
     unf_ms = unfused_step_ms(torch, bl, db, stream)
     conc_ms = concurrent_step_ms(torch, bl, inputs, db)
     sweep = gemv_sweep(torch, bl, db, stream)
+    midm = midm_sweep(torch, bl, db, stream)
     for r in sweep["gemv"]:
         r["frac"] = round(r["GB/s"] / hbm_peak, 4)
     n_fused = FusedDecode.launches  # act_stats + 4 fused GEMVs per layer, per M
@@ -850,6 +904,7 @@ def main():
                     "value": round(db.bytes_step / (unf_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                     "mode": "bitlinear_quant_act + bitlinear_forward per projection, PDL-chained graph"},
         "sweep": sweep,
+        "mid_m": midm,
         "prefill": prefill,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d_bytes,
