@@ -35,7 +35,9 @@ def test_layer_bytes_match_the_chain():
     # one 2B layer: 19.8 MB of packed weights dominate
     w = sum(N * K // 4 for _, N, K in SHAPES_2B)
     assert w == 4 * 2560 * 2560 // 4 + 3 * 6912 * 2560 // 4 == 19_824_640
-    assert 0 < bench.layer_bytes(1, SHAPES_2B) - w < 100_000
+    # M = 1: forwards 4 x (2560 + 4 + 2*2560 + 4) + 2 x (2560 + 4 + 2*6912 + 4) + (6912 + 4 + 2*2560 + 4),
+    # quantisers 3 x (3*2560 + 4) + (3*6912 + 4)
+    assert bench.layer_bytes(1, SHAPES_2B) - w == 30_752 + 32_784 + 12_040 + 23_052 + 20_740
 
 
 def test_whole_job_value():
