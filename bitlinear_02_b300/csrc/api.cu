@@ -57,6 +57,11 @@ extern "C" void bitlinear_set_wait_limit(uint32_t iterations) {
     bl::g_wait_limit.store(iterations ? iterations : bl::kDefaultWaitLimit);
 }
 
+// Batches up to this size run on the decode GEMV engine (16-token chunks in
+// one launch); larger ones on the tensor-core GEMM, whose 128-row tiles
+// leave most SMs idle below a few hundred tokens.
+constexpr int64_t kGemvMaxM = 64;
+
 extern "C" bitlinear_status_t bitlinear_forward(const int8_t *q, const float *tok_scale,
                                                 const uint8_t *packed, const float *gamma,
                                                 int64_t M, int64_t N, int64_t K, void *out_bf16,
@@ -70,12 +75,12 @@ extern "C" bitlinear_status_t bitlinear_forward(const int8_t *q, const float *to
     if (!aligned16(q) || !aligned4(tok_scale) || !aligned16(packed) || !aligned4(gamma) ||
         !aligned16(out_bf16) || (acc_out && !aligned16(acc_out)))
         return BITLINEAR_ERR_INVALID_ARG;
-    if ((N + 15) / 16 > 65535 * 4 && M <= 16) return BITLINEAR_ERR_UNSUPPORTED;
+    if ((N + 15) / 16 > 65535 * 4 && M <= kGemvMaxM) return BITLINEAR_ERR_UNSUPPORTED;
     if ((M + 63) / 64 > 65535) return BITLINEAR_ERR_UNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     auto *out = static_cast<__nv_bfloat16 *>(out_bf16);
     cudaError_t e;
-    if (M <= 16)
+    if (M <= kGemvMaxM)  // the decode GEMV, in 16-token chunks above 16
         e = launch_gemv(q, tok_scale, packed, gamma, static_cast<int>(M), static_cast<int>(N),
                         static_cast<int>(K), out, acc_out, st, num_sms());
     else

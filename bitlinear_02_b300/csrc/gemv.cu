@@ -48,6 +48,16 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
     __shared__ int32_t part[kWarps][NT * 8][kRows];
     __shared__ int32_t total[NT * 8 * kRows];
 
+    // Batches of up to 64 tokens: blockIdx.z picks a 16-token chunk (its rows
+    // of q, scales and outputs); the chunks share the weights through L2.
+    {
+        const int z = static_cast<int>(blockIdx.z);
+        q += static_cast<int64_t>(z) * 16 * K;
+        tok_scale += 16 * z;
+        out += static_cast<int64_t>(z) * 16 * N;
+        if (acc_out) acc_out += static_cast<int64_t>(z) * 16 * N;
+        M = min(16, M - 16 * z);
+    }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const int rb = blockIdx.y;
@@ -189,14 +199,15 @@ cudaError_t launch_gemv(const int8_t *q, const float *tok_scale, const uint8_t *
     const int KT = (K + 127) / 128;
     const int RGN = (N + 15) / 16;
     const int RB = (RGN + kGroups - 1) / kGroups;
-    int S = (2 * num_sms + RB - 1) / RB;
+    const int Z = (M + 15) / 16;  // 16-token chunks (M <= 64)
+    int S = (2 * num_sms + RB * Z - 1) / (RB * Z);
     const int smax = KT / kWarps > 1 ? KT / kWarps : 1;
     if (S > smax) S = smax;
     if (S > 8) S = 8;
     if (S < 1) S = 1;
     int tpc = (KT + S - 1) / S;
     S = (KT + tpc - 1) / tpc;
-    const dim3 grid(S, RB), block(kWarps * 32);
+    const dim3 grid(S, RB, Z), block(kWarps * 32);
     if (M <= 8)
         return launch_pdl(gemv_kernel<1>, grid, block, 0, st, S, q, tok_scale, packed, gamma, M, N, K,
                           KT, RGN, tpc, out, acc_out);

@@ -190,9 +190,10 @@ BITLINEAR_API bitlinear_status_t bitlinear_quant_act(const void *x_bf16, const v
  * cudaStreamWaitEvent.  Do not write it with a kernel of your own launched
  * immediately before this call on the same stream: launch that kernel on
  * another stream and join the streams with an event instead.
- * Engine choice is internal: M <= 16 runs the decode GEMV (legacy tensor
- * MMA on register-unpacked codes, HBM-bound), larger M runs the prefill
- * GEMM (tcgen05 MMA with TMEM accumulators).  Both give identical results.
+ * Engine choice is internal: M <= 64 runs the decode GEMV (legacy tensor
+ * MMA on register-unpacked codes; above 16 tokens in 16-token chunks of one
+ * launch), larger M runs the prefill GEMM (tcgen05 MMA with TMEM
+ * accumulators).  Both give identical results.
  * Every bounded wait inside the GEMM that expires sets a device status
  * word; bitlinear_check_status reports it.
  * Errors: INVALID_ARG (null/misaligned pointer, M < 0, N < 1, K < 16,

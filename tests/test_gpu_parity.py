@@ -323,7 +323,7 @@ def test_invalid_arguments_raise():
 
 
 def test_bounded_wait_timeout_is_reported_and_recovers():
-    N, K, M = 256, 1024, 64
+    N, K, M = 256, 1024, 65  # above the GEMV's 64 tokens: the GEMM, whose waits are bounded
     w = inputs.weights_fp32(N, K, seed=9)
     x = inputs.activations_bf16(M, K, seed=10)
     assert bl.bitlinear_check_status() == bl.OK
