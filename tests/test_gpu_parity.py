@@ -163,6 +163,15 @@ def test_decode_gemv_parity(M, N, K):
     check_full(w, x)
 
 
+@pytest.mark.parametrize("M", [18, 33, 48, 63])
+@pytest.mark.parametrize("N,K", [(512, 256), (200, 8640), (2560, 2560)])
+def test_chunked_gemv_parity(M, N, K):
+    # 16 < M <= 64: the decode GEMV in 16-token chunks (a partial last chunk included)
+    w = inputs.weights_fp32(N, K, seed=17 * N + K)
+    x = inputs.activations_bf16(M, K, seed=19 * M + K)
+    check_full(w, x)
+
+
 @pytest.mark.parametrize("M", [17, 64, 65, 128, 129, 200, 256, 300])
 @pytest.mark.parametrize("N,K", [(512, 256), (200, 8640), (144, 144), (1040, 1280)])
 def test_prefill_gemm_parity(M, N, K):
