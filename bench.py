@@ -1,39 +1,38 @@
 """Benchmark of the BitLinear hot path on B300 (one JSON line on stdout).
 
-Workload (default): one decode step of a stack of 2B-shaped layers, for
-M = 1, 4 and 16 tokens.  A layer has the seven projections q/k/v/o
-2560x2560, gate/up 2560->6912 and down 6912->2560, chained through the
-fused RMSNorm + absmax int8 quantiser:
+Headline workload (``value``): one decode step of a stack of 2B-shaped
+layers, for M = 1, 4 and 16 tokens.  A layer has the seven projections
+q/k/v/o 2560x2560, gate/up 2560->6912 and down 6912->2560, chained through
+the fused RMSNorm + absmax int8 quantiser:
     h = x; q,k,v = f(h); o = f(v); gate,up = f(o); down = f(up); next x = down
 The stack has LAYERS = 20 layers: 396 MB of packed 2-bit weights, the
 0.4 GB the asi.tokyo write-up gives for the 2B model's weights, and more
 than 3x the 126 MB L2, so every weight byte is read from HBM.  Each M runs
 the whole stack; a step is all of it for the three M, replayed as one CUDA
-graph.
-
-The step runs the fused decode path: per M one bitlinear_act_stats of the
-stack input, then per layer four bitlinear_forward_fused launches
+graph.  The step runs the fused decode path: per M one bitlinear_act_stats
+of the stack input, then per layer four bitlinear_forward_fused launches
 (q,k,v | o | gate,up | down), each quantising its input on the fly.
 
-value  = algorithmic bytes of the step (packed weights, activations in and
-         out, scales; the same count as the unfused quant + forward calls)
-         / device time, summed over ranks.
-e2e    = the same bytes / wall time of steps that also copy each M's input
-         from pinned host memory and read the last projection's output back.
-roofline: the fused decode GEMV, bytes per launch / average launch time.
-concurrent: the three M as independent decode streams (a graph branch per M,
-         each with its own weight copy), the throughput when their dependent
-         launches overlap.
-chain, unfused: the same stack through the persistent fused-chain kernel
-         (bitlinear_chain_run, one launch per M) and through separate
-         bitlinear_quant_act + bitlinear_forward calls, for comparison.
-sweep: the decode GEMV shape by shape (bitlinear_forward on a pre-quantised
-         input, every launch reading its weights from HBM after an L2 flush),
-         and bitlinear_quant_act on its own.
-mid_m: batches of 32-256 tokens through the tensor-core GEMM, shape by shape
-         (the crossover with the decode GEMV).
-prefill: the 2B prefill chain at M = 4096 (int8-exact tensor-core GEMM), TOPS.
-cpu_baseline: the CPU oracle on a bounded sample of the same workload.
+value    = algorithmic bytes of the step (packed weights, activations in and
+           out, scales; the count of the unfused quant + forward calls)
+           / device time, summed over ranks.
+e2e      = the same bytes / wall time of steps made of the public entry
+           points called one by one from the host (their host cost
+           included), with each M's input copied from pinned host memory and
+           the last output read back every step; `e2e.graph` is the same
+           step replayed as a CUDA graph.
+roofline = the fused decode kernel: bytes per launch / average launch time.
+configs  = every workload of the build: the small layer, the 2B decode
+           stack per M, the 2B prefill GEMMs (M = 512, 2048, 4096, both
+           activation entry points), and the 3B (26 layers) and 70B (80
+           layers) stacks' decode steps at every M, with tokens/s and
+           roofline fractions.  The stacks' ternary weights are drawn on the
+           device by a counter-based generator.
+sweep    = the decode GEMV shape by shape (2B, 3B and 70B shapes, every
+           launch reading its weights from HBM after an L2 flush).
+mid_m    = 32-256 tokens through bitlinear_forward and the f16 GEMM.
+cpu_baseline = the CPU oracle on a bounded sample of the same workload,
+           single-threaded and on all host cores.
 
 --impl reference times the CPU oracle (the reference arm of this build) on
 the same workload and prints the same kind of line.
@@ -57,13 +56,11 @@ METRIC = "BitLinear decode GB/s (% HBM peak) and prefill int8 TOPS, 2B-shape lay
 WORKLOAD = "decode_2b"
 M_LIST = (1, 4, 16)
 LAYERS = 20
-# DRAM bytes read per packed-weight byte by fused_gemv_kernel, from one ncu
-# capture (profiles/fused_gemv_decode_2b_M16_full.md: 15.826 MB read over
-# three launches holding 15.400 MB of packed weights).  Re-measure when the
-# kernel changes.
-FUSED_DRAM_PER_PACKED_BYTE = 1.0277
 FALLBACK_HBM_GBS = 6400.0
 FALLBACK_BF16_TFLOPS = 1800.0
+# DRAM bytes per packed-weight byte of the fused decode kernel, from an ncu
+# capture of its launches (profiles/), or None when the kernel changed since.
+FUSED_DRAM_PER_PACKED_BYTE = None
 
 
 def peaks():
@@ -116,7 +113,9 @@ def job_value(bytes_step, steps, ws, ms):
 # ------------------------------------------------------------ clocks ------
 
 class ClockSampler:
-    """nvidia-smi samples during the timed region (clocks, throttle reasons)."""
+    """nvidia-smi samples while GPU work is timed (clocks, throttle reasons).
+    `mark(True/False)` brackets timed regions; samples outside are dropped;
+    `take()` returns (and forgets) the samples kept since the last take."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -125,6 +124,8 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
+        self.all = []
+        self.active = False
 
     def __enter__(self):
         try:
@@ -138,9 +139,18 @@ class ClockSampler:
             self.proc = None
         return self
 
+    def mark(self, on: bool):
+        self.active = on
+
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            if self.active:
+                self.lines.append(line.strip())
+                self.all.append(line.strip())
+
+    def take(self):
+        out, self.lines = self.lines, []
+        return out
 
     def __exit__(self, *a):
         if self.proc:
@@ -150,10 +160,11 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self):
+    @staticmethod
+    def summary(lines):
         sm, mx, reasons = [], 0.0, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in self.lines:
+        for l in lines:
             f = [x.strip() for x in l.split(",")]
             if len(f) < 9:
                 continue
@@ -171,35 +182,33 @@ class ClockSampler:
 
 # ------------------------------------------------------------ workload ----
 
+def packed_bytes(N, K):
+    return (-(-N // 16) * 16) * (-(-K // 128) * 128) // 4
+
+
 def algo_bytes_forward(M, N, K):
-    Np, Kp = -(-N // 16) * 16, -(-K // 128) * 128
-    return Np * Kp // 4 + M * K + 4 * M + 2 * M * N + 4
+    return packed_bytes(N, K) + M * K + 4 * M + 2 * M * N + 4
 
 
 def algo_bytes_quant(M, K):
     return 2 * M * K + M * K + 4 * M
 
 
-def chain_plan(shapes):
-    """(kind, args) list for one layer: quant/forward with buffer names."""
+def chain_plan(shapes, o_from="v"):
+    """(kind, input, output) list for one layer, with the shapes by name."""
     d = {n: (N, K) for n, N, K in shapes}
     return [
         ("quant", "x", "h0"),
         ("fwd", "h0", "q"), ("fwd", "h0", "k"), ("fwd", "h0", "v"),
-        ("quant", "v", "h1"), ("fwd", "h1", "o"),
+        ("quant", o_from, "h1"), ("fwd", "h1", "o"),
         ("quant", "o", "h2"), ("fwd", "h2", "gate"), ("fwd", "h2", "up"),
         ("quant", "up", "h3"), ("fwd", "h3", "down"),
     ], d
 
 
-# projection inputs within a layer (chain slots relative to the layer):
-# 0 = the layer input, i + 1 = output of the layer's projection i
-LAYER_INPUTS = [0, 0, 0, 3, 4, 4, 6]
-
-
-def layer_bytes(M, shapes):
+def layer_bytes(M, shapes, o_from="v"):
     """Algorithmic bytes of one layer at M tokens (unfused-path count)."""
-    plan, dims = chain_plan(shapes)
+    plan, dims = chain_plan(shapes, o_from)
     width = {"x": dims["q"][1]}
     width.update({n: N for n, N, K in shapes})
     b = 0
@@ -212,185 +221,320 @@ def layer_bytes(M, shapes):
     return b
 
 
-class DecodeBench:
-    """The decode stack: LAYERS x 7 packed projections shared by every M."""
-
-    def __init__(self, torch, bl, inputs, dev, layers=LAYERS):
-        self.torch, self.bl, self.inputs, self.dev = torch, bl, inputs, dev
-        wl = inputs.WORKLOADS[WORKLOAD]
-        self.shapes = wl["shapes"]
-        self.layers = layers
-        self.eps_w, self.eps_a = wl["eps_w"], wl["eps_a"]
-        self.hidden = self.shapes[0][2]
-        self.w = []  # (packed, gamma, N) per projection, layer-major
-        for l in range(layers):
-            for i, (name, N, K) in enumerate(self.shapes):
-                W = inputs.weights_fp32(N, K, seed=wl["seed"] * 100000 + l * 10 + i, device=dev)
-                packed, gamma = bl.pack_weights(W, self.eps_w)
-                del W
-                self.w.append((packed, gamma, N))
-        self.packed_bytes = sum(p.numel() for p, _, _ in self.w)
-        self.x = {M: inputs.activations_bf16(M, self.hidden, seed=wl["seed"] * 7 + M, device=dev)
-                  for M in M_LIST}
-        self.chains = {}
-        for M in M_LIST:
-            projs = []
-            for l in range(layers):
-                base = 7 * l
-                for i, rel in enumerate(LAYER_INPUTS):
-                    slot = (base if l > 0 else 0) if rel == 0 else base + rel
-                    p, g, N = self.w[base + i]
-                    projs.append(dict(packed=p, gamma=g, N=N, input=slot))
-            self.chains[M] = bl.DecodeChain(M, self.hidden, projs, eps=self.eps_a)
-        self.bytes_per_M = {M: layer_bytes(M, self.shapes) * layers for M in M_LIST}
-        self.bytes_step = sum(self.bytes_per_M.values())
-        self.launches = len(M_LIST)
-        torch.cuda.synchronize()
-
-    def run_step(self, stream, h2d=None, d2h=None):
-        for M in M_LIST:
-            if h2d is not None:
-                self.x[M].copy_(h2d[M], non_blocking=True)
-            self.chains[M].run(self.x[M], stream)
-            if d2h is not None:
-                d2h[M].copy_(self.chains[M].out[-1], non_blocking=True)
-
-    def capture(self, stream, h2d=None, d2h=None):
-        torch = self.torch
-        with torch.cuda.stream(stream):  # one eager step: host-side set-up happens outside capture
-            self.run_step(stream)
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            self.run_step(stream, h2d, d2h)
-        return g
-
-
-def time_graphs(torch, graphs, steps, warmup, stream, barrier=None):
+def time_graphs(torch, graphs, steps, warmup, stream, barrier=None, clock=None):
     for i in range(warmup):
         graphs[i % len(graphs)].replay()
     torch.cuda.synchronize()
     if barrier:
         barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if clock:
+        clock.mark(True)
     with torch.cuda.stream(stream):
         e0.record(stream)
         for i in range(steps):
             graphs[(warmup + i) % len(graphs)].replay()
         e1.record(stream)
     e1.synchronize()
+    if clock:
+        clock.mark(False)
     torch.cuda.synchronize()
     if barrier:
         barrier()
     return e0.elapsed_time(e1)  # ms
 
 
-def unfused_step_ms(torch, bl, db, stream, reps=5):
-    """The same stack through the per-projection entry points: per layer
-    h0 = quant(x); q,k,v = fwd(h0); h1 = quant(v); o = fwd(h1);
-    h2 = quant(o); gate,up = fwd(h2); h3 = quant(up); down = fwd(h3),
-    chained with programmatic dependent launch in one CUDA graph.  Returns
-    ms per step (all M)."""
-    T = torch
-    bufs = {}
-    for M in M_LIST:
-        outs = [T.empty(M, N, dtype=T.bfloat16, device=db.dev) for _, N, _ in db.shapes]
-        hs = [(T.empty(M, K, dtype=T.int8, device=db.dev), T.empty(M, dtype=T.float32, device=db.dev))
-              for K in (db.hidden, db.shapes[2][1], db.shapes[3][1], db.shapes[5][1])]
-        bufs[M] = (outs, hs)
-    # (projection index, quantised input index) per layer; quant steps before them
-    order = [("quant", 0, None), ("fwd", 0, 0), ("fwd", 1, 0), ("fwd", 2, 0), ("quant", 1, 2), ("fwd", 3, 1),
-             ("quant", 2, 3), ("fwd", 4, 2), ("fwd", 5, 2), ("quant", 3, 5), ("fwd", 6, 3)]
-
-    def step():
-        for M in M_LIST:
-            outs, hs = bufs[M]
-            for l in range(db.layers):
-                for kind, a, b in order:
-                    if kind == "quant":
-                        src = (db.x[M] if l == 0 else outs[6]) if a == 0 else outs[b]
-                        q, sc = hs[a]
-                        bl.bitlinear_quant_act(src, None, M, src.shape[1], db.eps_a, q, sc)
-                    else:
-                        packed, gamma, N = db.w[7 * l + a]
-                        q, sc = hs[b]
-                        bl.bitlinear_forward(q, sc, packed, gamma, M, N, q.shape[1], outs[a])
-
-    with T.cuda.stream(stream):
-        step()
-    T.cuda.synchronize()
-    g = T.cuda.CUDAGraph()
-    with T.cuda.graph(g, stream=stream):
-        step()
-    ms = time_graphs(T, [g], reps, 2, stream)
-    del g, bufs
-    return ms / reps
+def capture(torch, fn, stream):
+    """One eager run (host-side set-up happens outside capture), then a graph."""
+    with torch.cuda.stream(stream):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
 
 
-class FusedDecode:
-    """The decode stack through the fused path: per M one bitlinear_act_stats
-    of the stack input, then per layer four bitlinear_forward_fused launches
-    (q,k,v | o | gate,up | down), each quantising its input on the fly."""
+class Stack:
+    """A decode stack: `layers` x 7 packed projections shared by every M.
 
-    def __init__(self, torch, bl, db, m_list=M_LIST):
-        self.torch, self.bl, self.db = torch, bl, db
-        T = torch
-        self.bufs = {}
-        self.m_list = tuple(m_list)
-        for M in self.m_list:
-            outs = [[T.empty(M, N, dtype=T.bfloat16, device=db.dev) for _, N, _ in db.shapes]
-                    for _ in range(db.layers)]
-            stats = [[bl.new_stats(db.dev) for _ in range(4)] for _ in range(db.layers)]  # v, o, up, down
-            x_stats = bl.new_stats(db.dev)
-            self.bufs[M] = (outs, stats, x_stats)
+    Workloads with master weights (the 2B ones) draw W ~ N(0, 0.02^2) and
+    absmean-pack it with bitlinear_pack_weights; the 3B and 70B stacks draw
+    ternary weights on the device with the counter-based generator of the
+    inputs module, pack them with bitlinear_pack_ternary, and take gamma ~
+    U(0.01, 0.05) per matrix.  o_from: the projection whose output feeds o
+    (v, or q where v is narrower than the hidden size)."""
 
-    def run_step(self, stream, h2d=None, d2h=None):
-        bl, db = self.bl, self.db
-        for M in self.m_list:
-            outs, stats, x_stats = self.bufs[M]
-            if h2d is not None:
-                db.x[M].copy_(h2d[M], non_blocking=True)
-            bl.bitlinear_act_stats(db.x[M], M, db.hidden, db.eps_a, x_stats, stream)
-            for l in range(db.layers):
-                o = outs[l]
-                st_v, st_o, st_up, st_down = stats[l]
-                x = db.x[M] if l == 0 else outs[l - 1][6]
-                xs = x_stats if l == 0 else stats[l - 1][3]
-
-                def fp(i, st=None):
-                    packed, gamma, N = db.w[7 * l + i]
-                    return bl.FusedProj(packed.data_ptr(), gamma.data_ptr(), N, o[i].data_ptr(), None,
-                                        st.data_ptr() if st is not None else None)
-
-                K = db.hidden
-                bl.bitlinear_forward_fused(x, xs, M, K, [fp(0), fp(1), fp(2, st_v)], db.eps_a, stream)
-                bl.bitlinear_forward_fused(o[2], st_v, M, o[2].shape[1], [fp(3, st_o)], db.eps_a, stream)
-                bl.bitlinear_forward_fused(o[3], st_o, M, o[3].shape[1], [fp(4), fp(5, st_up)], db.eps_a, stream)
-                # the last layer's output feeds nothing here: no factors for it
-                last = l == db.layers - 1
-                bl.bitlinear_forward_fused(o[5], st_up, M, o[5].shape[1], [fp(6, None if last else st_down)],
-                                           db.eps_a, stream)
-            if d2h is not None:
-                d2h[M].copy_(outs[-1][6], non_blocking=True)
-
-    def capture(self, stream, h2d=None, d2h=None):
-        torch = self.torch
-        with torch.cuda.stream(stream):
-            self.run_step(stream)
+    def __init__(self, torch, bl, inputs, dev, workload, layers=None):
+        self.torch, self.bl, self.inputs, self.dev = torch, bl, inputs, dev
+        wl = inputs.WORKLOADS[workload]
+        self.workload = workload
+        self.shapes = wl["shapes"]
+        self.layers = layers or wl.get("layers", LAYERS)
+        self.eps_a = wl["eps_a"]
+        self.hidden = self.shapes[0][2]
+        self.o_from = "v" if self.shapes[2][1] == self.hidden else "q"
+        self.o_src = [n for n, _, _ in self.shapes].index(self.o_from)
+        self.w = []  # (packed, gamma, N, K) per projection, layer-major
+        for l in range(self.layers):
+            for i, (name, N, K) in enumerate(self.shapes):
+                if "eps_w" in wl:
+                    W = inputs.weights_fp32(N, K, seed=wl["seed"] * 100000 + l * 10 + i, device=dev)
+                    packed, gamma = bl.pack_weights(W, wl["eps_w"])
+                    del W
+                else:
+                    wq = inputs.ternary_hash(N, K, inputs.stack_word(wl["seed"], l, i), device=dev)
+                    packed = bl.pack_ternary(wq)
+                    del wq
+                    g = inputs.gamma_uniform(wl["seed"] * 100000 + l * 10 + i)
+                    gamma = torch.tensor([g], dtype=torch.float32, device=dev)
+                self.w.append((packed, gamma, N, K))
         torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            self.run_step(stream, h2d, d2h)
-        return g
+        self.packed_bytes = sum(p.numel() for p, _, _, _ in self.w)
+        self.x = {}
 
-    launches = len(M_LIST) * (1 + 4 * LAYERS)
+    def input(self, M):
+        if M not in self.x:
+            self.x[M] = self.inputs.activations_bf16(M, self.hidden, seed=7 * M + 3, device=self.dev)
+        return self.x[M]
+
+    def bytes(self, M):
+        return layer_bytes(M, self.shapes, self.o_from) * self.layers
 
 
-def prefill_bench(torch, bl, inputs, dev, stream, steps=5, warmup=3, M=4096):
-    """2B prefill chain at M tokens (the seven projections chained through the
-    quantiser, f16-activation path: bitlinear_quant_act_f16 +
-    bitlinear_forward_f16): TOPS of the tensor-core GEMMs (2*M*N*K per
-    projection) and of the whole chain."""
+class FusedRunner:
+    """The stack through the fused decode path at M <= 16 tokens: one
+    bitlinear_act_stats of the stack input, then per layer four
+    bitlinear_forward_fused launches (q,k,v | o | gate,up | down), each
+    quantising its input on the fly."""
+
+    def __init__(self, st: Stack, M):
+        T, bl = st.torch, st.bl
+        self.st, self.M = st, M
+        self.outs = [[T.empty(M, N, dtype=T.bfloat16, device=st.dev) for _, N, _ in st.shapes]
+                     for _ in range(st.layers)]
+        self.stats = [[bl.new_stats(st.dev) for _ in range(4)] for _ in range(st.layers)]  # o_src, o, up, down
+        self.x_stats = bl.new_stats(st.dev)
+        self.launches = 1 + 4 * st.layers
+
+    def last_output(self):
+        return self.outs[-1][6]
+
+    def run(self, stream):
+        st, bl, M = self.st, self.st.bl, self.M
+        x0 = st.input(M)
+        bl.bitlinear_act_stats(x0, M, st.hidden, st.eps_a, self.x_stats, stream)
+        for l in range(st.layers):
+            o = self.outs[l]
+            s_src, s_o, s_up, s_down = self.stats[l]
+            x = x0 if l == 0 else self.outs[l - 1][6]
+            xs = self.x_stats if l == 0 else self.stats[l - 1][3]
+
+            def fp(i, sb=None):
+                packed, gamma, N, _ = st.w[7 * l + i]
+                return bl.FusedProj(packed.data_ptr(), gamma.data_ptr(), N, o[i].data_ptr(), None,
+                                    sb.data_ptr() if sb is not None else None)
+
+            qkv = [fp(i, s_src if i == st.o_src else None) for i in range(3)]
+            bl.bitlinear_forward_fused(x, xs, M, st.hidden, qkv, st.eps_a, stream)
+            src = o[st.o_src]
+            bl.bitlinear_forward_fused(src, s_src, M, src.shape[1], [fp(3, s_o)], st.eps_a, stream)
+            bl.bitlinear_forward_fused(o[3], s_o, M, o[3].shape[1], [fp(4), fp(5, s_up)], st.eps_a, stream)
+            last = l == st.layers - 1  # the last output feeds nothing here: no factors for it
+            bl.bitlinear_forward_fused(o[5], s_up, M, o[5].shape[1], [fp(6, None if last else s_down)],
+                                       st.eps_a, stream)
+
+
+class UnfusedRunner:
+    """The stack through the per-projection entry points at any M: per layer
+    h0 = quant(x); q,k,v = fwd(h0); h1 = quant(o_src); o = fwd(h1);
+    h2 = quant(o); gate,up = fwd(h2); h3 = quant(up); down = fwd(h3).
+    bitlinear_forward runs the decode GEMV up to 64 tokens and the tcgen05
+    GEMM above."""
+
+    def __init__(self, st: Stack, M):
+        T = st.torch
+        self.st, self.M = st, M
+        self.outs = [T.empty(M, N, dtype=T.bfloat16, device=st.dev) for _, N, _ in st.shapes]
+        widths = (st.hidden, st.shapes[st.o_src][1], st.shapes[3][1], st.shapes[5][1])
+        self.hs = [(T.empty(M, K, dtype=T.int8, device=st.dev), T.empty(M, dtype=T.float32, device=st.dev))
+                   for K in widths]
+        self.launches = 11 * st.layers
+
+    def last_output(self):
+        return self.outs[6]
+
+    def run(self, stream):
+        st, bl, M = self.st, self.st.bl, self.M
+        order = [("quant", 0, None), ("fwd", 0, 0), ("fwd", 1, 0), ("fwd", 2, 0), ("quant", 1, st.o_src),
+                 ("fwd", 3, 1), ("quant", 2, 3), ("fwd", 4, 2), ("fwd", 5, 2), ("quant", 3, 5), ("fwd", 6, 3)]
+        for l in range(st.layers):
+            for kind, a, b in order:
+                if kind == "quant":
+                    src = (st.input(M) if l == 0 else self.outs[6]) if a == 0 else self.outs[b]
+                    q, sc = self.hs[a]
+                    bl.bitlinear_quant_act(src, None, M, src.shape[1], st.eps_a, q, sc, stream)
+                else:
+                    packed, gamma, N, K = st.w[7 * l + a]
+                    q, sc = self.hs[b]
+                    bl.bitlinear_forward(q, sc, packed, gamma, M, N, K, self.outs[a], None, stream)
+
+
+def runner(st, M):
+    return FusedRunner(st, M) if M <= 16 else UnfusedRunner(st, M)
+
+
+def stack_rows(torch, st, m_list, stream, hbm_peak, reps, clock=None):
+    """Decode step per M through a stack: ms, GB/s, fraction, tokens/s."""
+    rows = []
+    for M in m_list:
+        r = runner(st, M)
+        g = capture(torch, lambda: r.run(stream), stream)
+        ms = time_graphs(torch, [g], reps, 3, stream, clock=clock) / reps
+        b = st.bytes(M)
+        gbs = b / (ms * 1e-3) / 1e9
+        rows.append({"M": M, "path": "fused" if M <= 16 else "quant_act + forward", "ms_per_step": round(ms, 4),
+                     "GB/s": round(gbs, 1), "frac": round(gbs / hbm_peak, 4),
+                     "tokens_per_s": round(M / (ms * 1e-3), 1), "launches": r.launches})
+        del g, r
+    return rows
+
+
+def gemv_sweep(torch, bl, inputs, dev, stream, hbm_peak, reps=7, m_list=M_LIST):
+    """The decode GEMV shape by shape: bitlinear_forward on a pre-quantised
+    input (the GEMV with its rescale epilogue), for the distinct projection
+    shapes of the 2B, 3B and 70B models.  Per (M, shape) one CUDA graph of
+    back-to-back launches over distinct copies of the packed matrix (at least
+    512 MB of them, so no launch finds its weights in L2), replayed right
+    after an L2 flush (a 256 MB write, outside the timed events).  Per-launch
+    time = median replay time / launches; GB/s = algorithmic bytes per
+    launch / that time."""
+    T = torch
+    flush = T.empty(256 << 20, dtype=T.uint8, device=dev)
+    e0, e1 = T.cuda.Event(enable_timing=True), T.cuda.Event(enable_timing=True)
+    shapes = [("2b", "q,k,v,o", 2560, 2560), ("2b", "gate,up", 6912, 2560), ("2b", "down", 2560, 6912),
+              ("3b", "q,k,v,o", 3200, 3200), ("3b", "gate,up", 8640, 3200), ("3b", "down", 3200, 8640),
+              ("70b", "q,o", 8192, 8192), ("70b", "k,v", 1024, 8192), ("70b", "gate,up", 28672, 8192),
+              ("70b", "down", 8192, 28672)]
+    rows = []
+    for si, (model, proj, N, K) in enumerate(shapes):
+        pb = packed_bytes(N, K)
+        ncopy = max(8, min(64, -(-(512 << 20) // pb)))
+        wq = inputs.ternary_hash(N, K, inputs.stack_word(9, 0, si), device=dev)
+        p0 = bl.pack_ternary(wq)
+        del wq
+        mats = [p0] + [p0.clone() for _ in range(ncopy - 1)]
+        gam = T.tensor([0.02], dtype=T.float32, device=dev)
+        for M in m_list:
+            x = inputs.activations_bf16(M, K, seed=900 + M, device=dev)
+            q, sc = bl.quant_act(x)
+            out = T.empty(M, N, dtype=T.bfloat16, device=dev)
+
+            def run():
+                for p in mats:
+                    bl.bitlinear_forward(q, sc, p, gam, M, N, K, out, None, stream)
+
+            g = capture(T, run, stream)
+            ts = []
+            with T.cuda.stream(stream):
+                for _ in range(reps):
+                    flush.zero_()
+                    e0.record(stream)
+                    g.replay()
+                    e1.record(stream)
+                    e1.synchronize()
+                    ts.append(e0.elapsed_time(e1))
+            ms = statistics.median(ts) / ncopy
+            b = algo_bytes_forward(M, N, K)
+            gbs = b / (ms * 1e-3) / 1e9
+            rows.append({"model": model, "proj": proj, "N": N, "K": K, "M": M, "us": round(ms * 1e3, 3),
+                         "GB/s": round(gbs, 1), "frac": round(gbs / hbm_peak, 4), "launches": ncopy})
+            del g
+        del mats, p0
+    del flush
+    T.cuda.empty_cache()
+    return {"mode": "per (shape, M): a graph of bitlinear_forward launches over distinct copies of the packed "
+                    "matrix on a pre-quantised input, replayed after a 256 MB L2 flush; median of "
+                    f"{reps} replays / launches", "rows": rows}
+
+
+def quant_sweep(torch, bl, inputs, dev, stream, reps=7):
+    """bitlinear_quant_act on its own at the decode sizes (20 distinct inputs per graph)."""
+    T = torch
+    rows = []
+    for M in M_LIST:
+        for K in (2560, 6912):
+            xs = [inputs.activations_bf16(M, K, seed=950 + M + i, device=dev) for i in range(20)]
+            qo = T.empty(M, K, dtype=T.int8, device=dev)
+            so = T.empty(M, dtype=T.float32, device=dev)
+
+            def runq():
+                for x in xs:
+                    bl.bitlinear_quant_act(x, None, M, K, 1e-5, qo, so, stream)
+
+            g = capture(T, runq, stream)
+            ms = time_graphs(T, [g], reps, 2, stream) / reps / len(xs)
+            rows.append({"M": M, "K": K, "us": round(ms * 1e3, 3),
+                         "GB/s": round(algo_bytes_quant(M, K) / (ms * 1e-3) / 1e9, 2)})
+            del g
+    return rows
+
+
+def midm_sweep(torch, bl, inputs, st, stream, reps=5, m_values=(32, 64, 65, 96, 128, 176, 256)):
+    """Mid-size batches through bitlinear_forward (int8 activations: the
+    decode GEMV in 16-token chunks up to 64, the tcgen05 GEMM above) and
+    through bitlinear_forward_f16 (always the GEMM), per (M, shape) on the
+    2B stack's matrices (20 copies per shape, 33-88 MB), after an L2 flush."""
+    T = torch
+    flush = T.empty(256 << 20, dtype=T.uint8, device=st.dev)
+    kinds = [("q,k,v,o", [0, 1, 2, 3]), ("gate,up", [4, 5]), ("down", [6])]
+    e0, e1 = T.cuda.Event(enable_timing=True), T.cuda.Event(enable_timing=True)
+    rows = []
+    for M in m_values:
+        for name, idxs in kinds:
+            _, N, K = st.shapes[idxs[0]]
+            x = inputs.activations_bf16(M, K, seed=700 + M, device=st.dev)
+            q, sc = bl.quant_act(x)
+            q16, sc16 = bl.quant_act_f16(x)
+            out = T.empty(M, N, dtype=T.bfloat16, device=st.dev)
+            mats = [st.w[7 * l + j] for l in range(st.layers) for j in idxs]
+            row = {"M": M, "proj": name, "N": N, "K": K}
+            for tag in ("forward", "forward_f16"):
+                def run():
+                    for packed, gamma, n, k in mats:
+                        if tag == "forward":
+                            bl.bitlinear_forward(q, sc, packed, gamma, M, n, k, out, None, stream)
+                        else:
+                            bl.bitlinear_forward_f16(q16, sc16, packed, gamma, M, n, k, out, None, stream)
+
+                g = capture(T, run, stream)
+                ts = []
+                with T.cuda.stream(stream):
+                    for _ in range(reps):
+                        flush.zero_()
+                        e0.record(stream)
+                        g.replay()
+                        e1.record(stream)
+                        e1.synchronize()
+                        ts.append(e0.elapsed_time(e1))
+                ms = statistics.median(ts) / len(mats)
+                row[tag + "_us"] = round(ms * 1e3, 3)
+                row[tag + "_TFLOP/s"] = round(2 * M * N * K / (ms * 1e-3) / 1e12, 1)
+                row[tag + "_weight_GB/s"] = round(packed_bytes(N, K) / (ms * 1e-3) / 1e9, 1)
+                del g
+            rows.append(row)
+    del flush
+    return {"mode": "per (M, shape): a graph of launches over the 2B stack's copies of that projection after a "
+                    f"256 MB L2 flush; median of {reps} replays / launches", "rows": rows}
+
+
+def prefill_bench(torch, bl, inputs, dev, stream, bf16_peak, steps=5, warmup=3, m_list=(512, 2048, 4096)):
+    """The 2B prefill workload: the seven projections chained through the
+    quantiser at M tokens.  Per M: the chain through the f16-activation path
+    (bitlinear_quant_act_f16 + bitlinear_forward_f16) and through the int8
+    entry points (bitlinear_quant_act + bitlinear_forward); TOPS of the
+    tensor-core GEMMs alone (2*M*N*K per projection) and of the whole chain,
+    and each distinct shape's f16 GEMM on its own."""
     wl = inputs.WORKLOADS["prefill_2b"]
     shapes = wl["shapes"]
     plan, dims = chain_plan(shapes)
@@ -400,57 +544,128 @@ def prefill_bench(torch, bl, inputs, dev, stream, steps=5, warmup=3, M=4096):
         W = inputs.weights_fp32(N, K, seed=wl["seed"] * 100 + i, device=dev)
         w[name] = bl.pack_weights(W, wl["eps_w"])
         del W
-    b = {"x": inputs.activations_bf16(M, hidden, seed=wl["seed"] * 1000 + M, outlier_frac=0.01,
-                                      outlier_scale=20.0, device=dev)}
-    for name, N, K in shapes:
-        b[name] = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
-    for h, src in (("h0", "x"), ("h1", "v"), ("h2", "o"), ("h3", "up")):
-        K = b[src].shape[1]
-        b[h] = (torch.empty(M, K, dtype=torch.float16, device=dev), torch.empty(M, dtype=torch.float32, device=dev))
-    ops = sum(2 * M * dims[o][0] * dims[o][1] for k, _, o in plan if k == "fwd")
+    res = []
+    for M in m_list:
+        b = {"x": inputs.activations_bf16(M, hidden, seed=wl["seed"] * 1000 + M, outlier_frac=0.01,
+                                          outlier_scale=20.0, device=dev)}
+        for name, N, K in shapes:
+            b[name] = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        for h, src in (("h0", "x"), ("h1", "v"), ("h2", "o"), ("h3", "up")):
+            K = b[src].shape[1]
+            b[h] = (torch.empty(M, K, dtype=torch.float16, device=dev), torch.empty(M, dtype=torch.float32, device=dev))
+            b[h + "i8"] = (torch.empty(M, K, dtype=torch.int8, device=dev),
+                           torch.empty(M, dtype=torch.float32, device=dev))
+        ops = sum(2 * M * dims[o][0] * dims[o][1] for k, _, o in plan if k == "fwd")
 
-    def step(kinds=("quant", "fwd")):
-        for kind, a, o in plan:
-            if kind == "quant" and "quant" in kinds:
-                q, s = b[o]
-                bl.bitlinear_quant_act_f16(b[a], None, M, b[a].shape[1], wl["eps_a"], q, s)
-            elif kind == "fwd" and "fwd" in kinds:
-                q, s = b[a]
-                N, K = dims[o]
-                bl.bitlinear_forward_f16(q, s, w[o][0], w[o][1], M, N, K, b[o])
+        def step(kinds=("quant", "fwd"), int8=False, only=None):
+            for kind, a, o in plan:
+                if kind == "quant" and "quant" in kinds:
+                    q, s = b[o + ("i8" if int8 else "")]
+                    if int8:
+                        bl.bitlinear_quant_act(b[a], None, M, b[a].shape[1], wl["eps_a"], q, s, stream)
+                    else:
+                        bl.bitlinear_quant_act_f16(b[a], None, M, b[a].shape[1], wl["eps_a"], q, s, stream)
+                elif kind == "fwd" and "fwd" in kinds and (only is None or o in only):
+                    q, s = b[a + ("i8" if int8 else "")]
+                    N, K = dims[o]
+                    if int8:
+                        bl.bitlinear_forward(q, s, w[o][0], w[o][1], M, N, K, b[o], None, stream)
+                    else:
+                        bl.bitlinear_forward_f16(q, s, w[o][0], w[o][1], M, N, K, b[o], None, stream)
 
-    with torch.cuda.stream(stream):  # eager warm-up outside capture
-        step()
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        step()
-    ms = time_graphs(torch, [g], steps, warmup, stream)
-    chain_tops = ops * steps / (ms * 1e-3) / 1e12
-    # GEMMs alone (quantised activations already in place)
-    g2 = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g2, stream=stream):
-        step(kinds=("fwd",))
-    ms2 = time_graphs(torch, [g2], steps, warmup, stream)
-    gemm_tops = ops * steps / (ms2 * 1e-3) / 1e12
-    del w, b, g, g2
-    return {"workload": f"prefill_2b M={M}", "path": "quant_act_f16 + forward_f16 (tensor-map activations)",
-            "chain_tops": round(chain_tops, 1), "gemm_tops": round(gemm_tops, 1),
-            "gemm_ms_per_chain": round(ms2 / steps, 4), "gemm_launches_per_chain": 7,
-            "gemm_us_per_launch": round(1000 * ms2 / steps / 7, 2),
-            "tokens_per_s": round(M * steps / (ms * 1e-3), 1)}
+        row = {"M": M}
+        for path, int8 in (("f16", False), ("int8", True)):
+            g = capture(torch, lambda: step(int8=int8), stream)
+            ms = time_graphs(torch, [g], steps, warmup, stream) / steps
+            g2 = capture(torch, lambda: step(kinds=("fwd",), int8=int8), stream)
+            ms2 = time_graphs(torch, [g2], steps, warmup, stream) / steps
+            row[path] = {"chain_ms": round(ms, 4), "chain_tops": round(ops / (ms * 1e-3) / 1e12, 1),
+                         "gemm_ms": round(ms2, 4), "gemm_tops": round(ops / (ms2 * 1e-3) / 1e12, 1),
+                         "gemm_frac": round(ops / (ms2 * 1e-3) / 1e12 / bf16_peak, 4),
+                         "tokens_per_s": round(M / (ms * 1e-3), 1)}
+            del g, g2
+        per_shape = []
+        for o in ("q", "gate", "down"):
+            N, K = dims[o]
+            g = capture(torch, lambda: step(kinds=("fwd",), only=(o,)), stream)
+            ms = time_graphs(torch, [g], steps * 4, warmup, stream) / (steps * 4)
+            t = 2 * M * N * K / (ms * 1e-3) / 1e12
+            per_shape.append({"proj": o, "N": N, "K": K, "us": round(ms * 1e3, 2), "TFLOP/s": round(t, 1),
+                              "frac": round(t / bf16_peak, 4)})
+            del g
+        row["f16_per_shape"] = per_shape
+        res.append(row)
+        del b
+    del w
+    torch.cuda.empty_cache()
+    return {"shapes": "q,k,v,o 2560x2560; gate,up 2560->6912; down 6912->2560",
+            "peak_note": "TOPS against the measured cuBLAS bf16 burst peak: the GEMM runs exact f16 tcgen05 "
+                         "MMAs (sm_103a has no int8 tcgen05 MMA)", "rows": res}
+
+
+def small_layer_row(torch, bl, inputs, dev, stream, hbm_peak, reps=200):
+    """The small single-layer workload (M = 1, K = 256, N = 512): quantise +
+    forward, back to back in a graph of 50 layers' worth of calls."""
+    wl = inputs.WORKLOADS["layer_small"]
+    _, N, K = wl["shapes"][0]
+    W = inputs.weights_fp32(N, K, seed=wl["seed"], device=dev)
+    packed, gamma = bl.pack_weights(W, wl["eps_w"])
+    x = inputs.activations_bf16(1, K, seed=1, device=dev)
+    q = torch.empty(1, K, dtype=torch.int8, device=dev)
+    s = torch.empty(1, dtype=torch.float32, device=dev)
+    out = torch.empty(1, N, dtype=torch.bfloat16, device=dev)
+
+    def run():
+        for _ in range(50):
+            bl.bitlinear_quant_act(x, None, 1, K, wl["eps_a"], q, s, stream)
+            bl.bitlinear_forward(q, s, packed, gamma, 1, N, K, out, None, stream)
+
+    g = capture(torch, run, stream)
+    ms = time_graphs(torch, [g], reps, 5, stream) / reps / 50
+    b = algo_bytes_quant(1, K) + algo_bytes_forward(1, N, K)
+    return {"M": 1, "K": K, "N": N, "us_per_layer": round(ms * 1e3, 3),
+            "GB/s": round(b / (ms * 1e-3) / 1e9, 2), "frac": round(b / (ms * 1e-3) / 1e9 / hbm_peak, 5),
+            "tokens_per_s": round(1 / (ms * 1e-3), 1),
+            "note": "32 KB of packed weights: two dependent launches' latency, not bandwidth"}
+
+
+def concurrent_step_ms(torch, bl, inputs, st0, stream_main, steps=300, warmup=5):
+    """The three M of the step as independent decode streams: one CUDA graph
+    with a branch per M, each branch on its own stream and with its OWN copy
+    of the stack's weights (so no branch reads weights another just pulled
+    into L2).  Returns ms per step."""
+    T = torch
+    copies = [st0] + [Stack(T, bl, inputs, st0.dev, WORKLOAD, layers=st0.layers) for _ in range(len(M_LIST) - 1)]
+    runs = [FusedRunner(copies[i], M) for i, M in enumerate(M_LIST)]
+    streams = [T.cuda.Stream() for _ in M_LIST]
+
+    def run():
+        for r, s in zip(runs, streams):
+            s.wait_stream(T.cuda.current_stream())
+            with T.cuda.stream(s):
+                r.run(s)
+        for s in streams:
+            T.cuda.current_stream().wait_stream(s)
+
+    g = capture(T, run, stream_main)
+    ms = time_graphs(T, [g], steps, warmup, stream_main) / steps
+    del g, runs, copies
+    T.cuda.synchronize()
+    return ms
 
 
 # ------------------------------------------------------------ CPU oracle --
 
-def oracle_step_sample(budget_s=20.0):
+def oracle_step_sample(budget_s=20.0, threads=0):
     """The oracle on a bounded sample of the decode workload: one layer of
     the 2B-shape stack for each M (quantise, unpack the packed weights,
     matmul, rescale, for the seven chained projections), repeated until
-    `budget_s` is spent (at least once).  Returns GB/s of the same
-    algorithmic bytes as the GPU line, steps, seconds, threads."""
+    `budget_s` is spent (at least once).  threads: 1 = single-threaded, 0 =
+    every host core.  Returns GB/s of the same algorithmic bytes as the GPU
+    line, reps, seconds, threads used."""
     import oracle
     from bitlinear_02_b300 import inputs
+    oracle.set_threads(threads)
     wl = inputs.WORKLOADS[WORKLOAD]
     shapes = wl["shapes"]
     plan, dims = chain_plan(shapes)
@@ -483,7 +698,9 @@ def oracle_step_sample(budget_s=20.0):
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    return nbytes / dt / 1e9, reps, dt, oracle.threads()
+    used = oracle.threads()
+    oracle.set_threads(0)
+    return nbytes / dt / 1e9, reps, dt, used
 
 
 # ------------------------------------------------------------ main --------
@@ -541,254 +758,94 @@ def profile_gemm(spec):
     return 0
 
 
+def profile_gemv(spec):
+    """--profile-gemv N,K,M[,copies]: the decode GEMV (bitlinear_forward) on
+    `copies` distinct copies of one ternary matrix, 2 warm-up passes + 3
+    timed passes (the driver for ncu captures of the decode kernel)."""
+    import torch
+    import bitlinear_02_b300 as bl
+    from bitlinear_02_b300 import inputs
+    parts = [int(v) for v in spec.split(",")]
+    N, K, M = parts[:3]
+    copies = parts[3] if len(parts) > 3 else 4
+    dev = torch.device("cuda:0")
+    wq = inputs.ternary_hash(N, K, inputs.stack_word(9, 0, 0), device=dev)
+    mats = [bl.pack_ternary(wq) for _ in range(copies)]
+    del wq
+    gam = torch.tensor([0.02], dtype=torch.float32, device=dev)
+    x = inputs.activations_bf16(M, K, seed=3, device=dev)
+    q, s = bl.quant_act(x)
+    out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+
+    def rnd():
+        for p in mats:
+            bl.bitlinear_forward(q, s, p, gam, M, N, K, out)
+
+    for _ in range(2):
+        rnd()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(3):
+        rnd()
+    e1.record()
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / (3 * copies)
+    assert bl.bitlinear_check_status() == bl.OK
+    print(json.dumps({"profile": "gemv", "N": N, "K": K, "M": M, "us": round(ms * 1000, 2),
+                      "weight_GB/s": round(packed_bytes(N, K) / (ms * 1e-3) / 1e9, 1)}))
+    return 0
+
+
 def profile_fused(spec):
-    """--profile-fused L,M: the fused decode path (act_stats + 4 fused GEMV
-    launches per layer) on an L-layer 2B-shape stack at M tokens, eagerly
-    launched: 3 warm-up + 5 timed passes (driver for ncu captures)."""
+    """--profile-fused L,M: the fused decode path on an L-layer 2B-shape
+    stack at M tokens, eagerly launched: 3 warm-up + 5 timed passes (driver
+    for ncu captures)."""
     import torch
     import bitlinear_02_b300 as bl
     from bitlinear_02_b300 import inputs
     L, M = (int(v) for v in spec.split(","))
     dev = torch.device("cuda:0")
     bl.load_library()
-    db = DecodeBench(torch, bl, inputs, dev, layers=L)
-    fd = FusedDecode(torch, bl, db, m_list=(M,))
+    st = Stack(torch, bl, inputs, dev, WORKLOAD, layers=L)
+    fr = FusedRunner(st, M)
     stream = torch.cuda.current_stream()
     for _ in range(3):
-        fd.run_step(stream)
+        fr.run(stream)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(5):
-        fd.run_step(stream)
+        fr.run(stream)
     e1.record()
     e1.synchronize()
     ms = e0.elapsed_time(e1) / 5
     assert bl.bitlinear_check_status() == bl.OK
     print(json.dumps({"profile": "fused", "layers": L, "M": M, "ms_per_pass": round(ms, 4),
-                      "launches_per_pass": 1 + 4 * L}))
+                      "launches_per_pass": fr.launches}))
     return 0
-
-
-def profile_chain(spec):
-    """--profile-chain L,M: the decode chain on an L-layer 2B-shape stack at
-    M tokens, 3 warm-up + 10 timed runs (driver for ncu captures)."""
-    import torch
-    import bitlinear_02_b300 as bl
-    from bitlinear_02_b300 import inputs
-    L, M = (int(v) for v in spec.split(","))
-    dev = torch.device("cuda:0")
-    shapes = inputs.WORKLOADS[WORKLOAD]["shapes"]
-    hidden = shapes[0][2]
-    projs = []
-    for l in range(L):
-        for i, rel in enumerate(LAYER_INPUTS):
-            _, N, K = shapes[i]
-            wq = inputs.ternary(N, K, seed=l * 10 + i, device=dev)
-            packed = bl.pack_ternary(wq)
-            slot = (7 * l if l > 0 else 0) if rel == 0 else 7 * l + rel
-            projs.append(dict(packed=packed, gamma=torch.tensor([0.02], device=dev), N=N, input=slot))
-    dc = bl.DecodeChain(M, hidden, projs)
-    x = inputs.activations_bf16(M, hidden, seed=M, device=dev)
-    for _ in range(3):
-        dc.run(x)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(10):
-        dc.run(x)
-    e1.record()
-    e1.synchronize()
-    ms = e0.elapsed_time(e1) / 10
-    assert bl.bitlinear_check_status() == bl.OK
-    wb = sum(p["packed"].numel() for p in projs)
-    print(json.dumps({"profile": "chain", "layers": L, "M": M, "us": round(ms * 1000, 2),
-                      "weight_gbs": round(wb / (ms * 1e-3) / 1e9, 1)}))
-    return 0
-
-
-def concurrent_step_ms(torch, bl, inputs, db, steps=300, warmup=5):
-    """The three M of the step as independent decode streams: one CUDA graph
-    with a branch per M, each branch on its own stream and with its OWN copy
-    of the stack's weights (so no branch reads weights another just pulled
-    into L2).  The branches' dependent launches overlap on the GPU; the
-    algorithmic bytes are those of the sequential step.  Returns ms per step."""
-    T = torch
-    copies = [db] + [DecodeBench(T, bl, inputs, db.dev) for _ in range(len(M_LIST) - 1)]
-    fds = [FusedDecode(T, bl, copies[i], m_list=(M,)) for i, M in enumerate(M_LIST)]
-    streams = [T.cuda.Stream() for _ in M_LIST]
-    main = T.cuda.Stream()
-
-    def run():
-        for f, s in zip(fds, streams):
-            s.wait_stream(T.cuda.current_stream())
-            with T.cuda.stream(s):
-                f.run_step(s)
-        for s in streams:
-            T.cuda.current_stream().wait_stream(s)
-
-    with T.cuda.stream(main):
-        run()
-    T.cuda.synchronize()
-    g = T.cuda.CUDAGraph()
-    with T.cuda.graph(g, stream=main):
-        run()
-    ms = time_graphs(T, [g], steps, warmup, main) / steps
-    del g, fds, copies
-    T.cuda.synchronize()
-    return ms
-
-
-def gemv_sweep(torch, bl, db, stream, reps=9):
-    """The 2B decode GEMV sweep, shape by shape: bitlinear_forward on a
-    pre-quantised input (the GEMV with its rescale epilogue), and
-    bitlinear_quant_act reported on its own.  Per (M, shape) one CUDA graph
-    of back-to-back launches over the stack's copies of that projection (20
-    layers x the projections of that shape), replayed right after an L2
-    flush (a 256 MB write, outside the timed events), so every launch reads
-    its weights from HBM.  Per-launch time = median replay time / launches;
-    GB/s = algorithmic bytes per launch / that time."""
-    T = torch
-    flush = T.empty(256 << 20, dtype=T.uint8, device=db.dev)
-    kinds = [("q,k,v,o", [0, 1, 2, 3]), ("gate,up", [4, 5]), ("down", [6])]
-    e0, e1 = T.cuda.Event(enable_timing=True), T.cuda.Event(enable_timing=True)
-
-    def timed(graph, n):
-        ts = []
-        with T.cuda.stream(stream):
-            for _ in range(reps):
-                flush.zero_()
-                e0.record(stream)
-                graph.replay()
-                e1.record(stream)
-                e1.synchronize()
-                ts.append(e0.elapsed_time(e1))
-        return statistics.median(ts) / n  # ms per launch
-
-    gemv, quant = [], []
-    tot_b, tot_ms = 0, 0.0
-    for M in M_LIST:
-        for name, idxs in kinds:
-            _, N, K = db.shapes[idxs[0]]
-            x = db.inputs.activations_bf16(M, K, seed=900 + M, device=db.dev)
-            q, sc = bl.quant_act(x, None, db.eps_a)
-            out = T.empty(M, N, dtype=T.bfloat16, device=db.dev)
-            mats = [db.w[7 * l + j] for l in range(db.layers) for j in idxs]
-
-            def run():
-                for packed, gamma, n in mats:
-                    bl.bitlinear_forward(q, sc, packed, gamma, M, n, K, out)
-
-            with T.cuda.stream(stream):
-                run()
-            T.cuda.synchronize()
-            g = T.cuda.CUDAGraph()
-            with T.cuda.graph(g, stream=stream):
-                run()
-            ms = timed(g, len(mats))
-            b = algo_bytes_forward(M, N, K)
-            gemv.append({"M": M, "proj": name, "N": N, "K": K, "us": round(ms * 1e3, 3),
-                         "GB/s": round(b / (ms * 1e-3) / 1e9, 1), "launches": len(mats)})
-            tot_b += b * len(mats)
-            tot_ms += ms * len(mats)
-            del g
-        for K in sorted({k for _, _, k in db.shapes}):
-            xs = [db.inputs.activations_bf16(M, K, seed=950 + M + i, device=db.dev) for i in range(20)]
-            qo = T.empty(M, K, dtype=T.int8, device=db.dev)
-            so = T.empty(M, dtype=T.float32, device=db.dev)
-
-            def runq():
-                for x in xs:
-                    bl.bitlinear_quant_act(x, None, M, K, db.eps_a, qo, so)
-
-            with T.cuda.stream(stream):
-                runq()
-            T.cuda.synchronize()
-            g = T.cuda.CUDAGraph()
-            with T.cuda.graph(g, stream=stream):
-                runq()
-            ms = timed(g, len(xs))
-            quant.append({"M": M, "K": K, "us": round(ms * 1e3, 3),
-                          "GB/s": round(algo_bytes_quant(M, K) / (ms * 1e-3) / 1e9, 2)})
-            del g
-    del flush
-    return {"mode": "per (M, shape): a graph of bitlinear_forward launches over the stack's copies of that "
-                    "projection on a pre-quantised input, replayed after a 256 MB L2 flush; median of "
-                    f"{reps} replays / launches",
-            "gemv": gemv, "quant_act": quant,
-            "gemv_all": {"GB/s": round(tot_b / (tot_ms * 1e-3) / 1e9, 1),
-                         "note": "all shapes and M: algorithmic bytes / summed launch times"}}
-
-
-def midm_sweep(torch, bl, db, stream, reps=7, m_values=(32, 64, 128, 256)):
-    """Mid-size batches (16 < M < 512) through the tensor-core GEMM
-    (bitlinear_quant_act_f16 + bitlinear_forward_f16), measured like the
-    GEMV sweep: per (M, shape) a graph of back-to-back launches over the
-    stack's copies of that projection, replayed after an L2 flush.  Reports
-    per launch us, TFLOP/s and packed-weight GB/s, to place the crossover
-    with the decode GEMV (M <= 16)."""
-    T = torch
-    flush = T.empty(256 << 20, dtype=T.uint8, device=db.dev)
-    kinds = [("q,k,v,o", [0, 1, 2, 3]), ("gate,up", [4, 5]), ("down", [6])]
-    e0, e1 = T.cuda.Event(enable_timing=True), T.cuda.Event(enable_timing=True)
-    rows = []
-    for M in m_values:
-        for name, idxs in kinds:
-            _, N, K = db.shapes[idxs[0]]
-            x = db.inputs.activations_bf16(M, K, seed=700 + M, device=db.dev)
-            q, sc = bl.quant_act_f16(x, None, db.eps_a)
-            out = T.empty(M, N, dtype=T.bfloat16, device=db.dev)
-            mats = [db.w[7 * l + j] for l in range(db.layers) for j in idxs]
-
-            def run():
-                for packed, gamma, n in mats:
-                    bl.forward_f16(q, sc, packed, gamma, n, out=out)
-
-            with T.cuda.stream(stream):
-                run()
-            T.cuda.synchronize()
-            g = T.cuda.CUDAGraph()
-            with T.cuda.graph(g, stream=stream):
-                run()
-            ts = []
-            with T.cuda.stream(stream):
-                for _ in range(reps):
-                    flush.zero_()
-                    e0.record(stream)
-                    g.replay()
-                    e1.record(stream)
-                    e1.synchronize()
-                    ts.append(e0.elapsed_time(e1))
-            ms = statistics.median(ts) / len(mats)
-            wbytes = (-(-N // 16) * 16) * (-(-K // 128) * 128) // 4
-            rows.append({"M": M, "proj": name, "N": N, "K": K, "us": round(ms * 1e3, 3),
-                         "TFLOP/s": round(2 * M * N * K / (ms * 1e-3) / 1e12, 1),
-                         "weight_GB/s": round(wbytes / (ms * 1e-3) / 1e9, 1)})
-            del g
-    del flush
-    return {"mode": "bitlinear_quant_act_f16 + bitlinear_forward_f16 (tcgen05 GEMM), per (M, shape) a graph of "
-                    "launches over the stack's copies after a 256 MB L2 flush; median of "
-                    f"{reps} replays / launches", "rows": rows}
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-stacks", action="store_true", help="skip the 3B and 70B stacks")
+    ap.add_argument("--no-sweeps", action="store_true", help="skip the per-shape and mid-M sweeps")
     ap.add_argument("--profile-gemm", default=None, help="N,K,M[,int8]: time one GEMM shape (ncu driver)")
-    ap.add_argument("--profile-chain", default=None, help="L,M: time the decode chain (ncu driver)")
+    ap.add_argument("--profile-gemv", default=None, help="N,K,M[,copies]: time the decode GEMV (ncu driver)")
     ap.add_argument("--profile-fused", default=None, help="L,M: time the fused decode path (ncu driver)")
     args = ap.parse_args()
     if args.profile_gemm:
         return profile_gemm(args.profile_gemm)
+    if args.profile_gemv:
+        return profile_gemv(args.profile_gemv)
     if args.profile_fused:
         return profile_fused(args.profile_fused)
-    if args.profile_chain:
-        return profile_chain(args.profile_chain)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
@@ -807,66 +864,123 @@ def main():
     hbm_peak, bf16_peak, bf16_sust, peak_kind = peaks()
     stream = torch.cuda.Stream()
 
-    db = DecodeBench(torch, bl, inputs, dev)
-    fd = FusedDecode(torch, bl, db)
-    graph = fd.capture(stream)
+    st = Stack(torch, bl, inputs, dev, WORKLOAD, layers=LAYERS)
+    runs = {M: FusedRunner(st, M) for M in M_LIST}
+    bytes_step = sum(st.bytes(M) for M in M_LIST)
+    n_launch = sum(r.launches for r in runs.values())
+
+    def step():
+        for M in M_LIST:
+            runs[M].run(stream)
+
+    graph = capture(torch, step, stream)
     sampler = ClockSampler(local)
     with sampler:
-        ms = time_graphs(torch, [graph], args.steps, args.warmup, stream, barrier)
-    clocks = sampler.summary()
-    ms = max_over_ranks(torch, ms, dev, dist)
-    assert bl.bitlinear_check_status() == bl.OK, "a bounded wait expired during the timed steps"
-    value = job_value(db.bytes_step, args.steps, ws, ms)
-    ms_step = ms / args.steps
-    del graph
+        ms = time_graphs(torch, [graph], args.steps, args.warmup, stream, barrier, clock=sampler)
+        clocks = ClockSampler.summary(sampler.take())
+        ms = max_over_ranks(torch, ms, dev, dist)
+        assert bl.bitlinear_check_status() == bl.OK, "a bounded wait expired during the timed steps"
+        value = job_value(bytes_step, args.steps, ws, ms)
+        ms_step = ms / args.steps
+        del graph
 
-    # e2e: each M's input copied from pinned host memory, the last output read back, every step
-    h2d = {M: db.x[M].cpu().pin_memory() for M in M_LIST}
-    d2h = {M: torch.empty_like(db.chains[M].out[-1], device="cpu").pin_memory() for M in M_LIST}
-    g_e2e = fd.capture(stream, h2d=h2d, d2h=d2h)
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            g_e2e.replay()
-        stream.synchronize()
+        # The fused decode kernel alone: the step less its three act_stats
+        # launches (timed on their own) is 4 * LAYERS fused launches per M.
+        stats_ms = 0.0
+        for M in M_LIST:
+            r = runs[M]
+            g1 = capture(torch, lambda: bl.bitlinear_act_stats(st.input(M), M, st.hidden, st.eps_a, r.x_stats,
+                                                               stream), stream)
+            stats_ms += time_graphs(torch, [g1], 200, 5, stream) / 200
+            del g1
+        n_fused = n_launch - len(M_LIST)
+        launch_us = 1000.0 * max(1e-9, ms_step - stats_ms) / n_fused
+        fused_bytes = bytes_step - sum(algo_bytes_quant(M, st.hidden) for M in M_LIST)
+        bytes_launch = fused_bytes / n_fused
+        fused_gbs = bytes_launch / (launch_us * 1e-6) / 1e9
+
+        # e2e: each M's input from pinned host memory, the public entry points
+        # called one by one from the host, the last output read back, every step
+        h2d = {M: st.input(M).cpu().pin_memory() for M in M_LIST}
+        d2h = {M: torch.empty_like(runs[M].last_output(), device="cpu").pin_memory() for M in M_LIST}
+
+        def e2e_step():
+            for M in M_LIST:
+                st.x[M].copy_(h2d[M], non_blocking=True)
+                runs[M].run(stream)
+                d2h[M].copy_(runs[M].last_output(), non_blocking=True)
+
         n_e2e = max(10, args.steps // 4)
-        t0 = time.perf_counter()
-        for i in range(n_e2e):
-            g_e2e.replay()            # replays on `stream`, the current stream here
-            stream.synchronize()      # the step, copies included, has finished
-            _ = float(d2h[16][0, 0])  # read the result on the host
-        e2e_s = time.perf_counter() - t0
-    e2e_val = db.bytes_step * n_e2e * ws / e2e_s / 1e9
-    h2d_bytes = sum(t.numel() * t.element_size() for t in h2d.values())
-    d2h_bytes = sum(t.numel() * t.element_size() for t in d2h.values())
-    del g_e2e
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                e2e_step()
+            stream.synchronize()
+            sampler.mark(True)
+            t0 = time.perf_counter()
+            for _ in range(n_e2e):
+                e2e_step()
+                stream.synchronize()
+                _ = float(d2h[16][0, 0])  # read the result on the host
+            e2e_s = time.perf_counter() - t0
+            sampler.mark(False)
+        e2e_val = bytes_step * n_e2e * ws / e2e_s / 1e9
+        h2d_bytes = sum(t.numel() * t.element_size() for t in h2d.values())
+        d2h_bytes = sum(t.numel() * t.element_size() for t in d2h.values())
+        g_e2e = capture(torch, e2e_step, stream)
+        with torch.cuda.stream(stream):
+            t0 = time.perf_counter()
+            for _ in range(n_e2e):
+                g_e2e.replay()
+                stream.synchronize()
+                _ = float(d2h[16][0, 0])
+            e2e_graph_s = time.perf_counter() - t0
+        del g_e2e
+        e2e_graph = bytes_step * n_e2e * ws / e2e_graph_s / 1e9
 
-    g_chain = db.capture(stream)
-    chain_ms = time_graphs(torch, [g_chain], max(20, args.steps // 10), 3, stream) / max(20, args.steps // 10)
-    del g_chain
-    unf_ms = unfused_step_ms(torch, bl, db, stream)
-    conc_ms = concurrent_step_ms(torch, bl, inputs, db)
-    sweep = gemv_sweep(torch, bl, db, stream)
-    midm = midm_sweep(torch, bl, db, stream)
-    for r in sweep["gemv"]:
-        r["frac"] = round(r["GB/s"] / hbm_peak, 4)
-    n_fused = FusedDecode.launches  # act_stats + 4 fused GEMVs per layer, per M
-    launch_us = 1000.0 * ms_step / n_fused
-    bytes_launch = db.bytes_step / n_fused
-    fused_gbs = bytes_launch / (launch_us * 1e-6) / 1e9
-    prefill = None
-    if not args.no_prefill:
-        prefill = prefill_bench(torch, bl, inputs, dev, stream)
-        prefill["roofline"] = {"bound": "tensor", "achieved": prefill["gemm_tops"],
-                               "peak": round(bf16_peak, 1), "unit": "TFLOP/s",
-                               "frac": round(prefill["gemm_tops"] / bf16_peak, 4),
-                               "peak_note": f"{peak_kind} cuBLAS bf16 burst; the GEMM runs f16 MMA (same rate); "
-                                            "sm_103a has no int8 tcgen05 MMA"}
+        unf = {M: UnfusedRunner(st, M) for M in M_LIST}
+        g_unf = capture(torch, lambda: [unf[M].run(stream) for M in M_LIST], stream)
+        unf_ms = time_graphs(torch, [g_unf], 20, 3, stream, clock=sampler) / 20
+        del g_unf, unf
+        conc_ms = concurrent_step_ms(torch, bl, inputs, st, stream)
+
+        configs = {"layer_small": small_layer_row(torch, bl, inputs, dev, stream, hbm_peak)}
+        rows2b = stack_rows(torch, st, M_LIST, stream, hbm_peak, reps=50, clock=sampler)
+        configs["decode_2b"] = {"layers": st.layers, "packed_mb": round(st.packed_bytes / 1e6, 1), "rows": rows2b}
+        sweep = midm = None
+        if not args.no_sweeps:
+            sweep = gemv_sweep(torch, bl, inputs, dev, stream, hbm_peak)
+            sweep["quant_act"] = quant_sweep(torch, bl, inputs, dev, stream)
+            midm = midm_sweep(torch, bl, inputs, st, stream)
+        del runs
+        if not args.no_prefill:
+            sampler.mark(True)
+            configs["prefill_2b"] = prefill_bench(torch, bl, inputs, dev, stream, bf16_peak)
+            sampler.mark(False)
+        if not args.no_stacks:
+            for wl, m_list in (("stack_3b", (1, 2, 4, 8, 16, 32, 64)),
+                               ("stack_70b", (1, 2, 4, 8, 16, 32, 64, 128, 256))):
+                t0 = time.perf_counter()
+                stk = Stack(torch, bl, inputs, dev, wl)
+                gen_s = time.perf_counter() - t0
+                rows = stack_rows(torch, stk, m_list, stream, hbm_peak, reps=10, clock=sampler)
+                configs[wl] = {"layers": stk.layers, "packed_gb": round(stk.packed_bytes / 1e9, 3),
+                               "weights": "ternary from the on-device counter-based generator, "
+                                          f"generated and packed in {gen_s:.1f} s", "o_from": stk.o_from,
+                               "rows": rows}
+                del stk
+                torch.cuda.empty_cache()
+        assert bl.bitlinear_check_status() == bl.OK, "a bounded wait expired during the measurements"
+        clocks_all = ClockSampler.summary(sampler.all)
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
-        gbs, reps, dt, cores = oracle_step_sample(budget_s=15.0)
+        gbs1, reps1, dt1, c1 = oracle_step_sample(budget_s=8.0, threads=1)
+        gbs, reps, dt, cores = oracle_step_sample(budget_s=12.0, threads=0)
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                "sample": f"{reps} x one 2B-shape layer for each M=1,4,16 (quantise, unpack, matmul, rescale; "
-                         f"7 chained projections) in {dt:.1f} s"}
+                         f"7 chained projections) in {dt:.1f} s",
+               "single_thread": {"value": round(gbs1, 4), "unit": "GB/s", "cores": c1,
+                                 "sample": f"{reps1} x the same sample in {dt1:.1f} s"}}
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
@@ -874,44 +988,45 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int8 x ternary -> int32 (f16 tensor-core operands, exact), bf16 out",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "M": list(M_LIST), "layers": db.layers, "hidden": 2560,
+        "config": {"workload": WORKLOAD, "M": list(M_LIST), "layers": st.layers, "hidden": 2560,
                    "ffn": 6912, "projections": "q,k,v,o 2560x2560; gate,up 2560->6912; down 6912->2560",
-                   "packed_mb": round(db.packed_bytes / 1e6, 1),
+                   "packed_mb": round(st.packed_bytes / 1e6, 1),
                    "l2": "inputs larger than L2: the stack's packed weights are 3x the 126 MB L2",
-                   "bytes_per_step": db.bytes_step,
-                   "graph": "one CUDA graph per step: per M one act_stats + 4 fused GEMV launches per layer",
+                   "bytes_per_step": bytes_step,
+                   "graph": "one CUDA graph per step: per M one act_stats + 4 fused decode launches per layer",
                    "parallelism": f"replicas x{ws}"},
         "hbm_frac_of_step": round(value / ws / hbm_peak, 4),
+        "tokens_per_s": {str(r["M"]): r["tokens_per_s"] for r in rows2b},
         "roofline": {"bound": "hbm", "achieved": round(fused_gbs, 1), "peak": round(hbm_peak, 1),
                      "unit": "GB/s", "frac": round(fused_gbs / hbm_peak, 4),
-                     "traffic": round(FUSED_DRAM_PER_PACKED_BYTE * db.packed_bytes * len(M_LIST) / n_fused),
-                     "traffic_note": "bytes per average launch: ncu DRAM bytes per packed-weight byte "
-                                     "(profiles/fused_gemv_decode_2b_M16_full.md) x packed bytes per launch",
-                     "kernel": "fused_gemv_kernel (decode GEMV with the quantiser folded in)",
-                     "launch_avg_us": round(launch_us, 2), "algo_bytes_per_launch": round(bytes_launch),
+                     "traffic": (round(FUSED_DRAM_PER_PACKED_BYTE * st.packed_bytes * len(M_LIST) / n_fused)
+                                 if FUSED_DRAM_PER_PACKED_BYTE else None),
+                     "kernel": "decode_kernel<NT, true> (the fused decode path: quantiser folded into the GEMV)",
+                     "launch_avg_us": round(launch_us, 3), "algo_bytes_per_launch": round(bytes_launch),
                      "peak_note": f"{peak_kind} HBM copy bandwidth",
-                     "method": "CUDA events around the timed graph replays; launch time = step time / "
-                               "launches in the step (3 of the 243 are act_stats)"},
-        "chain": {"ms_per_step": round(chain_ms, 4),
-                  "value": round(db.bytes_step / (chain_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-                  "mode": "persistent fused-chain kernel, one launch per M through the whole stack"},
+                     "method": "CUDA events on the launching stream around the timed graph replays; the three "
+                               "act_stats launches timed on their own and subtracted; average over the step's "
+                               f"{n_fused} fused launches"},
         "concurrent": {"ms_per_step": round(conc_ms, 4),
-                       "value": round(db.bytes_step / (conc_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                       "value": round(bytes_step / (conc_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                        "mode": "the three M as independent decode streams: one graph, a branch per M on its own "
-                               "stream, each branch with its own copy of the weights (3 x 396 MB, no shared L2 "
-                               "reads); same kernels and algorithmic bytes as the step"},
+                               "stream, each branch with its own copy of the weights; same kernels and bytes"},
         "unfused": {"ms_per_step": round(unf_ms, 4),
-                    "value": round(db.bytes_step / (unf_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                    "value": round(bytes_step / (unf_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                     "mode": "bitlinear_quant_act + bitlinear_forward per projection, PDL-chained graph"},
+        "configs": configs,
         "sweep": sweep,
         "mid_m": midm,
-        "prefill": prefill,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d_bytes,
                 "d2h_bytes_per_step": d2h_bytes,
-                "mode": "graph replay of the public API calls incl. pinned H2D/D2H copies, host sync per step"},
-        "gpu_launches": n_fused * args.steps,
+                "mode": "the public entry points called one by one from Python (ctypes) every step, with the "
+                        "pinned H2D input copies and D2H output reads inside, host sync per step",
+                "graph": {"value": round(e2e_graph, 2), "unit": "GB/s",
+                          "mode": "the same step (copies included) replayed as one CUDA graph"}},
+        "gpu_launches": n_launch * args.steps,
         "clocks": clocks,
+        "clocks_all_timed_regions": clocks_all,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

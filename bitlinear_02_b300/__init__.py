@@ -26,8 +26,6 @@ __all__ = [
     "pack_weights", "pack_ternary", "quant_act", "forward", "bitlinear",
     "FusedProj", "bitlinear_fused_stats_bytes", "bitlinear_act_stats", "bitlinear_forward_fused",
     "bitlinear_fused_factors", "fused_factors", "new_stats",
-    "ChainProj", "ChainPlan", "bitlinear_chain_workspace_bytes", "bitlinear_chain_prepare",
-    "bitlinear_chain_run", "bitlinear_chain_set_split", "DecodeChain",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -45,25 +43,6 @@ class FusedProj(ctypes.Structure):
     """bitlinear_fused_proj_t: one projection of a fused decode GEMV launch."""
     _fields_ = [("packed", ctypes.c_void_p), ("gamma", ctypes.c_void_p), ("N", ctypes.c_int64),
                 ("out_bf16", ctypes.c_void_p), ("acc_out", ctypes.c_void_p), ("stats", ctypes.c_void_p)]
-
-
-class ChainProj(ctypes.Structure):
-    """bitlinear_chain_proj_t: one projection of a fused decode chain."""
-    _fields_ = [("packed", ctypes.c_void_p), ("gamma", ctypes.c_void_p), ("N", ctypes.c_int64),
-                ("input", ctypes.c_int32), ("flags", ctypes.c_int32), ("out_bf16", ctypes.c_void_p),
-                ("acc_out", ctypes.c_void_p), ("tok_scale_out", ctypes.c_void_p)]
-
-
-class ChainPlan(ctypes.Structure):
-    """bitlinear_chain_plan_t (opaque): filled by bitlinear_chain_prepare."""
-    _fields_ = [("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_uint64),
-                ("M", ctypes.c_int64), ("K0", ctypes.c_int64), ("nphase", ctypes.c_int32),
-                ("nproj", ctypes.c_int32), ("grid", ctypes.c_int32), ("threads", ctypes.c_int32),
-                ("smem_bytes", ctypes.c_int32), ("mp", ctypes.c_int32), ("q_bytes", ctypes.c_uint32),
-                ("part_bytes", ctypes.c_uint32), ("off_phases", ctypes.c_uint64),
-                ("off_projs", ctypes.c_uint64), ("off_xstats", ctypes.c_uint64),
-                ("off_partials", ctypes.c_uint64), ("eps", ctypes.c_float),
-                ("ring_bytes", ctypes.c_uint32), ("magic", ctypes.c_uint64)]
 
 
 class BitLinearError(RuntimeError):
@@ -111,18 +90,10 @@ def load_library():
     L.bitlinear_forward_fused.argtypes = [P, P, I64, I64, ctypes.c_int32, ctypes.POINTER(FusedProj), F, P]
     L.bitlinear_fused_factors.argtypes = [P, I64, I64, F, ctypes.c_int32, P, P, P]
     L.bitlinear_forward_f16.argtypes = [P, P, P, P, I64, I64, I64, P, P, P]
-    L.bitlinear_chain_workspace_bytes.argtypes = [I64, I64, ctypes.POINTER(ChainProj), ctypes.c_int32]
-    L.bitlinear_chain_workspace_bytes.restype = ctypes.c_size_t
-    L.bitlinear_chain_prepare.argtypes = [I64, I64, ctypes.POINTER(ChainProj), ctypes.c_int32, F, P,
-                                          ctypes.c_size_t, ctypes.POINTER(ChainPlan), P]
-    L.bitlinear_chain_run.argtypes = [ctypes.POINTER(ChainPlan), P, P]
-    L.bitlinear_chain_set_split.argtypes = [ctypes.c_int32]
-    L.bitlinear_chain_set_split.restype = None
     for name in ("bitlinear_pack_weights", "bitlinear_pack_weights_noalloc", "bitlinear_pack_ternary", "bitlinear_quant_act",
-                 "bitlinear_forward", "bitlinear_check_status", "bitlinear_chain_prepare",
+                 "bitlinear_forward", "bitlinear_check_status",
                  "bitlinear_quant_act_f16", "bitlinear_forward_f16", "bitlinear_act_stats",
-                 "bitlinear_forward_fused", "bitlinear_fused_factors",
-                 "bitlinear_chain_run"):
+                 "bitlinear_forward_fused", "bitlinear_fused_factors"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -263,78 +234,7 @@ def bitlinear_set_wait_limit(iterations: int) -> None:
     load_library().bitlinear_set_wait_limit(int(iterations))
 
 
-def _proj_array(projs):
-    arr = (ChainProj * len(projs))()
-    for i, p in enumerate(projs):
-        arr[i] = p
-    return arr
-
-
-def bitlinear_chain_workspace_bytes(M: int, K0: int, projs) -> int:
-    arr = _proj_array(projs)
-    return int(load_library().bitlinear_chain_workspace_bytes(int(M), int(K0), arr, len(projs)))
-
-
-def bitlinear_chain_prepare(M: int, K0: int, projs, eps: float, workspace, workspace_bytes: int,
-                            stream=None) -> ChainPlan:
-    arr = _proj_array(projs)
-    plan = ChainPlan()
-    _check(load_library().bitlinear_chain_prepare(int(M), int(K0), arr, len(projs), float(eps),
-                                                  _ptr(workspace), int(workspace_bytes),
-                                                  ctypes.byref(plan), _stream(stream)),
-           "bitlinear_chain_prepare")
-    return plan
-
-
-def bitlinear_chain_run(plan: ChainPlan, x, stream=None) -> None:
-    _check(load_library().bitlinear_chain_run(ctypes.byref(plan), _ptr(x), _stream(stream)),
-           "bitlinear_chain_run")
-
-
-def bitlinear_chain_set_split(split: int) -> None:
-    load_library().bitlinear_chain_set_split(int(split))
-
-
 # ------------------------------------------------------------ convenience ---
-
-class DecodeChain:
-    """A prepared fused decode chain.
-
-    ``projs`` is a list of dicts with keys ``packed``, ``gamma`` (device
-    tensors), ``N`` and ``input`` (0 = the chain input, i + 1 = output of
-    projection i).  Every projection gets a bf16 output tensor
-    (``self.out[j]``); ``keep_acc`` / ``keep_scales`` also keep the exact
-    int32 accumulators and the token scales of each projection's input.
-    """
-
-    def __init__(self, M: int, K0: int, projs, eps: float = 1e-5, device=None,
-                 keep_acc: bool = False, keep_scales: bool = False, stream=None):
-        device = device or projs[0]["packed"].device
-        self.M, self.K0 = int(M), int(K0)
-        self.out, self.acc, self.tok_scale = [], [], []
-        cp = []
-        for p in projs:
-            N = int(p["N"])
-            o = torch.empty(M, N, dtype=torch.bfloat16, device=device)
-            a = torch.empty(M, N, dtype=torch.int32, device=device) if keep_acc else None
-            t = torch.empty(M, dtype=torch.float32, device=device) if keep_scales else None
-            self.out.append(o)
-            self.acc.append(a)
-            self.tok_scale.append(t)
-            cp.append(ChainProj(p["packed"].data_ptr(), p["gamma"].data_ptr(), N, int(p["input"]), 0,
-                                o.data_ptr(), a.data_ptr() if a is not None else None,
-                                t.data_ptr() if t is not None else None))
-        self._keep = [p["packed"] for p in projs] + [p["gamma"] for p in projs]
-        nbytes = bitlinear_chain_workspace_bytes(M, K0, cp)
-        if nbytes == 0:
-            raise BitLinearError(ERR_INVALID_ARG, "bitlinear_chain_workspace_bytes")
-        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
-        self.plan = bitlinear_chain_prepare(M, K0, cp, eps, self.workspace, nbytes, stream)
-
-    def run(self, x: torch.Tensor, stream=None):
-        bitlinear_chain_run(self.plan, x, stream)
-        return self.out
-
 
 def pack_weights(W: torch.Tensor, eps: float = 1e-5):
     """fp32 [N, K] CUDA tensor -> (packed uint8 tensor, gamma float32 [1] tensor)."""

@@ -1,5 +1,5 @@
 // Register-level arithmetic of the decode engines (M <= 16 tokens), shared by
-// the per-projection GEMV and the fused decode chain.
+// the per-projection GEMV and the fused decode GEMV.
 //
 // The packed 2-bit code c = Wq + 1 of a weight is fed to the legacy
 // tensor-core MMA (m16n8k16, f16 inputs, fp32 accumulate) without being

@@ -1,8 +1,9 @@
-// Prefill engine (M > 16 tokens): a dense contraction on the 5th-generation
-// tensor cores.
+// Prefill engine (bitlinear_forward above 64 tokens, bitlinear_forward_f16 at
+// any M): a dense contraction on the 5th-generation tensor cores.
 //
-// asi.tokyo 2B4T write-up: packed ternary weights are unpacked next to the
-// math units and multiplied with 8-bit activations.  B300 (sm_103a) has no
+// asi.tokyo 2B4T write-up, on its GPU kernel (four weights packed per byte):
+// packed ternary weights are unpacked next to the math units and multiplied
+// with 8-bit activations.  B300 (sm_103a) has no
 // int8 tcgen05 MMA, so both operands are fed as f16: ternary codes become
 // -1/0/+1 and int8 activations their exact f16 values.  Every product is an
 // integer of magnitude <= 128 and every partial sum an integer below 2^24
@@ -11,8 +12,8 @@
 // CTA tile: 128 weight rows (MMA M, TMEM lanes) x BN tokens (MMA N, TMEM
 // columns); k advances 64 per pipeline stage.  Roles:
 //   - loader (warp 9, one thread): per stage, a 2-D tensor-map copy of the
-//     int8 activation tile (BN tokens x 64 k) and bulk copies of the eight
-//     512-byte packed weight tiles, into the stage's raw buffers;
+//     int8 activation tile (BN tokens x 64 k) and one 3-D tensor-map copy of
+//     the eight 512-byte packed weight tiles, into the stage's raw buffers;
 //   - converters (warps 0-7): the weight operand A lives in tensor memory:
 //     warps 0-3 each own 32 rows (their TMEM lane quarter), expand the
 //     row's 2-bit codes to f16 in registers and store them with tcgen05.st;
@@ -269,9 +270,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // layout the MMA reads, so the converter warps only expand the weight codes
 // into tensor memory.  Stage = swizzled f16 tile | packed codes.
 // ---------------------------------------------------------------------------
-// NSTG stages; MINB CTAs per SM (2: each CTA's prologue and epilogue run
-// under the other's main loop, so the tensor pipe keeps working across tile
-// boundaries; that needs the TMEM columns of both to fit in 512).
+// NSTG stages; MINB CTAs per SM (a template parameter: with 2, one CTA's
+// prologue and epilogue could run under the other's main loop, but the
+// TMEM columns of both must then fit in 512; every launch uses MINB = 1).
 template <int BN, int NSTG>
 struct Smem16 {
     static constexpr uint32_t kTileB = BN * 128;

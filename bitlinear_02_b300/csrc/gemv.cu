@@ -1,8 +1,9 @@
-// Decode engine (M <= 16 tokens): HBM-bound stream of packed ternary weights.
+// Decode engine (bitlinear_forward up to 64 tokens: 16-token chunks as
+// blockIdx.z): HBM-bound stream of packed ternary weights.
 //
-// asi.tokyo 2B4T write-up: the weights travel packed four per byte and are
-// unpacked right next to the math units, then multiplied with 8-bit
-// activations.  Here every 16-byte lane chunk of the packed layout is
+// asi.tokyo 2B4T write-up, on its GPU kernel (four weights packed per
+// byte): the weights travel packed four per byte and are unpacked right next
+// to the math units, then multiplied with 8-bit activations.  Here every 16-byte lane chunk of the packed layout is
 // loaded once (128-bit, streaming), unpacked in registers and fed to the
 // legacy tensor-core MMA (m16n8k16, f16 inputs, fp32 accumulate) - on B300
 // its f16 rate is four times its int8 rate and far above dp4a.
@@ -192,7 +193,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
 
 }  // namespace
 
-// Host launcher (called by bitlinear_forward for M <= 16).
+// Host launcher (called by bitlinear_forward for M <= 64, in 16-token chunks).
 cudaError_t launch_gemv(const int8_t *q, const float *tok_scale, const uint8_t *packed,
                         const float *gamma, int M, int N, int K, __nv_bfloat16 *out,
                         int32_t *acc_out, cudaStream_t st, int num_sms) {

@@ -199,6 +199,10 @@ cudaError_t workspace(unsigned long long **out) {
 
 bool shape_ok(int64_t N, int64_t K) { return N >= 1 && K >= 16 && (K % 16) == 0 && N <= (1ll << 31) && K <= (1ll << 31); }
 
+// Each exponent bucket gathers up to N*K mantissas below 2^24; keeping
+// N*K <= 2^40 keeps every 64-bit counter below 2^64.
+constexpr int64_t kMaxSumElems = 1ll << 40;
+
 // The matmul kernels read packed weights before they wait for the kernel
 // that precedes them in the stream (weights are static, so their loads can
 // overlap that kernel).  The packers must therefore hand over weights that
@@ -241,6 +245,7 @@ extern "C" bitlinear_status_t bitlinear_pack_weights(const float *W, int64_t N, 
     using namespace bl;
     if (!W || !packed || !gamma || !shape_ok(N, K)) return BITLINEAR_ERR_INVALID_ARG;
     if (!aligned16(W) || !aligned16(packed) || !aligned4(gamma)) return BITLINEAR_ERR_INVALID_ARG;
+    if (N * K > kMaxSumElems) return BITLINEAR_ERR_UNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     unsigned long long *ws = nullptr;
     if (workspace(&ws) != cudaSuccess) return BITLINEAR_ERR_CUDA;
@@ -288,10 +293,6 @@ namespace {
 // 256 64-bit counters (2 KB): the whole scratch of the absmean sum.
 static __device__ __align__(256) unsigned long long g_noalloc_buckets[kBuckets];
 
-// Each bucket gathers up to N*K mantissas below 2^24; keeping N*K <= 2^40
-// keeps every counter below 2^64.
-constexpr int64_t kNoAllocMaxElems = 1ll << 40;
-
 std::mutex g_noalloc_mutex;
 unsigned long long *g_noalloc_ptr[64] = {nullptr};
 
@@ -323,7 +324,7 @@ extern "C" bitlinear_status_t bitlinear_pack_weights_noalloc(const float *W, int
     using namespace bl;
     if (!W || !packed || !gamma || !shape_ok(N, K)) return BITLINEAR_ERR_INVALID_ARG;
     if (!aligned16(W) || !aligned16(packed) || !aligned4(gamma)) return BITLINEAR_ERR_INVALID_ARG;
-    if (N * K > kNoAllocMaxElems) return BITLINEAR_ERR_UNSUPPORTED;
+    if (N * K > kMaxSumElems) return BITLINEAR_ERR_UNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     unsigned long long *ws = nullptr;
     if (noalloc_scratch(&ws) != cudaSuccess) return BITLINEAR_ERR_CUDA;

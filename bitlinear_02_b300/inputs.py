@@ -18,6 +18,10 @@ cheatsheet.md tables):
                     M in {1, 2, 4, ..., 64}.
 * ``stack_70b``     80 layers, hidden 8192, FFN 28672, K/V 8192->1024;
                     ternary weights as above; M in {1, 2, 4, ..., 256}.
+
+The two stacks' weights (0.8 GB and 17.1 GB packed) are drawn on the device
+by ``ternary_hash``, a counter-based generator (SplitMix64), so that any row
+can be regenerated on the host and no weight crosses the PCIe bus.
 """
 from __future__ import annotations
 
@@ -107,3 +111,66 @@ def gain_bf16(K: int, seed: int, device="cpu") -> torch.Tensor:
 def bf16_bits(x: torch.Tensor):
     """bf16 tensor -> numpy uint16 bit patterns (host)."""
     return x.detach().to("cpu").contiguous().view(torch.int16).numpy().view("uint16")
+
+
+# ---------------------------------------------------------------- SplitMix64 ---
+# Counter-based ternary weights for the stacked workloads.  SplitMix64
+# (Steele, Lea and Flood, OOPSLA 2014): the i-th output (i = 0, 1, ...) of
+# the generator seeded with s is mix(s + (i + 1) * 0x9E3779B97F4A7C15), with
+#   mix(z): z = (z ^ z >> 30) * 0xBF58476D1CE4E5B9;
+#           z = (z ^ z >> 27) * 0x94D049BB133111EB;  z ^ z >> 31
+# (64-bit wrap-around, logical shifts).  A matrix keyed by `word` takes
+# s = the first output of SplitMix64 seeded with `word`; its element (n, k)
+# is output n*K + k of SplitMix64 seeded with s, mapped to {-1, 0, +1} as
+# floor(hi32 * 3 / 2^32) - 1, hi32 being the output's upper 32 bits.
+# Written here with torch int64 tensors (two's-complement wrap-around), so
+# it runs on the GPU; the oracle has its own C version of the definition.
+
+_GOLDEN = 0x9E3779B97F4A7C15
+_MIX1 = 0xBF58476D1CE4E5B9
+_MIX2 = 0x94D049BB133111EB
+
+
+def _i64(u: int) -> int:
+    """A uint64 constant as the int64 with the same bits."""
+    u &= (1 << 64) - 1
+    return u - (1 << 64) if u >= (1 << 63) else u
+
+
+def _srl(x: torch.Tensor, s: int) -> torch.Tensor:
+    """Logical right shift of int64 bit patterns."""
+    return (x >> s) & ((1 << (64 - s)) - 1)
+
+
+def _mix(z: torch.Tensor) -> torch.Tensor:
+    z = (z ^ _srl(z, 30)) * _i64(_MIX1)
+    z = (z ^ _srl(z, 27)) * _i64(_MIX2)
+    return z ^ _srl(z, 31)
+
+
+def _mix_int(z: int) -> int:
+    m = (1 << 64) - 1
+    z &= m
+    z = ((z ^ (z >> 30)) * _MIX1) & m
+    z = ((z ^ (z >> 27)) * _MIX2) & m
+    return z ^ (z >> 31)
+
+
+def stack_word(seed: int, layer: int, proj: int) -> int:
+    """Key of one matrix of a stacked workload (its seed, layer, projection)."""
+    return (int(seed) << 40) | (int(layer) << 8) | int(proj)
+
+
+def ternary_hash(N: int, K: int, word: int, device="cpu", rows_per_chunk: int = 4096) -> torch.Tensor:
+    """The [N, K] ternary matrix keyed by `word`, int8 in {-1, 0, +1}
+    (P = 1/3 each up to 2^-32), computed on `device`."""
+    s = _mix_int(int(word) + _GOLDEN)  # first output of SplitMix64 seeded with word
+    out = torch.empty(N, K, dtype=torch.int8, device=device)
+    col = torch.arange(K, dtype=torch.int64, device=device)
+    for n0 in range(0, N, rows_per_chunk):
+        n1 = min(N, n0 + rows_per_chunk)
+        rows = torch.arange(n0, n1, dtype=torch.int64, device=device)
+        i1 = rows[:, None] * K + col[None, :] + 1          # i + 1
+        v = _mix(i1 * _i64(_GOLDEN) + _i64(s))
+        out[n0:n1] = ((_srl(v, 32) * 3) >> 32).to(torch.int8) - 1
+    return out

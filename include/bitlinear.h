@@ -102,7 +102,8 @@ BITLINEAR_API size_t bitlinear_packed_bytes(int64_t N, int64_t K);
  * that first call is therefore not capturable in a CUDA graph.  Calls on
  * different streams of the same device must not overlap in time.
  * Errors: INVALID_ARG (null/misaligned pointer, N < 1, K < 1, K % 16 != 0),
- * CUDA (workspace allocation or launch failure).
+ * UNSUPPORTED (N*K > 2^40 weights: the exact 64-bit bucket sums could
+ * overflow), CUDA (workspace allocation or launch failure).
  */
 BITLINEAR_API bitlinear_status_t bitlinear_pack_weights(const float *W, int64_t N, int64_t K, float eps,
                                           uint8_t *packed, float *gamma, void *stream);
@@ -293,91 +294,6 @@ BITLINEAR_API bitlinear_status_t bitlinear_forward_fused(const void *x_bf16, voi
 BITLINEAR_API bitlinear_status_t bitlinear_fused_factors(void *stats, int64_t M, int64_t K, float eps,
                                                          int32_t consume, float *c_out, float *ts_out,
                                                          void *stream);
-
-/*
- * Fused decode chain: a sequence of BitLinear projections for M <= 16
- * tokens, each one quantising its input (RMSNorm + per-token absmax int8,
- * as bitlinear_quant_act with no gain) and multiplying it with its ternary
- * weights (as bitlinear_forward), run by one persistent kernel per call.
- *
- * The cheatsheet.md summary ("BitNet b1.58とは？") quantises every
- * BitLinear input per token by its absolute maximum, so each projection
- * depends on the whole output of the one feeding it.  For decode-sized
- * batches those dependencies, not the weight bytes, dominate a chain of
- * separate calls; this engine keeps the weights streaming from HBM while the
- * dependencies resolve.  Results: the exact int32 accumulators equal those
- * of bitlinear_quant_act + bitlinear_forward on the same input; the token
- * scales agree to ~1e-7 relative (a float reduction in another order); the
- * bf16 outputs are the epilogue of those accumulators and scales.
- *
- * Projection j reads activation slot `input`: 0 is the chain input x
- * (bf16 [M, K0]); i + 1 is the output of projection i (i < j).  Consecutive
- * projections with the same input run together (as one phase).  An output
- * that a later projection reads must have N % 16 == 0.
- */
-typedef struct {
-    const uint8_t *packed;  /* device: packed weights of an [N, K] matrix, K = width of its input */
-    const float *gamma;     /* device: the matrix's scale (one float) */
-    int64_t N;              /* output features, 1 <= N <= 2^24 */
-    int32_t input;          /* 0 = chain input x, i + 1 = output of projection i */
-    int32_t flags;          /* must be 0 */
-    void *out_bf16;         /* device bf16 [M, N], 16-byte aligned, or NULL */
-    int32_t *acc_out;       /* device int32 [M, N], 16-byte aligned, or NULL (exact accumulators) */
-    float *tok_scale_out;   /* device fp32 [M], or NULL: the token scales of this projection's input */
-} bitlinear_chain_proj_t;
-
-/* Filled by bitlinear_chain_prepare; treat as opaque and pass to
- * bitlinear_chain_run.  It refers to the workspace given to prepare. */
-typedef struct {
-    void *workspace;
-    uint64_t workspace_bytes;
-    int64_t M, K0;
-    int32_t nphase, nproj, grid, threads, smem_bytes, mp;
-    uint32_t q_bytes, part_bytes;
-    uint64_t off_phases, off_projs, off_xstats, off_partials;
-    float eps;
-    uint32_t ring_bytes;
-    uint64_t magic;
-} bitlinear_chain_plan_t;
-
-/* Workspace bytes for a chain on the current device (0 if the description
- * is invalid).  1 <= M <= 16, K0 % 16 == 0, 16 <= K0 <= 65536. */
-BITLINEAR_API size_t bitlinear_chain_workspace_bytes(int64_t M, int64_t K0,
-                                                     const bitlinear_chain_proj_t *projs,
-                                                     int32_t nproj);
-
-/*
- * Plans the chain into `workspace` (device, 16-byte aligned, at least
- * bitlinear_chain_workspace_bytes, owned by the caller and kept alive and
- * unmodified while the plan is used) and fills `plan`.  The output pointers
- * of `projs` are recorded in the plan.  Enqueues a clear and a copy of the
- * plan tables on `stream` and synchronises it (a set-up call: not
- * capturable).  eps: the RMSNorm epsilon (1e-5 in the workloads).
- * Errors: INVALID_ARG (bad sizes, pointers, slot indices, workspace too
- * small), UNSUPPORTED (more than 1024 projections or 1000 phases, more than
- * 256 SMs, or a phase that does not fit the kernel's shared memory), CUDA.
- */
-BITLINEAR_API bitlinear_status_t bitlinear_chain_prepare(int64_t M, int64_t K0,
-                                                         const bitlinear_chain_proj_t *projs,
-                                                         int32_t nproj, float eps, void *workspace,
-                                                         size_t workspace_bytes,
-                                                         bitlinear_chain_plan_t *plan, void *stream);
-
-/*
- * Runs a prepared chain on x (device bf16 [M, K0], 16-byte aligned):
- * one cooperative kernel launch with one CTA per SM (capturable in a CUDA
- * graph).  Weights are static, as for bitlinear_forward.  Launches on one
- * workspace must not overlap in time.  A bounded wait that expires sets the
- * status word read by bitlinear_check_status.
- * Errors: INVALID_ARG (not a prepared plan, bad x), CUDA (launch failure,
- * e.g. the SMs cannot all be held at once).
- */
-BITLINEAR_API bitlinear_status_t bitlinear_chain_run(const bitlinear_chain_plan_t *plan,
-                                                     const void *x_bf16, void *stream);
-
-/* Test hook: force the K-split of every phase of chains prepared after
- * this call (0 restores the automatic choice). */
-BITLINEAR_API void bitlinear_chain_set_split(int32_t split);
 
 /*
  * Reads and clears the current device's kernel status word after

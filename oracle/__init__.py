@@ -57,12 +57,16 @@ def lib():
         L.bl_oracle_unpack.restype = I64
         L.bl_oracle_quant_act.argtypes = [P, P, I64, I64, ctypes.c_float, P, P]
         L.bl_oracle_matmul.argtypes = [P, P, I64, I64, I64, P]
+        L.bl_oracle_splitmix64.argtypes = [ctypes.c_uint64, I64, P]
+        L.bl_oracle_ternary_hash.argtypes = [ctypes.c_uint64, I64, I64, I64, P]
         L.bl_oracle_matmul.restype = ctypes.c_int
         L.bl_oracle_matmul_pairs.argtypes = [P, P, I64, P, P, I64, P]
         L.bl_oracle_epilogue.argtypes = [P, P, ctypes.c_float, I64, I64, P]
         L.bl_oracle_f32_to_bf16.argtypes = [ctypes.c_float]
         L.bl_oracle_f32_to_bf16.restype = ctypes.c_uint16
         L.bl_oracle_threads.restype = ctypes.c_int
+        L.bl_oracle_set_threads.argtypes = [ctypes.c_int]
+        L.bl_oracle_set_threads.restype = None
         _lib = L
     return _lib
 
@@ -169,6 +173,11 @@ def threads() -> int:
     return int(lib().bl_oracle_threads())
 
 
+def set_threads(n: int) -> None:
+    """Threads of the oracle's parallel loops (n <= 0: all cores)."""
+    lib().bl_oracle_set_threads(int(n))
+
+
 def forward(x_bf16: np.ndarray, w: np.ndarray, eps_w: float, eps_a: float, gain_bf16=None):
     """The whole path on the CPU: (gamma, packed, q, s_tok, acc, out_bf16)."""
     g = gamma(w)
@@ -178,3 +187,18 @@ def forward(x_bf16: np.ndarray, w: np.ndarray, eps_w: float, eps_a: float, gain_
     acc = matmul(q, wq)
     out = epilogue(acc, s, g)
     return g, packed, q, s, acc, out
+
+
+def splitmix64(seed: int, n: int) -> np.ndarray:
+    """The first n outputs of SplitMix64 seeded with `seed` (uint64)."""
+    out = np.empty(n, dtype=np.uint64)
+    lib().bl_oracle_splitmix64(ctypes.c_uint64(seed & (2**64 - 1)), n, _ptr(out))
+    return out
+
+
+def ternary_hash(word: int, K: int, n0: int, n1: int) -> np.ndarray:
+    """Rows [n0, n1) of the ternary matrix keyed by `word` (int8, {-1,0,1}):
+    the synthetic weights of the stacked workloads, from SplitMix64."""
+    out = np.empty((n1 - n0, K), dtype=np.int8)
+    lib().bl_oracle_ternary_hash(ctypes.c_uint64(word & (2**64 - 1)), K, n0, n1, _ptr(out))
+    return out

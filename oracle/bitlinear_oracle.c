@@ -292,6 +292,16 @@ void bl_oracle_epilogue(const int32_t *acc, const float *s_tok, float gamma, int
     }
 }
 
+/* Sets the number of OpenMP threads of the parallel loops (timing of the
+   single-threaded baseline); n <= 0 restores all cores. */
+void bl_oracle_set_threads(int n) {
+#ifdef _OPENMP
+    omp_set_num_threads(n > 0 ? n : omp_get_num_procs());
+#else
+    (void)n;
+#endif
+}
+
 /* Number of OpenMP threads the parallel loops above use. */
 int bl_oracle_threads(void) {
     int t = 1;
@@ -305,4 +315,46 @@ int bl_oracle_threads(void) {
         }
     }
     return t;
+}
+
+/* ------------------------------------------------------------------ */
+/* Synthetic ternary weights by a counter-based generator (inputs, not */
+/* the method).  The large stacked workloads draw their weights on the */
+/* device, element by element, from SplitMix64 (Steele, Lea and Flood, */
+/* "Fast splittable pseudorandom number generators", OOPSLA 2014): the */
+/* i-th output (i = 0, 1, ...) of SplitMix64 seeded with s is          */
+/* mix(s + (i+1)*0x9E3779B97F4A7C15).  A matrix keyed by `word` (its   */
+/* workload seed, layer and projection) takes s = the first output of  */
+/* SplitMix64 seeded with `word`; its element (n, k) is the output     */
+/* i = n*K + k of SplitMix64 seeded with s, mapped to {-1, 0, +1} as   */
+/* floor(hi32 * 3 / 2^32) - 1 (hi32: the output's upper 32 bits).      */
+/* This implementation is written from that definition alone; the     */
+/* device side has its own.                                            */
+/* ------------------------------------------------------------------ */
+
+static uint64_t splitmix_mix(uint64_t z) {
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+/* The first n outputs of SplitMix64 seeded with `seed`. */
+void bl_oracle_splitmix64(uint64_t seed, int64_t n, uint64_t *out) {
+    uint64_t x = seed;
+    for (int64_t i = 0; i < n; ++i) {
+        x += 0x9E3779B97F4A7C15ull;
+        out[i] = splitmix_mix(x);
+    }
+}
+
+/* Rows [n0, n1) of the [N, K] ternary matrix keyed by `word`, row-major. */
+void bl_oracle_ternary_hash(uint64_t word, int64_t K, int64_t n0, int64_t n1, int8_t *out) {
+    uint64_t s;
+    bl_oracle_splitmix64(word, 1, &s);
+    for (int64_t n = n0; n < n1; ++n)
+        for (int64_t k = 0; k < K; ++k) {
+            const uint64_t i = (uint64_t)n * (uint64_t)K + (uint64_t)k;
+            const uint64_t v = splitmix_mix(s + (i + 1u) * 0x9E3779B97F4A7C15ull);
+            out[(n - n0) * K + k] = (int8_t)((int)(((v >> 32) * 3u) >> 32) - 1);
+        }
 }

@@ -163,7 +163,7 @@ def test_decode_gemv_parity(M, N, K):
     check_full(w, x)
 
 
-@pytest.mark.parametrize("M", [18, 33, 48, 63])
+@pytest.mark.parametrize("M", [17, 18, 33, 48, 63, 64])
 @pytest.mark.parametrize("N,K", [(512, 256), (200, 8640), (2560, 2560)])
 def test_chunked_gemv_parity(M, N, K):
     # 16 < M <= 64: the decode GEMV in 16-token chunks (a partial last chunk included)
@@ -172,9 +172,10 @@ def test_chunked_gemv_parity(M, N, K):
     check_full(w, x)
 
 
-@pytest.mark.parametrize("M", [17, 64, 65, 128, 129, 200, 256, 300])
+@pytest.mark.parametrize("M", [65, 80, 128, 129, 200, 256, 300])
 @pytest.mark.parametrize("N,K", [(512, 256), (200, 8640), (144, 144), (1040, 1280)])
 def test_prefill_gemm_parity(M, N, K):
+    # bitlinear_forward above 64 tokens: the tcgen05 GEMM with int8 activations
     w = inputs.weights_fp32(N, K, seed=11 * N + K)
     x = inputs.activations_bf16(M, K, seed=13 * M + K, outlier_frac=0.01)
     check_full(w, x)
@@ -349,3 +350,4 @@ def test_bounded_wait_timeout_is_reported_and_recovers():
     assert bl.bitlinear_check_status() == bl.OK
     check_full(w, x)
     assert bl.bitlinear_check_status() == bl.OK
+
