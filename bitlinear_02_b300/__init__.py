@@ -22,7 +22,7 @@ __all__ = [
     "bitlinear_pack_ternary",
     "bitlinear_quant_act", "bitlinear_forward", "bitlinear_check_status",
     "bitlinear_quant_act_f16", "bitlinear_forward_f16", "quant_act_f16", "forward_f16",
-    "bitlinear_set_wait_limit", "bitlinear_status_string", "bitlinear_version",
+    "bitlinear_set_wait_limit", "bitlinear_set_engine", "bitlinear_status_string", "bitlinear_version",
     "pack_weights", "pack_ternary", "quant_act", "forward", "bitlinear",
     "FusedProj", "bitlinear_fused_stats_bytes", "bitlinear_act_stats", "bitlinear_forward_fused",
     "bitlinear_fused_factors", "fused_factors", "new_stats",
@@ -83,6 +83,7 @@ def load_library():
     L.bitlinear_check_status.argtypes = [P]
     L.bitlinear_set_wait_limit.argtypes = [ctypes.c_uint32]
     L.bitlinear_set_wait_limit.restype = None
+    L.bitlinear_set_engine.argtypes = [ctypes.c_int32, ctypes.c_int32]
     L.bitlinear_quant_act_f16.argtypes = [P, P, I64, I64, F, P, P, P]
     L.bitlinear_fused_stats_bytes.argtypes = []
     L.bitlinear_fused_stats_bytes.restype = ctypes.c_size_t
@@ -93,7 +94,7 @@ def load_library():
     for name in ("bitlinear_pack_weights", "bitlinear_pack_weights_noalloc", "bitlinear_pack_ternary", "bitlinear_quant_act",
                  "bitlinear_forward", "bitlinear_check_status",
                  "bitlinear_quant_act_f16", "bitlinear_forward_f16", "bitlinear_act_stats",
-                 "bitlinear_forward_fused", "bitlinear_fused_factors"):
+                 "bitlinear_forward_fused", "bitlinear_fused_factors", "bitlinear_set_engine"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -232,6 +233,11 @@ def bitlinear_check_status(stream=None) -> int:
 
 def bitlinear_set_wait_limit(iterations: int) -> None:
     load_library().bitlinear_set_wait_limit(int(iterations))
+
+
+def bitlinear_set_engine(gemv_max_tokens: int = -1, split_k: int = 0) -> None:
+    """Engine choice of the forward calls (-1 / 0 restore the defaults)."""
+    _check(load_library().bitlinear_set_engine(int(gemv_max_tokens), int(split_k)), "bitlinear_set_engine")
 
 
 # ------------------------------------------------------------ convenience ---

@@ -11,10 +11,10 @@ cudaError_t launch_gemv(const int8_t *q, const float *tok_scale, const uint8_t *
                         int32_t *acc_out, cudaStream_t st, int num_sms);
 cudaError_t launch_gemm(const int8_t *q, const float *tok_scale, const uint8_t *packed,
                         const float *gamma, int M, int N, int K, __nv_bfloat16 *out,
-                        int32_t *acc_out, cudaStream_t st, uint32_t wait_limit);
+                        int32_t *acc_out, cudaStream_t st, uint32_t wait_limit, int split);
 cudaError_t launch_gemm16(const void *q16, const float *tok_scale, const uint8_t *packed,
                           const float *gamma, int M, int N, int K, __nv_bfloat16 *out,
-                          int32_t *acc_out, cudaStream_t st, uint32_t wait_limit);
+                          int32_t *acc_out, cudaStream_t st, uint32_t wait_limit, int split);
 cudaError_t gemm_status(unsigned int *out, cudaStream_t st);
 
 namespace {
@@ -57,10 +57,25 @@ extern "C" void bitlinear_set_wait_limit(uint32_t iterations) {
     bl::g_wait_limit.store(iterations ? iterations : bl::kDefaultWaitLimit);
 }
 
-// Batches up to this size run on the decode GEMV engine (16-token chunks in
-// one launch); larger ones on the tensor-core GEMM, whose 128-row tiles
-// leave most SMs idle below a few hundred tokens.
+// Batches up to gemv_max_tokens run on the decode GEMV engine (16-token
+// chunks in one launch, at most kGemvMaxM); larger ones on the tensor-core
+// GEMM.
 constexpr int64_t kGemvMaxM = 64;
+namespace bl {
+namespace {
+constexpr int32_t kDefaultGemvMaxTokens = 64;
+std::atomic<int32_t> g_gemv_max_tokens{kDefaultGemvMaxTokens};
+std::atomic<int32_t> g_split_k{0};
+}  // namespace
+}  // namespace bl
+
+extern "C" bitlinear_status_t bitlinear_set_engine(int32_t gemv_max_tokens, int32_t split_k) {
+    if (gemv_max_tokens < -1 || gemv_max_tokens > kGemvMaxM || split_k < 0 || split_k > 16)
+        return BITLINEAR_ERR_INVALID_ARG;
+    bl::g_gemv_max_tokens.store(gemv_max_tokens < 0 ? bl::kDefaultGemvMaxTokens : gemv_max_tokens);
+    bl::g_split_k.store(split_k);
+    return BITLINEAR_OK;
+}
 
 extern "C" bitlinear_status_t bitlinear_forward(const int8_t *q, const float *tok_scale,
                                                 const uint8_t *packed, const float *gamma,
@@ -75,17 +90,17 @@ extern "C" bitlinear_status_t bitlinear_forward(const int8_t *q, const float *to
     if (!aligned16(q) || !aligned4(tok_scale) || !aligned16(packed) || !aligned4(gamma) ||
         !aligned16(out_bf16) || (acc_out && !aligned16(acc_out)))
         return BITLINEAR_ERR_INVALID_ARG;
-    if ((N + 15) / 16 > 65535 * 4 && M <= kGemvMaxM) return BITLINEAR_ERR_UNSUPPORTED;
+    if ((N + 15) / 16 > 65535 * 4 && M <= g_gemv_max_tokens.load()) return BITLINEAR_ERR_UNSUPPORTED;
     if ((M + 63) / 64 > 65535) return BITLINEAR_ERR_UNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     auto *out = static_cast<__nv_bfloat16 *>(out_bf16);
     cudaError_t e;
-    if (M <= kGemvMaxM)  // the decode GEMV, in 16-token chunks above 16
+    if (M <= g_gemv_max_tokens.load())  // the decode GEMV, in 16-token chunks above 16
         e = launch_gemv(q, tok_scale, packed, gamma, static_cast<int>(M), static_cast<int>(N),
                         static_cast<int>(K), out, acc_out, st, num_sms());
     else
         e = launch_gemm(q, tok_scale, packed, gamma, static_cast<int>(M), static_cast<int>(N),
-                        static_cast<int>(K), out, acc_out, st, g_wait_limit.load());
+                        static_cast<int>(K), out, acc_out, st, g_wait_limit.load(), g_split_k.load());
     return e == cudaSuccess ? BITLINEAR_OK : BITLINEAR_ERR_CUDA;
 }
 
@@ -105,7 +120,7 @@ extern "C" bitlinear_status_t bitlinear_forward_f16(const void *q_f16, const flo
     const cudaError_t e =
         launch_gemm16(q_f16, tok_scale, packed, gamma, static_cast<int>(M), static_cast<int>(N),
                       static_cast<int>(K), static_cast<__nv_bfloat16 *>(out_bf16), acc_out,
-                      static_cast<cudaStream_t>(stream), g_wait_limit.load());
+                      static_cast<cudaStream_t>(stream), g_wait_limit.load(), g_split_k.load());
     return e == cudaSuccess ? BITLINEAR_OK : BITLINEAR_ERR_CUDA;
 }
 

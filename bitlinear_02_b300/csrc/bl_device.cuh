@@ -124,45 +124,39 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     return false;
 }
 
+// Bounded wait of one thread that also gives up as soon as another role of
+// the CTA has raised the shared abort flag; a wait that expires raises it.
+// So one expired wait ends every role's waits within a few polls, instead
+// of each role spinning through its own limit.
+__device__ __forceinline__ bool mbar_wait_abortable(uint64_t *bar, uint32_t parity, uint32_t limit,
+                                                    volatile int *abort) {
+    for (uint32_t i = 0; i < limit; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+    }
+    *abort = 1;
+    return false;
+}
+// The same for a whole warp (every lane calls it; the outcome is the same in
+// every lane, so the warp stays converged for .sync.aligned instructions).
+__device__ __forceinline__ bool mbar_wait_abortable_warp(uint64_t *bar, uint32_t parity, uint32_t limit,
+                                                         volatile int *abort) {
+    for (uint32_t i = 0; i < limit; ++i) {
+        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+        if (__any_sync(0xffffffffu, *abort != 0)) return false;
+    }
+    *abort = 1;
+    return false;
+}
+
 // Arrive on an mbarrier and add `bytes` to the transaction count it waits for.
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
                  "r"(bytes)
                  : "memory");
 }
-// Bulk copy global -> shared (no tensor map); completes `bytes` of the
-// mbarrier's transaction count.  Both addresses 16-byte aligned, bytes a
-// multiple of 16.
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar))
-        : "memory");
-}
 
-// ---- relaxed gpu-scope accesses (tagged data exchange between CTAs) ----
-__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p) {
-    unsigned long long v;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v) {
-    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-// Weak 8-byte load/store through L2 only (no L1 allocation): for tagged
-// words, whose freshness the reader checks itself.  Unlike .relaxed.gpu
-// accesses these are pipelined freely.
-__device__ __forceinline__ unsigned long long ld_cg_u64(const unsigned long long *p) {
-    unsigned long long v;
-    asm volatile("ld.global.cg.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ ulonglong2 ld_cg_u64x2(const unsigned long long *p) {
-    ulonglong2 v;
-    asm volatile("ld.global.cg.v2.u64 {%0, %1}, [%2];" : "=l"(v.x), "=l"(v.y) : "l"(p) : "memory");
-    return v;
-}
+// ---- L2-only accesses (statistics exchanged between CTAs) ----
 // Bulk prefetch of a global range into L2 (16-byte aligned, size a multiple of 16).
 __device__ __forceinline__ void bulk_prefetch_l2(const void *p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
@@ -173,41 +167,7 @@ __device__ __forceinline__ unsigned ld_cg_u32(const void *p) {
     return v;
 }
 __device__ __forceinline__ float ld_cg_f32(const void *p) { return __uint_as_float(ld_cg_u32(p)); }
-__device__ __forceinline__ void st_cg_u64(unsigned long long *p, unsigned long long v) {
-    asm volatile("st.global.cg.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned *p) {
-    unsigned v;
-    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void red_relaxed_add_u32(unsigned *p, unsigned v) {
-    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-// Named barrier over the first `threads` threads of the block.
-__device__ __forceinline__ void named_sync(uint32_t id, uint32_t threads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-// Named barrier that also returns the OR of `pred` over the participants
-// (the same value in every thread).
-__device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t threads, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{.reg .pred p, q; setp.ne.u32 p, %3, 0;\n\t"
-        "barrier.red.or.pred q, %1, %2, p;\n\t"
-        "selp.u32 %0, 1, 0, q;}"
-        : "=r"(r)
-        : "r"(id), "r"(threads), "r"(static_cast<uint32_t>(pred))
-        : "memory");
-    return r != 0;
-}
-// Bounded mbarrier wait whose outcome is the same in every lane of the warp
-// (all lanes must call it).
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, uint32_t limit) {
-    for (uint32_t i = 0; i < limit; ++i)
-        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
-    return false;
-}
+
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -227,6 +187,20 @@ __device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
     int v;
     asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
     return v;
+}
+// Four consecutive 32-bit words of a cluster peer's shared memory (16-byte aligned).
+__device__ __forceinline__ int4 ld_cluster_v4(uint32_t addr) {
+    int4 v;
+    asm volatile("ld.shared::cluster.v4.s32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
 }
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
@@ -254,15 +228,6 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16, fp32 accumulate.
-__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                           uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{.reg .pred p; setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
 // D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16, fp32 accumulate; A is
 // 128 rows (lanes) x 16 f16 (8 columns, two f16 per column) in tensor memory.
 __device__ __forceinline__ void tc_mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
@@ -273,17 +238,6 @@ __device__ __forceinline__ void tc_mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, 
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
-// 32 lanes x 32 consecutive 32-bit columns from 32 registers per thread.
-__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
-        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
-        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
 // 32 lanes x 16 consecutive 32-bit columns from 16 registers per thread.
 __device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
@@ -292,6 +246,13 @@ __device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&r)[16])
         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
         "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
+}
+// One lane of a converged warp (elect.sync): the lane that issues the
+// warp's single-thread tcgen05 operations.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t p;
+    asm volatile("{.reg .pred P; .reg .b32 r; elect.sync r|P, 0xffffffff; selp.u32 %0, 1, 0, P;}" : "=r"(p));
+    return p != 0;
 }
 __device__ __forceinline__ void tc_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");

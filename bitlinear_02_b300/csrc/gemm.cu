@@ -12,20 +12,33 @@
 // CTA tile: 128 weight rows (MMA M, TMEM lanes) x BN tokens (MMA N, TMEM
 // columns); k advances 64 per pipeline stage.  Roles:
 //   - loader (warp 9, one thread): per stage, a 2-D tensor-map copy of the
-//     int8 activation tile (BN tokens x 64 k) and one 3-D tensor-map copy of
-//     the eight 512-byte packed weight tiles, into the stage's raw buffers;
+//     activation tile (BN tokens x 64 k) and one 3-D tensor-map copy of the
+//     eight 512-byte packed weight tiles, into the stage's buffers;
 //   - converters (warps 0-7): the weight operand A lives in tensor memory:
-//     warps 0-3 each own 32 rows (their TMEM lane quarter), expand the
+//     warps 0-3 / 4-7 each own 32 rows (their TMEM lane quarter), expand the
 //     row's 2-bit codes to f16 in registers and store them with tcgen05.st;
-//     all eight warps expand the int8 tile to f16 into the 128-byte-
-//     swizzled K-major B tile in shared memory;
-//   - MMA issuer (warp 8, one thread): tcgen05.mma kind::f16, A from TMEM,
-//     B from shared memory, 4 x K16 per stage, committed to the stage's
-//     "empty" mbarrier.
-// No thread waits on a global load in the main loop.  After the last stage
-// warps 0-7 read the accumulator with tcgen05.ld and apply the rescale
-// epilogue.  Every mbarrier wait is bounded; an expired wait sets a device
-// status word.
+//     with int8 activations all eight warps also expand the int8 tile to f16
+//     into the 128-byte-swizzled K-major B tile in shared memory;
+//   - MMA issuer (warp 8): the whole warp waits, one elected lane issues
+//     tcgen05.mma kind::f16 (A from TMEM, B from shared memory), 4 x K16 per
+//     stage, committed to the stage's "empty" mbarrier.  (Issue from an
+//     elected lane of a converged warp costs a fraction of issue from one
+//     lane of a diverged warp.)
+// After the last stage warps 0-7 read the accumulator with tcgen05.ld and
+// apply the rescale epilogue.
+//
+// Split K (a cluster of S CTAs per output tile): where the output tiles
+// alone would leave most SMs idle (a few dozen row tiles at 65-256 tokens),
+// the S CTAs of a cluster take consecutive k ranges of the same tile; each
+// moves its partial accumulator into its own shared memory as int32, and
+// after a cluster barrier CTA r sums the S partials (read through
+// distributed shared memory) over its share of the token columns and
+// writes those outputs.  Integer partials make the sum exact in any order.
+//
+// Every mbarrier wait is bounded.  A wait that expires raises a flag in
+// shared memory that ends every other role's waits at their next poll; the
+// CTA then drains the copies and MMAs it issued, frees its tensor memory and
+// sets the device status word.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -45,6 +58,15 @@ constexpr int kConverters = 256;                // warps 0-7
 constexpr int kThreads = kConverters + 64;      // + MMA warp 8 + loader warp 9
 constexpr uint32_t kDrainLimit = 1u << 30;
 constexpr uint32_t kRawA = 8 * 512;             // packed codes of 8 row groups, one k-tile
+constexpr int kMaxSplit = 16;                   // CTAs of a cluster sharing one tile's k range
+constexpr int kMinSplitStages = 4;              // 64-k stages per CTA of a split, at least
+
+// Control words behind the mbarriers.
+struct Ctl {
+    uint32_t tmem;  // TMEM base address from tcgen05.alloc
+    int issued;     // stages whose copies the loader issued
+    int abort;      // raised by the first wait that expires
+};
 
 template <int BN>
 struct Smem {
@@ -52,11 +74,29 @@ struct Smem {
     static constexpr uint32_t kRawB = BN * 64;              // int8 tile, BN tokens x 64 k
     static constexpr uint32_t kRawStage = kRawA + kRawB;    // packed codes | int8 tile
     static constexpr uint32_t kRawBase = kOps * kTileB;     // operand tiles first: 1024-aligned
-    static constexpr uint32_t kBytes = kRawBase + kRaw * kRawStage + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr uint32_t kBarOff = kRawBase + kRaw * kRawStage;
+    static constexpr uint32_t kBytes = kBarOff + 1024 /*align*/ + 256 /*barriers*/;
     // TMEM: accumulator in columns [0, BN), weight stages after it (32 columns each)
     static constexpr uint32_t kACol = BN;
     static constexpr uint32_t kCols = BN + 32 * kOps <= 256 ? 256 : 512;
+    static_assert(128u * BN * 4u <= kBarOff, "a split's int32 partial tile fits below the barriers");
 };
+
+// f16 activations: stage = swizzled f16 tile | packed codes.
+template <int BN, int NSTG>
+struct Smem16 {
+    static constexpr uint32_t kTileB = BN * 128;
+    static constexpr uint32_t kStage = kTileB + kRawA;  // multiple of 1024
+    static constexpr uint32_t kBarOff = NSTG * kStage;
+    static constexpr uint32_t kBytes = kBarOff + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr uint32_t kACol = BN;
+    static constexpr uint32_t kCols = BN + 32 * NSTG <= 128 ? 128 : (BN + 32 * NSTG <= 256 ? 256 : 512);
+    static_assert(128u * BN * 4u <= kBarOff, "a split's int32 partial tile fits below the barriers");
+};
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
+}
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
     asm volatile(
@@ -79,31 +119,206 @@ __device__ __forceinline__ void tma_load_w8(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+// The 2-bit codes of one weight row at 32 k (two 16-k words of the row's
+// lane in the packed tile) -> 16 registers of f16 pairs (Wq = code - 1),
+// i.e. 16 TMEM columns.  `w0`, `w1`: the row's 32-bit code words.
+__device__ __forceinline__ void expand_codes(uint32_t w0, uint32_t w1, uint32_t (&f)[16]) {
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        f[p] = hadd2(((w0 >> (2 * p)) & 0x00030003u) | 0x64006400u, 0xE401E401u);
+        f[8 + p] = hadd2(((w1 >> (2 * p)) & 0x00030003u) | 0x64006400u, 0xE401E401u);
+    }
+}
+
+// One output element: bf16(acc * (gamma * s_tok)), both products rounded to
+// nearest in fp32.
+__device__ __forceinline__ __nv_bfloat16 rescale(int a, float gam, float ts) {
+    return __float2bfloat16_rn(__fmul_rn(static_cast<float>(a), __fmul_rn(gam, ts)));
+}
+
+// The accumulator tile (TMEM lanes = 128 weight rows, columns = BN tokens)
+// to the outputs, by warps 0-7 (warp w: lane quarter w % 4, column half w / 4).
 template <int BN>
+__device__ __forceinline__ void store_tile(uint32_t tmem, int warp, int lane, int tile, int tok0, int M, int N,
+                                           float gam, const float *__restrict__ tok_scale,
+                                           __nv_bfloat16 *__restrict__ out, int32_t *__restrict__ acc_out) {
+    const int lq = warp & 3, ch = warp >> 2;
+    const int n = tile * 128 + 32 * lq + lane;
+#pragma unroll 1
+    for (int col = ch * (BN / 2); col < (ch + 1) * (BN / 2); col += 16) {
+        uint32_t v[16];
+        tc_ld16(tmem + (static_cast<uint32_t>(32 * lq) << 16) + col, v);
+        tc_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int tk = tok0 + col + i;
+            if (tk < M && n < N) {
+                const int a = __float2int_rn(__uint_as_float(v[i]));
+                out[static_cast<int64_t>(tk) * N + n] = rescale(a, gam, tok_scale[tk]);
+                if (acc_out) acc_out[static_cast<int64_t>(tk) * N + n] = a;
+            }
+        }
+    }
+}
+
+// Split K, step 1: this CTA's partial accumulator tile into its own shared
+// memory as int32 [BN tokens][128 rows] (exact: every partial is an integer
+// below 2^24).
+template <int BN>
+__device__ __forceinline__ void stage_partial(uint32_t tmem, int warp, int lane, int32_t *red) {
+    const int lq = warp & 3, ch = warp >> 2, row = 32 * lq + lane;
+#pragma unroll 1
+    for (int col = ch * (BN / 2); col < (ch + 1) * (BN / 2); col += 16) {
+        uint32_t v[16];
+        tc_ld16(tmem + (static_cast<uint32_t>(32 * lq) << 16) + col, v);
+        tc_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) red[(col + i) * 128 + row] = __float2int_rn(__uint_as_float(v[i]));
+    }
+}
+
+// Split K, step 2 (after a cluster barrier): CTA `split` of the S sums the S
+// partial tiles over its share of the token columns, reading the peers'
+// shared memory, and writes those outputs.  Each item is four consecutive
+// rows of one token column (a 16-byte read from every peer).
+template <int BN>
+__device__ __forceinline__ void reduce_partials(const int32_t *red, int split, int S, int tid, int tile, int tok0,
+                                                int M, int N, float gam, const float *__restrict__ tok_scale,
+                                                __nv_bfloat16 *__restrict__ out, int32_t *__restrict__ acc_out) {
+    const int per = (BN + S - 1) / S;
+    const int c0 = split * per, c1 = c0 + per < BN ? c0 + per : BN;
+    const uint32_t base = smem_addr(red);
+    const bool vec = (N & 3) == 0;  // then a 4-row group is all in range and 8/16-byte aligned
+    for (int item = tid; item < (c1 - c0) * 32; item += kConverters) {
+        const int col = c0 + (item >> 5), r4 = (item & 31) * 4;
+        const int tk = tok0 + col, n0 = tile * 128 + r4;
+        if (tk >= M || n0 >= N) continue;
+        const uint32_t off = base + static_cast<uint32_t>((col * 128 + r4) * 4);
+        int a[4] = {0, 0, 0, 0};
+        for (int p0 = 0; p0 < S; p0 += 8) {
+            int4 part[8];
+#pragma unroll
+            for (int p = 0; p < 8; ++p)
+                part[p] = p0 + p < S ? ld_cluster_v4(cluster_map(off, static_cast<uint32_t>(p0 + p)))
+                                     : make_int4(0, 0, 0, 0);
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+                a[0] += part[p].x;
+                a[1] += part[p].y;
+                a[2] += part[p].z;
+                a[3] += part[p].w;
+            }
+        }
+        const float ts = tok_scale[tk];
+        const int64_t o = static_cast<int64_t>(tk) * N + n0;
+        if (vec) {
+            __nv_bfloat162 lo, hi;
+            lo.x = rescale(a[0], gam, ts);
+            lo.y = rescale(a[1], gam, ts);
+            hi.x = rescale(a[2], gam, ts);
+            hi.y = rescale(a[3], gam, ts);
+            uint2 pk;
+            pk.x = *reinterpret_cast<uint32_t *>(&lo);
+            pk.y = *reinterpret_cast<uint32_t *>(&hi);
+            *reinterpret_cast<uint2 *>(out + o) = pk;
+            if (acc_out) *reinterpret_cast<int4 *>(acc_out + o) = make_int4(a[0], a[1], a[2], a[3]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (n0 + j < N) {
+                    out[o + j] = rescale(a[j], gam, ts);
+                    if (acc_out) acc_out[o + j] = a[j];
+                }
+        }
+    }
+}
+
+// The part every kernel ends with: the outputs (directly, or through the
+// cluster's split-K reduction), the status word, and the teardown (drain the
+// issued copies and MMAs, free the tensor memory).  All threads call it.
+template <int BN, bool SPLIT>
+__device__ __forceinline__ void finish_tile(uint8_t *smem, uint32_t tmem, uint32_t cols, uint64_t *accum,
+                                            uint64_t *full, int nfull, const Ctl *ctl, volatile int *abort,
+                                            bool timed_out, int split, int S, int tile, int M, int N,
+                                            const float *__restrict__ tok_scale, const float *__restrict__ gamma,
+                                            __nv_bfloat16 *__restrict__ out, int32_t *__restrict__ acc_out,
+                                            uint32_t wait_limit) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tok0 = blockIdx.y * BN;
+    if (warp < 8) {
+        const bool have = mbar_wait_abortable_warp(accum, 0, wait_limit, abort);
+        if (!have) timed_out = true;
+        tc_fence_after();
+        if (have) {
+            if constexpr (SPLIT)
+                stage_partial<BN>(tmem, warp, lane, reinterpret_cast<int32_t *>(smem));
+            else
+                store_tile<BN>(tmem, warp, lane, tile, tok0, M, N, *gamma, tok_scale, out, acc_out);
+        }
+    }
+    if constexpr (SPLIT) {
+        __syncwarp();
+        cluster_sync();  // every CTA's partial tile is in its shared memory
+        if (warp < 8)
+            reduce_partials<BN>(reinterpret_cast<const int32_t *>(smem), split, S, tid, tile, tok0, M, N, *gamma,
+                                tok_scale, out, acc_out);
+        __syncwarp();
+        cluster_sync();  // the peers have read this CTA's partials
+    }
+    if (timed_out) atomicOr(&g_gemm_status, 1u);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 8) {
+        // All MMAs must have retired, and every copy landed, before the
+        // accumulator and shared memory are released.
+        if (lane == 0) {
+            mbar_wait_bounded(accum, 0, kDrainLimit);
+            const int n = ctl->issued;  // only copies that were issued can be in flight
+            for (int j = n > nfull ? n - nfull : 0; j < n; ++j)
+                mbar_wait_bounded(&full[j % nfull], (j / nfull) & 1, kDrainLimit);
+        }
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, cols);
+    }
+}
+
+// The k range (in 64-k stages) of CTA `split` of S.
+__device__ __forceinline__ void split_range(int NS, int split, int S, int &st0, int &ns) {
+    st0 = static_cast<int>(static_cast<int64_t>(NS) * split / S);
+    ns = static_cast<int>(static_cast<int64_t>(NS) * (split + 1) / S) - st0;
+}
+
+// ---------------------------------------------------------------------------
+// int8 activations (bitlinear_quant_act).
+// ---------------------------------------------------------------------------
+template <int BN, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap wmap,
-                const float *__restrict__ tok_scale,
-                const uint8_t *__restrict__ packed, const float *__restrict__ gamma, int M, int N,
-                int K, int KT, int RGN, __nv_bfloat16 *__restrict__ out,
-                int32_t *__restrict__ acc_out, uint32_t wait_limit) {
+                const float *__restrict__ tok_scale, const float *__restrict__ gamma, int M, int N, int KT,
+                int RGN, __nv_bfloat16 *__restrict__ out, int32_t *__restrict__ acc_out, uint32_t wait_limit) {
     using L = Smem<BN>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~static_cast<uintptr_t>(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kRawBase + kRaw * L::kRawStage);
+    uint8_t *smem = align1024(smem_raw);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
     uint64_t *raw_full = bars, *raw_empty = bars + kRaw;
     uint64_t *mma_full = bars + 2 * kRaw, *op_empty = bars + 2 * kRaw + kOps;
     uint64_t *accum = bars + 2 * kRaw + 2 * kOps;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum + 1);
-    int *issued = reinterpret_cast<int *>(tmem_slot + 1);  // stages whose copies the loader issued
+    Ctl *ctl = reinterpret_cast<Ctl *>(accum + 1);
+    volatile int *abort = &ctl->abort;
 
     pdl_launch_dependents();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int NS = 2 * KT;  // 64-k stages
+    const int S = SPLIT ? static_cast<int>(cluster_size()) : 1;
+    const int split = SPLIT ? static_cast<int>(cluster_rank()) : 0;
+    const int tile = blockIdx.x / S;
+    int st0, ns;
+    split_range(2 * KT, split, S, st0, ns);
     bool timed_out = false;
 
     if (tid == 0) {
-        *issued = 0;
+        ctl->issued = 0;
+        ctl->abort = 0;
         for (int i = 0; i < kRaw; ++i) {
             mbar_init(&raw_full[i], 1);
             mbar_init(&raw_empty[i], kConverters);
@@ -116,14 +331,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_fence_init();
     }
     if (warp == 8) {
-        tmem_alloc(tmem_slot, L::kCols);
+        tmem_alloc(&ctl->tmem, L::kCols);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const int rg0 = blockIdx.x * 8;
+    const uint32_t tmem = ctl->tmem;
+    const int rg0 = tile * 8;
     const int nrg = RGN - rg0 < 8 ? RGN - rg0 : 8;
 
     if (warp == 9) {
@@ -133,9 +348,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the packed weights are static: their copies may start before the
             // previous kernel finished; the activations may not
             bool waited = false;
-            for (int st = 0; st < NS; ++st) {
-                const int rs = st % kRaw;
-                if (!mbar_wait_bounded(&raw_empty[rs], ((st / kRaw) & 1) ^ 1, wait_limit)) {
+            for (int j = 0; j < ns; ++j) {
+                const int st = st0 + j, rs = j % kRaw;
+                if (!mbar_wait_abortable(&raw_empty[rs], ((j / kRaw) & 1) ^ 1, wait_limit, abort)) {
                     timed_out = true;
                     break;
                 }
@@ -147,9 +362,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     waited = true;
                 }
                 tma_load_2d(raw + kRawA, &qmap, st * 64, blockIdx.y * BN, &raw_full[rs]);
-                *issued = st + 1;
+                ctl->issued = j + 1;
             }
         }
+        __syncwarp();
     } else if (warp < 8) {
         // Warp w owns TMEM lane quarter w % 4 (weight rows 32(w%4) + lane)
         // and half t' = w / 4 of each stage's 32 weight columns.
@@ -158,32 +374,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_ok = rgl < nrg;
         const uint32_t a_off = 512 * rgl + 16 * 4 * (ri & 7) + 4 * (ri >> 3);
         const uint32_t a_lane = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-        for (int st = 0; st < NS; ++st) {
-            const int rs = st % kRaw, slot = st % kOps;
-            if (!mbar_wait_bounded(&raw_full[rs], (st / kRaw) & 1, wait_limit)) timed_out = true;
-            if (!mbar_wait_bounded(&op_empty[slot], ((st / kOps) & 1) ^ 1, wait_limit)) timed_out = true;
+        for (int j = 0; j < ns; ++j) {
+            const int st = st0 + j, rs = j % kRaw, slot = j % kOps;
+            if (!mbar_wait_abortable_warp(&raw_full[rs], (j / kRaw) & 1, wait_limit, abort) ||
+                !mbar_wait_abortable_warp(&op_empty[slot], ((j / kOps) & 1) ^ 1, wait_limit, abort)) {
+                timed_out = true;
+                break;
+            }
             const uint8_t *raw = smem + L::kRawBase + rs * L::kRawStage;
             uint8_t *stage = smem + slot * L::kTileB;
             {
                 // column c of the stage holds k = 2c, 2c+1: word (t' = c/16, P = (c%16)/8), pair p = c%8
-                const int hf = st & 1;
+                const uint32_t *wp = reinterpret_cast<const uint32_t *>(raw + a_off + 16 * (2 * (st & 1) + t2));
                 uint32_t f[16];
-#pragma unroll
-                for (int P = 0; P < 2; ++P) {
-                    const uint32_t w = row_ok ? *reinterpret_cast<const uint32_t *>(
-                                                    raw + a_off + 16 * (2 * hf + t2) + 8 * P)
-                                              : 0x55555555u;
-#pragma unroll
-                    for (int p = 0; p < 8; ++p)
-                        f[8 * P + p] = hadd2(((w >> (2 * p)) & 0x00030003u) | 0x64006400u, 0xE401E401u);  // Wq
-                }
+                expand_codes(row_ok ? wp[0] : 0x55555555u, row_ok ? wp[2] : 0x55555555u, f);
                 tc_st16(tmem + a_lane + L::kACol + 32 * slot + 16 * t2, f);
             }
             // int8 tile (token-major, 64 bytes per token) -> swizzled f16 tile
             const uint8_t *rb = raw + kRawA;
 #pragma unroll
-            for (int j = 0; j < BN * 4 / kConverters; ++j) {
-                const int e = tid + kConverters * j;
+            for (int i = 0; i < BN * 4 / kConverters; ++i) {
+                const int e = tid + kConverters * i;
                 const int tok = e >> 2, ch = e & 3;
                 const uint4 xv = *reinterpret_cast<const uint4 *>(rb + 16 * e);
                 const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
@@ -203,109 +414,66 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(&mma_full[slot]);
         }
-    } else if (lane == 0) {
-        // ---------------- MMA issuer ----------------
+    } else {
+        // ---------------- MMA issuer (warp 8) ----------------
         constexpr uint32_t idesc = idesc_f16_f32(128, BN);
         const uint32_t base = smem_addr(smem);
-        for (int st = 0; st < NS; ++st) {
-            const int slot = st % kOps;
-            if (!mbar_wait_bounded(&mma_full[slot], (st / kOps) & 1, wait_limit)) timed_out = true;
+        for (int j = 0; j < ns; ++j) {
+            const int slot = j % kOps;
+            if (!mbar_wait_abortable_warp(&mma_full[slot], (j / kOps) & 1, wait_limit, abort)) {
+                timed_out = true;
+                break;
+            }
             tc_fence_after();
-            const uint64_t bd = sw128_desc(base + slot * L::kTileB);
-            const uint32_t at = tmem + L::kACol + 32 * slot;
+            if (elect_one()) {
+                const uint64_t bd = sw128_desc(base + slot * L::kTileB);
+                const uint32_t at = tmem + L::kACol + 32 * slot;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                tc_mma_f16_ta(tmem, at + 8 * kk, bd + 2 * kk, idesc, (st > 0 || kk > 0) ? 1u : 0u);
-            tc_commit(&op_empty[slot]);
+                for (int kk = 0; kk < 4; ++kk)
+                    tc_mma_f16_ta(tmem, at + 8 * kk, bd + 2 * kk, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(&op_empty[slot]);
+            }
+            __syncwarp();
         }
-        tc_commit(accum);
+        if (elect_one()) tc_commit(accum);
+        __syncwarp();
     }
 
-    // ---------------- epilogue (warps 0-7) ----------------
-    if (warp < 8) {
-        if (!mbar_wait_bounded(accum, 0, wait_limit)) timed_out = true;
-        tc_fence_after();
-        const int lq = warp & 3, ch = warp >> 2;
-        const float gam = *gamma;
-        const int n = blockIdx.x * 128 + 32 * lq + lane;
-#pragma unroll 1
-        for (int col = ch * (BN / 2); col < (ch + 1) * (BN / 2); col += 16) {
-            uint32_t v[16];
-            tc_ld16(tmem + (static_cast<uint32_t>(32 * lq) << 16) + col, v);
-            tc_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int tk = blockIdx.y * BN + col + i;
-                if (tk < M && n < N) {
-                    const int a = __float2int_rn(__uint_as_float(v[i]));
-                    const float f = __fmul_rn(gam, tok_scale[tk]);
-                    out[static_cast<int64_t>(tk) * N + n] =
-                        __float2bfloat16_rn(__fmul_rn(static_cast<float>(a), f));
-                    if (acc_out) acc_out[static_cast<int64_t>(tk) * N + n] = a;
-                }
-            }
-        }
-    }
-    if (timed_out) atomicOr(&g_gemm_status, 1u);
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 8) {
-        // All MMAs must have retired, and every copy landed, before the
-        // accumulator and shared memory are released.
-        if (lane == 0) {
-            mbar_wait_bounded(accum, 0, kDrainLimit);
-            const int n = *issued;  // only copies that were issued can be in flight
-            for (int st = n > kRaw ? n - kRaw : 0; st < n; ++st)
-                mbar_wait_bounded(&raw_full[st % kRaw], (st / kRaw) & 1, kDrainLimit);
-        }
-        __syncwarp();
-        tc_fence_after();
-        tmem_dealloc(tmem, L::kCols);
-    }
+    finish_tile<BN, SPLIT>(smem, tmem, L::kCols, accum, raw_full, kRaw, ctl, abort, timed_out, split, S, tile, M,
+                           N, tok_scale, gamma, out, acc_out, wait_limit);
 }
 
 // ---------------------------------------------------------------------------
-// Variant with f16 activations (bitlinear_quant_act_f16): the activation
-// tile arrives by tensor-map copy already in the 128-byte-swizzled K-major
-// layout the MMA reads, so the converter warps only expand the weight codes
-// into tensor memory.  Stage = swizzled f16 tile | packed codes.
+// f16 activations (bitlinear_quant_act_f16): the activation tile arrives by
+// tensor-map copy already in the 128-byte-swizzled K-major layout the MMA
+// reads, so the converter warps only expand the weight codes into tensor
+// memory.  NSTG stages of swizzled f16 tile | packed codes.
 // ---------------------------------------------------------------------------
-// NSTG stages; MINB CTAs per SM (a template parameter: with 2, one CTA's
-// prologue and epilogue could run under the other's main loop, but the
-// TMEM columns of both must then fit in 512; every launch uses MINB = 1).
-template <int BN, int NSTG>
-struct Smem16 {
-    static constexpr uint32_t kTileB = BN * 128;
-    static constexpr uint32_t kStage = kTileB + kRawA;  // multiple of 1024
-    static constexpr uint32_t kBytes = NSTG * kStage + 1024 /*align*/ + 256 /*barriers*/;
-    static constexpr uint32_t kACol = BN;
-    static constexpr uint32_t kCols = BN + 32 * NSTG <= 128 ? 128 : (BN + 32 * NSTG <= 256 ? 256 : 512);
-};
-
-template <int BN, int NSTG, int MINB>
-__global__ void __launch_bounds__(kThreads, MINB)
+template <int BN, int NSTG, bool SPLIT>
+__global__ void __launch_bounds__(kThreads, 1)
     gemm16_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap wmap,
-                  const float *__restrict__ tok_scale,
-                  const uint8_t *__restrict__ packed, const float *__restrict__ gamma, int M, int N,
-                  int K, int KT, int RGN, __nv_bfloat16 *__restrict__ out,
-                  int32_t *__restrict__ acc_out, uint32_t wait_limit) {
+                  const float *__restrict__ tok_scale, const float *__restrict__ gamma, int M, int N, int KT,
+                  int RGN, __nv_bfloat16 *__restrict__ out, int32_t *__restrict__ acc_out, uint32_t wait_limit) {
     using L = Smem16<BN, NSTG>;
-    static_assert(MINB * L::kCols <= 512, "the CTAs of an SM share 512 TMEM columns");
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~static_cast<uintptr_t>(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NSTG * L::kStage);
+    uint8_t *smem = align1024(smem_raw);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
     uint64_t *full = bars, *a_ready = bars + NSTG, *empty = bars + 2 * NSTG;
     uint64_t *accum = bars + 3 * NSTG;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum + 1);
-    int *issued = reinterpret_cast<int *>(tmem_slot + 1);
+    Ctl *ctl = reinterpret_cast<Ctl *>(accum + 1);
+    volatile int *abort = &ctl->abort;
 
     pdl_launch_dependents();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int NS = 2 * KT;  // 64-k stages
+    const int S = SPLIT ? static_cast<int>(cluster_size()) : 1;
+    const int split = SPLIT ? static_cast<int>(cluster_rank()) : 0;
+    const int tile = blockIdx.x / S;
+    int st0, ns;
+    split_range(2 * KT, split, S, st0, ns);
     bool timed_out = false;
     if (tid == 0) {
-        *issued = 0;
+        ctl->issued = 0;
+        ctl->abort = 0;
         for (int i = 0; i < NSTG; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&a_ready[i], kConverters / 2);
@@ -315,14 +483,14 @@ __global__ void __launch_bounds__(kThreads, MINB)
         mbar_fence_init();
     }
     if (warp == 8) {
-        tmem_alloc(tmem_slot, L::kCols);
+        tmem_alloc(&ctl->tmem, L::kCols);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const int rg0 = blockIdx.x * 8;
+    const uint32_t tmem = ctl->tmem;
+    const int rg0 = tile * 8;
     const int nrg = RGN - rg0 < 8 ? RGN - rg0 : 8;
 
     if (warp == 9) {
@@ -330,9 +498,9 @@ __global__ void __launch_bounds__(kThreads, MINB)
         if (lane == 0) {
             const uint32_t bytes = kRawA + L::kTileB;  // a full box: rows past N arrive zero-filled (unread)
             bool waited = false;
-            for (int st = 0; st < NS; ++st) {
-                const int s = st % NSTG;
-                if (!mbar_wait_bounded(&empty[s], ((st / NSTG) & 1) ^ 1, wait_limit)) {
+            for (int j = 0; j < ns; ++j) {
+                const int st = st0 + j, s = j % NSTG;
+                if (!mbar_wait_abortable(&empty[s], ((j / NSTG) & 1) ^ 1, wait_limit, abort)) {
                     timed_out = true;
                     break;
                 }
@@ -344,9 +512,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
                     waited = true;
                 }
                 tma_load_2d(stage, &qmap, st * 64, blockIdx.y * BN, &full[s]);
-                *issued = st + 1;
+                ctl->issued = j + 1;
             }
         }
+        __syncwarp();
     } else if (warp < 8) {
         // ---------------- converters: weight codes -> f16 in TMEM ----------------
         // Warp w owns TMEM lane quarter w % 4 (weight rows 32(w%4) + lane) and
@@ -356,95 +525,82 @@ __global__ void __launch_bounds__(kThreads, MINB)
         const bool row_ok = rgl < nrg;
         const uint32_t a_off = 512 * rgl + 16 * 4 * (ri & 7) + 4 * (ri >> 3);
         const uint32_t a_lane = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-        for (int st = warp >> 2; st < NS; st += 2) {
-            const int s = st % NSTG;
-            if (!mbar_wait_bounded(&full[s], (st / NSTG) & 1, wait_limit)) timed_out = true;
+        for (int j = warp >> 2; j < ns; j += 2) {
+            const int st = st0 + j, s = j % NSTG;
+            if (!mbar_wait_abortable_warp(&full[s], (j / NSTG) & 1, wait_limit, abort)) {
+                timed_out = true;
+                break;
+            }
             const uint8_t *codes = smem + s * L::kStage + L::kTileB;
-            const int hf = st & 1;
 #pragma unroll
             for (int t2 = 0; t2 < 2; ++t2) {  // two 16-column halves (fewer live registers)
+                const uint32_t *wp = reinterpret_cast<const uint32_t *>(codes + a_off + 16 * (2 * (st & 1) + t2));
                 uint32_t f[16];
-#pragma unroll
-                for (int P = 0; P < 2; ++P) {
-                    const uint32_t w = row_ok ? *reinterpret_cast<const uint32_t *>(codes + a_off + 16 * (2 * hf + t2) + 8 * P)
-                                              : 0x55555555u;
-#pragma unroll
-                    for (int p = 0; p < 8; ++p)
-                        f[8 * P + p] = hadd2(((w >> (2 * p)) & 0x00030003u) | 0x64006400u, 0xE401E401u);
-                }
+                expand_codes(row_ok ? wp[0] : 0x55555555u, row_ok ? wp[2] : 0x55555555u, f);
                 tc_st16(tmem + a_lane + L::kACol + 32 * s + 16 * t2, f);
             }
             tc_wait_st();
             tc_fence_before();
             mbar_arrive(&a_ready[s]);
         }
-    } else if (lane == 0) {
-        // ---------------- MMA issuer ----------------
+    } else {
+        // ---------------- MMA issuer (warp 8) ----------------
         constexpr uint32_t idesc = idesc_f16_f32(128, BN);
         const uint32_t base = smem_addr(smem);
-        for (int st = 0; st < NS; ++st) {
-            const int s = st % NSTG;
-            if (!mbar_wait_bounded(&full[s], (st / NSTG) & 1, wait_limit)) timed_out = true;
-            if (!mbar_wait_bounded(&a_ready[s], (st / NSTG) & 1, wait_limit)) timed_out = true;
+        for (int j = 0; j < ns; ++j) {
+            const int s = j % NSTG;
+            if (!mbar_wait_abortable_warp(&full[s], (j / NSTG) & 1, wait_limit, abort) ||
+                !mbar_wait_abortable_warp(&a_ready[s], (j / NSTG) & 1, wait_limit, abort)) {
+                timed_out = true;
+                break;
+            }
             tc_fence_after();
-            const uint64_t bd = sw128_desc(base + s * L::kStage);
-            const uint32_t at = tmem + L::kACol + 32 * s;
+            if (elect_one()) {
+                const uint64_t bd = sw128_desc(base + s * L::kStage);
+                const uint32_t at = tmem + L::kACol + 32 * s;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                tc_mma_f16_ta(tmem, at + 8 * kk, bd + 2 * kk, idesc, (st > 0 || kk > 0) ? 1u : 0u);
-            tc_commit(&empty[s]);
+                for (int kk = 0; kk < 4; ++kk)
+                    tc_mma_f16_ta(tmem, at + 8 * kk, bd + 2 * kk, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(&empty[s]);
+            }
+            __syncwarp();
         }
-        tc_commit(accum);
+        if (elect_one()) tc_commit(accum);
+        __syncwarp();
     }
 
-    // ---------------- epilogue (warps 0-7) ----------------
-    if (warp < 8) {
-        if (!mbar_wait_bounded(accum, 0, wait_limit)) timed_out = true;
-        tc_fence_after();
-        const int lq = warp & 3, ch = warp >> 2;
-        const float gam = *gamma;
-        const int n = blockIdx.x * 128 + 32 * lq + lane;
-#pragma unroll 1
-        for (int col = ch * (BN / 2); col < (ch + 1) * (BN / 2); col += 16) {
-            uint32_t v[16];
-            tc_ld16(tmem + (static_cast<uint32_t>(32 * lq) << 16) + col, v);
-            tc_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int tk = blockIdx.y * BN + col + i;
-                if (tk < M && n < N) {
-                    const int a = __float2int_rn(__uint_as_float(v[i]));
-                    const float f = __fmul_rn(gam, tok_scale[tk]);
-                    out[static_cast<int64_t>(tk) * N + n] =
-                        __float2bfloat16_rn(__fmul_rn(static_cast<float>(a), f));
-                    if (acc_out) acc_out[static_cast<int64_t>(tk) * N + n] = a;
-                }
-            }
-        }
-    }
-    if (timed_out) atomicOr(&g_gemm_status, 1u);
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 8) {
-        if (lane == 0) {
-            mbar_wait_bounded(accum, 0, kDrainLimit);
-            const int n = *issued;  // only copies that were issued can be in flight
-            for (int st = n > NSTG ? n - NSTG : 0; st < n; ++st)
-                mbar_wait_bounded(&full[st % NSTG], (st / NSTG) & 1, kDrainLimit);
-        }
-        __syncwarp();
-        tc_fence_after();
-        tmem_dealloc(tmem, L::kCols);
-    }
+    finish_tile<BN, SPLIT>(smem, tmem, L::kCols, accum, full, NSTG, ctl, abort, timed_out, split, S, tile, M, N,
+                           tok_scale, gamma, out, acc_out, wait_limit);
 }
 
-// Tensor map of the int8 activations [M, K] (row-major): BN x 64 boxes.
+// ------------------------------------------------------------------ host ---
+
 std::mutex g_encode_mutex;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-// The driver's tensor-map encoder, looked up once.
-cudaError_t tensor_map_encoder() {
-    std::lock_guard<std::mutex> lock(g_encode_mutex);
+// Tensor maps already encoded, keyed by address and shape: a map holds
+// nothing but those, so a cached one is valid for any buffer at that
+// address with that shape.
+struct MapEntry {
+    const void *ptr;
+    uint64_t key;
+    bool used;
+    CUtensorMap map;
+};
+constexpr int kMapCache = 64;
+MapEntry g_maps[kMapCache];
+int g_map_next = 0;
+
+// Encode a tiled tensor map through the driver (its entry point looked up
+// once), or copy it from the cache.  Caller holds g_encode_mutex.
+cudaError_t encode_locked(CUtensorMap *map, const void *ptr, uint64_t key, CUtensorMapDataType type, uint32_t rank,
+                          const cuuint64_t *dims, const cuuint64_t *strides, const cuuint32_t *box,
+                          CUtensorMapSwizzle swz) {
+    for (int i = 0; i < kMapCache; ++i)
+        if (g_maps[i].used && g_maps[i].ptr == ptr && g_maps[i].key == key) {
+            *map = g_maps[i].map;
+            return cudaSuccess;
+        }
     if (!g_encode) {
         cudaDriverEntryPointQueryResult qr;
         void *fn = nullptr;
@@ -452,105 +608,174 @@ cudaError_t tensor_map_encoder() {
         if (e != cudaSuccess || qr != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
         g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    const CUresult r = g_encode(map, type, rank, const_cast<void *>(ptr), dims, strides, box, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    MapEntry &slot = g_maps[g_map_next];
+    g_map_next = (g_map_next + 1) % kMapCache;
+    slot.ptr = ptr;
+    slot.key = key;
+    slot.map = *map;
+    slot.used = true;
     return cudaSuccess;
 }
 
+// Activations [M, K] row-major (int8, or f16 landing in the MMA's 128-byte
+// swizzle): boxes of 64 k x BN tokens.
 cudaError_t make_qmap(CUtensorMap *map, const void *q, int M, int K, int BN, bool f16) {
-    cudaError_t e0 = tensor_map_encoder();
-    if (e0 != cudaSuccess) return e0;
+    std::lock_guard<std::mutex> lock(g_encode_mutex);
+    const uint64_t key = 0u | (static_cast<uint64_t>(f16) << 1) | (static_cast<uint64_t>(BN) << 2) |
+                         (static_cast<uint64_t>(K) << 11) | (static_cast<uint64_t>(M) << 28);
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * (f16 ? 2u : 1u)};
     const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(BN)};
-    const cuuint32_t estr[2] = {1u, 1u};
-    const CUresult r = g_encode(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
-                                const_cast<void *>(q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                f16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    return encode_locked(map, q, key, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dims,
+                         strides, box, f16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-// Tensor map of the packed weights (layout of bitlinear_packed_bytes): u64
-// [RGN][KT][64], boxes of 64 x 1 x 8.
+// Packed weights (layout of bitlinear_packed_bytes) as u64 [RGN][KT][64],
+// boxes of 64 x 1 x 8.
 cudaError_t make_wmap(CUtensorMap *map, const uint8_t *packed, int RGN, int KT) {
-    cudaError_t e = tensor_map_encoder();
-    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_encode_mutex);
+    const uint64_t key = 1u | (static_cast<uint64_t>(KT) << 11) | (static_cast<uint64_t>(RGN) << 28);
     const cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(KT), static_cast<cuuint64_t>(RGN)};
     const cuuint64_t strides[2] = {512u, static_cast<cuuint64_t>(KT) * 512u};
     const cuuint32_t box[3] = {64u, 1u, 8u};
-    const cuuint32_t estr[3] = {1u, 1u, 1u};
-    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<uint8_t *>(packed), dims, strides,
-                                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    return encode_locked(map, packed, key, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-template <int BN, int NSTG, int MINB>
-cudaError_t launch16_bn(const void *q16, const float *tok_scale, const uint8_t *packed, const float *gamma,
-                        int M, int N, int K, __nv_bfloat16 *out, int32_t *acc_out, cudaStream_t st,
-                        uint32_t wait_limit) {
-    const int KT = (K + 127) / 128;
-    const int RGN = (N + 15) / 16;
-    const uint32_t smem = Smem16<BN, NSTG>::kBytes;
-    static bool configured[64] = {false};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-        e = cudaFuncSetAttribute(gemm16_kernel<BN, NSTG, MINB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem));
+int device_sms(int dev) {
+    static int sms[64] = {0};
+    if (!sms[dev]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+        sms[dev] = v;
+    }
+    return sms[dev];
+}
+
+// One kernel family (a token tile, int8 or f16 activations): the plain
+// kernel, its split-K twin, their attributes (set once per device) and the
+// number of S-CTA clusters of the twin that fit on the GPU at once.
+template <typename Kern>
+struct Family {
+    Kern plain, split;
+    uint32_t smem;
+    bool configured[64] = {false};
+    int clusters[64][kMaxSplit + 1] = {};  // 0: not asked yet, -1: none fit
+
+    cudaError_t configure(int dev) {
+        if (configured[dev]) return cudaSuccess;
+        cudaError_t e = cudaFuncSetAttribute(plain, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(split, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(split, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
+        return cudaSuccess;
     }
-    CUtensorMap qmap, wmap;
-    e = make_qmap(&qmap, q16, M, K, BN, true);
-    if (e != cudaSuccess) return e;
-    e = make_wmap(&wmap, packed, RGN, KT);
-    if (e != cudaSuccess) return e;
-    const dim3 grid((RGN + 7) / 8, (M + BN - 1) / BN);
-    return launch_pdl(gemm16_kernel<BN, NSTG, MINB>, grid, dim3(kThreads), smem, st, 1, qmap, wmap, tok_scale, packed, gamma,
-                      M, N, K, KT, RGN, out, acc_out, wait_limit);
-}
+    int max_clusters(int dev, int S) {
+        if (!clusters[dev][S]) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(S, 1, 1);
+            cfg.blockDim = dim3(kThreads);
+            cfg.dynamicSmemBytes = smem;
+            cudaLaunchAttribute attr;
+            attr.id = cudaLaunchAttributeClusterDimension;
+            attr.val.clusterDim.x = S;
+            attr.val.clusterDim.y = 1;
+            attr.val.clusterDim.z = 1;
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, split, &cfg) != cudaSuccess || n <= 0) {
+                cudaGetLastError();  // a size that cannot be placed is not an error of the call
+                n = -1;
+            }
+            clusters[dev][S] = n;
+        }
+        return clusters[dev][S];
+    }
+    // CTAs per cluster along K: 1 where the tiles already occupy half the
+    // SMs, else the largest S whose clusters all fit in one wave with at
+    // least kMinSplitStages stages each.
+    int choose_split(int dev, int tiles, int NS) {
+        if (2 * tiles > device_sms(dev)) return 1;
+        int best = 1;
+        for (int S = 2; S <= kMaxSplit && NS >= S * kMinSplitStages; ++S)
+            if (max_clusters(dev, S) >= tiles) best = S;
+        return best;
+    }
+};
 
 template <int BN>
-cudaError_t launch_bn(const int8_t *q, const float *tok_scale, const uint8_t *packed,
-                      const float *gamma, int M, int N, int K, __nv_bfloat16 *out,
-                      int32_t *acc_out, cudaStream_t st, uint32_t wait_limit) {
+Family<decltype(&gemm_kernel<BN, false>)> &family8() {
+    static Family<decltype(&gemm_kernel<BN, false>)> f{gemm_kernel<BN, false>, gemm_kernel<BN, true>,
+                                                        Smem<BN>::kBytes};
+    return f;
+}
+template <int BN, int NSTG>
+Family<decltype(&gemm16_kernel<BN, NSTG, false>)> &family16() {
+    static Family<decltype(&gemm16_kernel<BN, NSTG, false>)> f{gemm16_kernel<BN, NSTG, false>,
+                                                                gemm16_kernel<BN, NSTG, true>, Smem16<BN, NSTG>::kBytes};
+    return f;
+}
+
+std::mutex g_family_mutex;
+
+// Plan and launch one GEMM of a family: grid (row tiles x S, token tiles),
+// clusters of S along x.
+template <typename Fam>
+cudaError_t launch_family(Fam &fam, int BN, const void *q, bool f16, const float *tok_scale, const uint8_t *packed,
+                          const float *gamma, int M, int N, int K, __nv_bfloat16 *out, int32_t *acc_out,
+                          cudaStream_t st, uint32_t wait_limit, int force_split) {
     const int KT = (K + 127) / 128;
     const int RGN = (N + 15) / 16;
-    const uint32_t smem = Smem<BN>::kBytes;
-    static bool configured[64] = {false};  // the attribute is set once per device
+    const int row_tiles = (RGN + 7) / 8, tok_tiles = (M + BN - 1) / BN;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-        e = cudaFuncSetAttribute(gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem));
+    int S;
+    {
+        std::lock_guard<std::mutex> lock(g_family_mutex);
+        e = fam.configure(dev);
         if (e != cudaSuccess) return e;
-        configured[dev] = true;
+        if (force_split > 0) {  // clamped to the stages there are and to a cluster size that fits
+            S = force_split < 2 * KT ? force_split : 2 * KT;
+            if (S > kMaxSplit) S = kMaxSplit;
+            while (S > 1 && fam.max_clusters(dev, S) <= 0) --S;
+        } else {
+            S = fam.choose_split(dev, row_tiles * tok_tiles, 2 * KT);
+        }
     }
     CUtensorMap qmap, wmap;
-    e = make_qmap(&qmap, q, M, K, BN, false);
+    e = make_qmap(&qmap, q, M, K, BN, f16);
     if (e != cudaSuccess) return e;
     e = make_wmap(&wmap, packed, RGN, KT);
     if (e != cudaSuccess) return e;
-    const dim3 grid((RGN + 7) / 8, (M + BN - 1) / BN);
-    return launch_pdl(gemm_kernel<BN>, grid, dim3(kThreads), smem, st, 1, qmap, wmap, tok_scale, packed, gamma,
-                      M, N, K, KT, RGN, out, acc_out, wait_limit);
+    const dim3 grid(row_tiles * S, tok_tiles);
+    if (S == 1)
+        return launch_pdl(fam.plain, grid, dim3(kThreads), fam.smem, st, 1, qmap, wmap, tok_scale, gamma, M, N, KT,
+                          RGN, out, acc_out, wait_limit);
+    return launch_pdl(fam.split, grid, dim3(kThreads), fam.smem, st, static_cast<unsigned>(S), qmap, wmap, tok_scale,
+                      gamma, M, N, KT, RGN, out, acc_out, wait_limit);
 }
 
 }  // namespace
 
-// Token tile (MMA N) of the f16 GEMM for M > 128, one CTA per SM holding a
-// 128-row x BN tile: 256, or 192 where that takes fewer whole waves.  A 64-k
-// stage costs about the same down to BN = 192 (its copies and weight
-// conversion set a floor), so a narrower tile pays only where the wave count
-// drops: e.g. N = 2560 (20 row tiles) at M = 4096 gives 320 tiles with
-// BN = 256 (2.2 waves, three paid) and 440 with BN = 192 (three full waves).
+// Token tile (MMA N) above 128 tokens, one CTA per SM holding a 128-row x
+// BN tile: 256, or 192 where that takes fewer whole waves.  A 64-k stage
+// costs about the same down to BN = 192 (its copies and weight conversion
+// set a floor), so a narrower tile pays only where the wave count drops:
+// e.g. N = 2560 (20 row tiles) at M = 4096 gives 320 tiles with BN = 256
+// (2.2 waves, three paid) and 440 with BN = 192 (three full waves).
 int token_tile(int M, int N) {
     int sms = 148, dev = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) sms = device_sms(dev);
     const int64_t row_tiles = (N + 127) / 128;
     auto cost = [&](int bn) {  // whole waves x a per-tile time with a large fixed part
         const int64_t tiles = row_tiles * ((M + bn - 1) / bn);
@@ -559,22 +784,37 @@ int token_tile(int M, int N) {
     return cost(192) < cost(256) ? 192 : 256;
 }
 
-cudaError_t launch_gemm16(const void *q16, const float *tok_scale, const uint8_t *packed,
-                          const float *gamma, int M, int N, int K, __nv_bfloat16 *out,
-                          int32_t *acc_out, cudaStream_t st, uint32_t wait_limit) {
-    if (M <= 64) return launch16_bn<64, 6, 1>(q16, tok_scale, packed, gamma, M, N, K, out, acc_out, st, wait_limit);
-    if (M <= 128) return launch16_bn<128, 6, 1>(q16, tok_scale, packed, gamma, M, N, K, out, acc_out, st, wait_limit);
+// `split`: CTAs per cluster along K, or 0 to let the planner choose.
+cudaError_t launch_gemm16(const void *q16, const float *tok_scale, const uint8_t *packed, const float *gamma, int M,
+                          int N, int K, __nv_bfloat16 *out, int32_t *acc_out, cudaStream_t st, uint32_t wait_limit,
+                          int split) {
+    if (M <= 64)
+        return launch_family(family16<64, 6>(), 64, q16, true, tok_scale, packed, gamma, M, N, K, out, acc_out, st,
+                             wait_limit, split);
+    if (M <= 128)
+        return launch_family(family16<128, 6>(), 128, q16, true, tok_scale, packed, gamma, M, N, K, out, acc_out, st,
+                             wait_limit, split);
     if (token_tile(M, N) == 192)
-        return launch16_bn<192, 6, 1>(q16, tok_scale, packed, gamma, M, N, K, out, acc_out, st, wait_limit);
-    return launch16_bn<256, 6, 1>(q16, tok_scale, packed, gamma, M, N, K, out, acc_out, st, wait_limit);
+        return launch_family(family16<192, 6>(), 192, q16, true, tok_scale, packed, gamma, M, N, K, out, acc_out, st,
+                             wait_limit, split);
+    return launch_family(family16<256, 6>(), 256, q16, true, tok_scale, packed, gamma, M, N, K, out, acc_out, st,
+                         wait_limit, split);
 }
 
-cudaError_t launch_gemm(const int8_t *q, const float *tok_scale, const uint8_t *packed,
-                        const float *gamma, int M, int N, int K, __nv_bfloat16 *out,
-                        int32_t *acc_out, cudaStream_t st, uint32_t wait_limit) {
-    if (M <= 64) return launch_bn<64>(q, tok_scale, packed, gamma, M, N, K, out, acc_out, st, wait_limit);
-    if (M <= 128) return launch_bn<128>(q, tok_scale, packed, gamma, M, N, K, out, acc_out, st, wait_limit);
-    return launch_bn<256>(q, tok_scale, packed, gamma, M, N, K, out, acc_out, st, wait_limit);
+cudaError_t launch_gemm(const int8_t *q, const float *tok_scale, const uint8_t *packed, const float *gamma, int M,
+                        int N, int K, __nv_bfloat16 *out, int32_t *acc_out, cudaStream_t st, uint32_t wait_limit,
+                        int split) {
+    if (M <= 64)
+        return launch_family(family8<64>(), 64, q, false, tok_scale, packed, gamma, M, N, K, out, acc_out, st,
+                             wait_limit, split);
+    if (M <= 128)
+        return launch_family(family8<128>(), 128, q, false, tok_scale, packed, gamma, M, N, K, out, acc_out, st,
+                             wait_limit, split);
+    if (token_tile(M, N) == 192)
+        return launch_family(family8<192>(), 192, q, false, tok_scale, packed, gamma, M, N, K, out, acc_out, st,
+                             wait_limit, split);
+    return launch_family(family8<256>(), 256, q, false, tok_scale, packed, gamma, M, N, K, out, acc_out, st,
+                         wait_limit, split);
 }
 
 // Device address of the status word, for kernels in other translation units.

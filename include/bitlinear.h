@@ -312,6 +312,24 @@ BITLINEAR_API bitlinear_status_t bitlinear_check_status(void *stream);
  */
 BITLINEAR_API void bitlinear_set_wait_limit(uint32_t iterations);
 
+/*
+ * Engine choice of bitlinear_forward and bitlinear_forward_f16 (tuning and
+ * testing; the defaults are measured choices, and every setting computes the
+ * same bits).
+ *   gemv_max_tokens: batches of up to this many tokens run bitlinear_forward
+ *     on the decode GEMV engine (16-token chunks of one launch), larger ones
+ *     on the tensor-core GEMM.  -1 restores the default; 0 sends every batch
+ *     to the GEMM; at most 64.
+ *   split_k: CTAs per cluster that share one GEMM output tile's k range
+ *     (their int32 partial tiles summed through distributed shared memory).
+ *     0 restores the default (the planner picks 1..16 from the tile count,
+ *     the SM count and K); 1..16 forces that value where K has at least that
+ *     many 64-k stages.
+ * Returns BITLINEAR_ERR_INVALID_ARG for a value out of range (nothing
+ * changes), else BITLINEAR_OK.  Settings are process-wide.
+ */
+BITLINEAR_API bitlinear_status_t bitlinear_set_engine(int32_t gemv_max_tokens, int32_t split_k);
+
 #ifdef __cplusplus
 }
 #endif

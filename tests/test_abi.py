@@ -152,3 +152,12 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(bl, "_HERE", str(tmp_path))
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         bl.load_library()
+
+
+def test_set_engine_validates_without_a_gpu(lib):
+    assert lib.bitlinear_set_engine(65, 0) == bl.ERR_INVALID_ARG   # the GEMV takes at most 64 tokens
+    assert lib.bitlinear_set_engine(-2, 0) == bl.ERR_INVALID_ARG
+    assert lib.bitlinear_set_engine(0, 17) == bl.ERR_INVALID_ARG   # clusters of at most 16 CTAs
+    assert lib.bitlinear_set_engine(0, -1) == bl.ERR_INVALID_ARG
+    assert lib.bitlinear_set_engine(0, 16) == bl.OK
+    assert lib.bitlinear_set_engine(-1, 0) == bl.OK                # the defaults again

@@ -330,24 +330,3 @@ def test_invalid_arguments_raise():
     out = torch.empty(2, 32, dtype=torch.bfloat16, device=DEV)
     with pytest.raises(bl.BitLinearError):
         bl.bitlinear_forward(q, s, packed, gamma, 2, 32, 60, out)
-
-
-def test_bounded_wait_timeout_is_reported_and_recovers():
-    N, K, M = 256, 1024, 65  # above the GEMV's 64 tokens: the GEMM, whose waits are bounded
-    w = inputs.weights_fp32(N, K, seed=9)
-    x = inputs.activations_bf16(M, K, seed=10)
-    assert bl.bitlinear_check_status() == bl.OK
-    packed, gamma = gpu_pack(w)
-    q, s = bl.quant_act(x.to(DEV))
-    try:
-        bl.bitlinear_set_wait_limit(1)
-        bl.forward(q, s, packed, gamma, N)
-        st = bl.bitlinear_check_status()
-    finally:
-        bl.bitlinear_set_wait_limit(0)
-    assert st == bl.ERR_TIMEOUT
-    # the context is still usable and results are right again
-    assert bl.bitlinear_check_status() == bl.OK
-    check_full(w, x)
-    assert bl.bitlinear_check_status() == bl.OK
-
