@@ -12,8 +12,8 @@
 // CTA tile: 128 weight rows (MMA M, TMEM lanes) x BN tokens (MMA N, TMEM
 // columns); k advances 64 per pipeline stage.  Roles:
 //   - loader (warp 9, one thread): per stage, a 2-D tensor-map copy of the
-//     activation tile (BN tokens x 64 k) and one 3-D tensor-map copy of the
-//     eight 512-byte packed weight tiles, into the stage's buffers;
+//     activation tile (BN tokens x 64 k) and one 5-D tensor-map copy of the
+//     stage's half of the eight packed weight tiles, into the stage's buffers;
 //   - converters (warps 0-7): the weight operand A lives in tensor memory:
 //     warps 0-3 / 4-7 each own 32 rows (their TMEM lane quarter), expand the
 //     row's 2-bit codes to f16 in registers and store them with tcgen05.st;
@@ -52,14 +52,17 @@ __device__ unsigned int g_gemm_status = 0u;
 
 namespace {
 
-constexpr int kRaw = 6;    // raw (packed weights + int8 activations) stages in flight
-constexpr int kOps = 3;    // operand stages (f16 activation tile + weight TMEM columns)
 constexpr int kConverters = 256;                // warps 0-7
 constexpr int kThreads = kConverters + 64;      // + MMA warp 8 + loader warp 9
 constexpr uint32_t kDrainLimit = 1u << 30;
-constexpr uint32_t kRawA = 8 * 512;             // packed codes of 8 row groups, one k-tile
+constexpr uint32_t kRawA = 8 * 256;             // packed codes of 8 row groups, one 64-k stage
 constexpr int kMaxSplit = 16;                   // CTAs of a cluster sharing one tile's k range
 constexpr int kMinSplitStages = 4;              // 64-k stages per CTA of a split, at least
+
+// Behind the stages: the mbarriers, then the control words, and at +512 the
+// epilogue's per-token factors gamma * s_tok (up to 256 floats).
+constexpr uint32_t kFactorOff = 512;
+constexpr uint32_t kCtlBytes = kFactorOff + 256 * 4;
 
 // Control words behind the mbarriers.
 struct Ctl {
@@ -68,30 +71,47 @@ struct Ctl {
     int abort;      // raised by the first wait that expires
 };
 
+// int8 activations: kRaw raw stages (packed weights + int8 tile, landed by
+// TMA) feed kOps operand stages (f16 B tile in shared memory + 32 weight
+// columns in TMEM).  A converted operand stage waits on a proxy fence and two
+// barrier hand-offs before its MMAs can run, so the operand ring is made as
+// deep as shared memory (227 KB) and TMEM (512 columns, the accumulator
+// first) allow for the token tile.
 template <int BN>
 struct Smem {
+    static constexpr int kOps = BN <= 64 ? 8 : BN <= 128 ? 6 : BN <= 192 ? 5 : 4;
+    static constexpr int kRaw = BN <= 64 ? 16 : BN <= 128 ? 7 : 5;
     static constexpr uint32_t kTileB = BN * 128;        // f16 tile, BN tokens x 64 k, swizzled
     static constexpr uint32_t kRawB = BN * 64;              // int8 tile, BN tokens x 64 k
     static constexpr uint32_t kRawStage = kRawA + kRawB;    // packed codes | int8 tile
     static constexpr uint32_t kRawBase = kOps * kTileB;     // operand tiles first: 1024-aligned
     static constexpr uint32_t kBarOff = kRawBase + kRaw * kRawStage;
-    static constexpr uint32_t kBytes = kBarOff + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr uint32_t kBytes = kBarOff + 1024 /*align*/ + kCtlBytes;
     // TMEM: accumulator in columns [0, BN), weight stages after it (32 columns each)
     static constexpr uint32_t kACol = BN;
     static constexpr uint32_t kCols = BN + 32 * kOps <= 256 ? 256 : 512;
+    static_assert(BN + 32 * kOps <= 512, "accumulator and weight stages fit in TMEM");
+    static_assert(kBytes <= 227 * 1024, "shared memory per CTA");
+    static_assert(8 * (2 * kRaw + 2 * kOps + 1) + sizeof(int) * 3 <= kFactorOff, "barriers and control words");
     static_assert(128u * BN * 4u <= kBarOff, "a split's int32 partial tile fits below the barriers");
+    static_assert(128u * BN * 6u <= kBarOff, "the staged bf16 and int32 output tiles fit below the barriers");
 };
 
-// f16 activations: stage = swizzled f16 tile | packed codes.
+// f16 activations: NSTG stages of swizzled f16 tile | packed codes (as deep
+// as shared memory and TMEM allow for the token tile).
 template <int BN, int NSTG>
 struct Smem16 {
     static constexpr uint32_t kTileB = BN * 128;
     static constexpr uint32_t kStage = kTileB + kRawA;  // multiple of 1024
     static constexpr uint32_t kBarOff = NSTG * kStage;
-    static constexpr uint32_t kBytes = kBarOff + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr uint32_t kBytes = kBarOff + 1024 /*align*/ + kCtlBytes;
     static constexpr uint32_t kACol = BN;
     static constexpr uint32_t kCols = BN + 32 * NSTG <= 128 ? 128 : (BN + 32 * NSTG <= 256 ? 256 : 512);
+    static_assert(BN + 32 * NSTG <= 512, "accumulator and weight stages fit in TMEM");
+    static_assert(kBytes <= 227 * 1024, "shared memory per CTA");
+    static_assert(8 * (3 * NSTG + 1) + sizeof(int) * 3 <= kFactorOff, "barriers and control words");
     static_assert(128u * BN * 4u <= kBarOff, "a split's int32 partial tile fits below the barriers");
+    static_assert(128u * BN * 6u <= kBarOff, "the staged bf16 and int32 output tiles fit below the barriers");
 };
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
@@ -106,17 +126,49 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
-// Packed weights of 8 row groups at one 128-k tile, by one tensor-map copy:
-// the packed buffer seen as u64 [row group][k-tile][64], box 64 x 1 x 8
-// (4 KB, row group major, so the 512-byte tiles land back to back).  One
-// copy instead of eight 512-byte bulk copies: the copy instructions, issued
-// by one loader thread, set the pace of the pipeline.
-__device__ __forceinline__ void tma_load_w8(void *dst, const CUtensorMap *map, int c, int rg0, uint64_t *bar) {
+// Shared -> global tensor-map store (bulk group), and its completion.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_addr(src)), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_and_wait() {
+    asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Packed weights of 8 row groups for one 64-k stage (half of a 128-k tile),
+// by one tensor-map copy.  A tile's lane chunk (g, t), 16 bytes at 64g + 16t,
+// holds rows g and g+8 at k 32t..32t+31 as words x y z w = (g, P0) (g+8, P0)
+// (g, P1) (g+8, P1).  The map lists the dimensions word, g, t, k-tile, row
+// group (g before t), so the box 4 x 8 x 2 x 1 x 8 over the stage's two t
+// lands as [row group][t'][g][word], 256 bytes per row group: a
+// converter lane reading word (hi + 2P) of (g, t') at 16g + 4(hi + 2P)
+// hits a bank of its own among the 16 rows of a row group.
+__device__ __forceinline__ void tma_load_w8(void *dst, const CUtensorMap *map, int half, int c, int rg0,
+                                            uint64_t *bar) {
     asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-        "[%5];" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(c), "r"(rg0), "r"(smem_addr(bar))
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+        "%5, %6}], [%7];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(2 * half), "r"(c), "r"(rg0), "r"(smem_addr(bar))
         : "memory");
+}
+
+// The two code words (P = 0, 1) of one weight row at one 64-k stage, from the
+// stage's packed codes: row `ri` (0..15) of row group `rgl`, k-half t2 (32 k).
+// Odd row groups read P = 1 first, so the 32 lanes of a warp (two row groups)
+// touch 32 distinct banks in each of the two loads.
+__device__ __forceinline__ void load_codes(const uint8_t *codes, int rgl, int ri, int t2, bool row_ok, uint32_t &w0,
+                                           uint32_t &w1) {
+    if (!row_ok) {
+        w0 = w1 = 0x55555555u;  // code 1: weight 0
+        return;
+    }
+    const uint32_t *base = reinterpret_cast<const uint32_t *>(codes + 256 * rgl + 128 * t2 + 16 * (ri & 7)) + (ri >> 3);
+    const int sw = rgl & 1;
+    const uint32_t a = base[2 * sw], b = base[2 * (sw ^ 1)];
+    w0 = sw ? b : a;
+    w1 = sw ? a : b;
 }
 
 // The 2-bit codes of one weight row at 32 k (two 16-k words of the row's
@@ -130,42 +182,99 @@ __device__ __forceinline__ void expand_codes(uint32_t w0, uint32_t w1, uint32_t 
     }
 }
 
-// One output element: bf16(acc * (gamma * s_tok)), both products rounded to
-// nearest in fp32.
-__device__ __forceinline__ __nv_bfloat16 rescale(int a, float gam, float ts) {
-    return __float2bfloat16_rn(__fmul_rn(static_cast<float>(a), __fmul_rn(gam, ts)));
+// Outputs from accumulator values: bf16(acc * f), f = gamma * s_tok rounded
+// to nearest in fp32 (once per token, into shared memory), the product
+// rounded likewise.  The fp32 accumulator holds the exact integer acc, so it
+// is multiplied as it is: float(int(v)) == v, and the conversions to and
+// from int32 (slow-pipe instructions, three per output with the bf16
+// rounding) reduce to one packed bf16 rounding per two outputs.
+__device__ __forceinline__ __nv_bfloat162 rescale2(float v0, float f0, float v1, float f1) {
+    return __floats2bfloat162_rn(__fmul_rn(v0, f0), __fmul_rn(v1, f1));
 }
 
 // The accumulator tile (TMEM lanes = 128 weight rows, columns = BN tokens)
-// to the outputs, by warps 0-7 (warp w: lane quarter w % 4, column half w / 4).
+// to the outputs, by warps 0-7 (warp w: lane quarter w % 4, column half w / 4),
+// two 16-column loads in flight at a time.
 template <int BN>
 __device__ __forceinline__ void store_tile(uint32_t tmem, int warp, int lane, int tile, int tok0, int M, int N,
-                                           float gam, const float *__restrict__ tok_scale,
-                                           __nv_bfloat16 *__restrict__ out, int32_t *__restrict__ acc_out) {
+                                           const float *s_f, __nv_bfloat16 *__restrict__ out,
+                                           int32_t *__restrict__ acc_out) {
+    static_assert((BN / 2) % 32 == 0, "column halves in steps of 32");
     const int lq = warp & 3, ch = warp >> 2;
     const int n = tile * 128 + 32 * lq + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * lq) << 16);
 #pragma unroll 1
-    for (int col = ch * (BN / 2); col < (ch + 1) * (BN / 2); col += 16) {
-        uint32_t v[16];
-        tc_ld16(tmem + (static_cast<uint32_t>(32 * lq) << 16) + col, v);
+    for (int col = ch * (BN / 2); col < (ch + 1) * (BN / 2); col += 32) {
+        uint32_t v[32];
+        tc_ld16(lane_base + col, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+        tc_ld16(lane_base + col + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
         tc_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int tk = tok0 + col + i;
-            if (tk < M && n < N) {
-                const int a = __float2int_rn(__uint_as_float(v[i]));
-                out[static_cast<int64_t>(tk) * N + n] = rescale(a, gam, tok_scale[tk]);
-                if (acc_out) acc_out[static_cast<int64_t>(tk) * N + n] = a;
+        for (int i = 0; i < 32; i += 2) {
+            const int c = col + i, tk = tok0 + c;
+            const __nv_bfloat162 o = rescale2(__uint_as_float(v[i]), s_f[c], __uint_as_float(v[i + 1]), s_f[c + 1]);
+            if (n < N) {
+                if (tk < M) {
+                    out[static_cast<int64_t>(tk) * N + n] = o.x;
+                    if (acc_out) acc_out[static_cast<int64_t>(tk) * N + n] = __float2int_rn(__uint_as_float(v[i]));
+                }
+                if (tk + 1 < M) {
+                    out[static_cast<int64_t>(tk + 1) * N + n] = o.y;
+                    if (acc_out)
+                        acc_out[static_cast<int64_t>(tk + 1) * N + n] = __float2int_rn(__uint_as_float(v[i + 1]));
+                }
             }
         }
     }
 }
 
-// Split K, step 1: this CTA's partial accumulator tile into its own shared
-// memory as int32 [BN tokens][128 rows] (exact: every partial is an integer
-// below 2^24).
+// The same through shared memory: warps 0-7 write the bf16 tile (and the
+// int32 tile if wanted) as [token][row], 256 (512) bytes per token, then one
+// thread stores each with a tensor-map copy, which also drops the rows and
+// tokens past N and M.  (Per-thread 2-byte stores of a thread's row across
+// tokens kept the store path busy for a third of a tile's time.)  The stage
+// buffers are free: every copy landed and every MMA that read them retired.
 template <int BN>
-__device__ __forceinline__ void stage_partial(uint32_t tmem, int warp, int lane, int32_t *red) {
+__device__ __forceinline__ void store_tile_staged(uint32_t tmem, int warp, int lane, int tile, int tok0,
+                                                  const float *s_f, uint8_t *smem, const CUtensorMap *omap,
+                                                  const CUtensorMap *amap) {
+    const int lq = warp & 3, ch = warp >> 2, r = 32 * lq + lane;
+    __nv_bfloat16 *ob = reinterpret_cast<__nv_bfloat16 *>(smem);
+    int32_t *oa = reinterpret_cast<int32_t *>(smem + BN * 256);
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * lq) << 16);
+#pragma unroll 1
+    for (int col = ch * (BN / 2); col < (ch + 1) * (BN / 2); col += 32) {
+        uint32_t v[32];
+        tc_ld16(lane_base + col, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+        tc_ld16(lane_base + col + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+        tc_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+            const int c = col + i;
+            const __nv_bfloat162 o = rescale2(__uint_as_float(v[i]), s_f[c], __uint_as_float(v[i + 1]), s_f[c + 1]);
+            ob[c * 128 + r] = o.x;
+            ob[(c + 1) * 128 + r] = o.y;
+            if (amap) {
+                oa[c * 128 + r] = __float2int_rn(__uint_as_float(v[i]));
+                oa[(c + 1) * 128 + r] = __float2int_rn(__uint_as_float(v[i + 1]));
+            }
+        }
+    }
+    fence_proxy_async_smem();
+    asm volatile("bar.sync 1, %0;" ::"r"(kConverters) : "memory");
+    if (warp == 0 && lane == 0) {
+        tma_store_2d(omap, ob, tile * 128, tok0);
+        if (amap) tma_store_2d(amap, oa, tile * 128, tok0);
+        bulk_commit_and_wait();
+    }
+}
+
+// Split K, step 1: this CTA's partial accumulator tile into its own shared
+// memory as fp32 [BN tokens][128 rows] (exact integers below 2^24, so any
+// sum of them below 2^24 - every partial and total of a K <= 65536 dot
+// product of ternary and int8 values - is exact in fp32, in any order).
+template <int BN>
+__device__ __forceinline__ void stage_partial(uint32_t tmem, int warp, int lane, uint32_t *red) {
     const int lq = warp & 3, ch = warp >> 2, row = 32 * lq + lane;
 #pragma unroll 1
     for (int col = ch * (BN / 2); col < (ch + 1) * (BN / 2); col += 16) {
@@ -173,7 +282,7 @@ __device__ __forceinline__ void stage_partial(uint32_t tmem, int warp, int lane,
         tc_ld16(tmem + (static_cast<uint32_t>(32 * lq) << 16) + col, v);
         tc_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) red[(col + i) * 128 + row] = __float2int_rn(__uint_as_float(v[i]));
+        for (int i = 0; i < 16; ++i) red[(col + i) * 128 + row] = v[i];
     }
 }
 
@@ -182,9 +291,9 @@ __device__ __forceinline__ void stage_partial(uint32_t tmem, int warp, int lane,
 // shared memory, and writes those outputs.  Each item is four consecutive
 // rows of one token column (a 16-byte read from every peer).
 template <int BN>
-__device__ __forceinline__ void reduce_partials(const int32_t *red, int split, int S, int tid, int tile, int tok0,
-                                                int M, int N, float gam, const float *__restrict__ tok_scale,
-                                                __nv_bfloat16 *__restrict__ out, int32_t *__restrict__ acc_out) {
+__device__ __forceinline__ void reduce_partials(const uint32_t *red, int split, int S, int tid, int tile, int tok0,
+                                                int M, int N, const float *s_f, __nv_bfloat16 *__restrict__ out,
+                                                int32_t *__restrict__ acc_out) {
     const int per = (BN + S - 1) / S;
     const int c0 = split * per, c1 = c0 + per < BN ? c0 + per : BN;
     const uint32_t base = smem_addr(red);
@@ -194,7 +303,7 @@ __device__ __forceinline__ void reduce_partials(const int32_t *red, int split, i
         const int tk = tok0 + col, n0 = tile * 128 + r4;
         if (tk >= M || n0 >= N) continue;
         const uint32_t off = base + static_cast<uint32_t>((col * 128 + r4) * 4);
-        int a[4] = {0, 0, 0, 0};
+        float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         for (int p0 = 0; p0 < S; p0 += 8) {
             int4 part[8];
 #pragma unroll
@@ -203,34 +312,47 @@ __device__ __forceinline__ void reduce_partials(const int32_t *red, int split, i
                                      : make_int4(0, 0, 0, 0);
 #pragma unroll
             for (int p = 0; p < 8; ++p) {
-                a[0] += part[p].x;
-                a[1] += part[p].y;
-                a[2] += part[p].z;
-                a[3] += part[p].w;
+                a[0] = __fadd_rn(a[0], __int_as_float(part[p].x));
+                a[1] = __fadd_rn(a[1], __int_as_float(part[p].y));
+                a[2] = __fadd_rn(a[2], __int_as_float(part[p].z));
+                a[3] = __fadd_rn(a[3], __int_as_float(part[p].w));
             }
         }
-        const float ts = tok_scale[tk];
+        const float f = s_f[col];
         const int64_t o = static_cast<int64_t>(tk) * N + n0;
+        const __nv_bfloat162 lo = rescale2(a[0], f, a[1], f), hi = rescale2(a[2], f, a[3], f);
         if (vec) {
-            __nv_bfloat162 lo, hi;
-            lo.x = rescale(a[0], gam, ts);
-            lo.y = rescale(a[1], gam, ts);
-            hi.x = rescale(a[2], gam, ts);
-            hi.y = rescale(a[3], gam, ts);
             uint2 pk;
-            pk.x = *reinterpret_cast<uint32_t *>(&lo);
-            pk.y = *reinterpret_cast<uint32_t *>(&hi);
+            pk.x = *reinterpret_cast<const uint32_t *>(&lo);
+            pk.y = *reinterpret_cast<const uint32_t *>(&hi);
             *reinterpret_cast<uint2 *>(out + o) = pk;
-            if (acc_out) *reinterpret_cast<int4 *>(acc_out + o) = make_int4(a[0], a[1], a[2], a[3]);
+            if (acc_out)
+                *reinterpret_cast<int4 *>(acc_out + o) =
+                    make_int4(__float2int_rn(a[0]), __float2int_rn(a[1]), __float2int_rn(a[2]), __float2int_rn(a[3]));
         } else {
+            const __nv_bfloat16 ob[4] = {lo.x, lo.y, hi.x, hi.y};
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 if (n0 + j < N) {
-                    out[o + j] = rescale(a[j], gam, ts);
-                    if (acc_out) acc_out[o + j] = a[j];
+                    out[o + j] = ob[j];
+                    if (acc_out) acc_out[o + j] = __float2int_rn(a[j]);
                 }
         }
     }
+}
+
+// Named barrier `id` over the first `threads` threads, returning the AND of
+// `pred` over them (the same value in every participant).
+__device__ __forceinline__ bool bar_and(uint32_t id, uint32_t threads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{.reg .pred p, q; setp.ne.u32 p, %3, 0;\n\t"
+        "barrier.red.and.pred q, %1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;}"
+        : "=r"(r)
+        : "r"(id), "r"(threads), "r"(static_cast<uint32_t>(pred))
+        : "memory");
+    return r != 0;
 }
 
 // The part every kernel ends with: the outputs (directly, or through the
@@ -238,30 +360,42 @@ __device__ __forceinline__ void reduce_partials(const int32_t *red, int split, i
 // issued copies and MMAs, free the tensor memory).  All threads call it.
 template <int BN, bool SPLIT>
 __device__ __forceinline__ void finish_tile(uint8_t *smem, uint32_t tmem, uint32_t cols, uint64_t *accum,
-                                            uint64_t *full, int nfull, const Ctl *ctl, volatile int *abort,
+                                            uint64_t *full, int nfull, const Ctl *ctl, float *s_f, volatile int *abort,
                                             bool timed_out, int split, int S, int tile, int M, int N,
                                             const float *__restrict__ tok_scale, const float *__restrict__ gamma,
                                             __nv_bfloat16 *__restrict__ out, int32_t *__restrict__ acc_out,
-                                            uint32_t wait_limit) {
+                                            const CUtensorMap *omap, const CUtensorMap *amap, uint32_t wait_limit) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tok0 = blockIdx.y * BN;
     if (warp < 8) {
-        const bool have = mbar_wait_abortable_warp(accum, 0, wait_limit, abort);
+        // The tile's token factors, while the last MMAs run (the scales come
+        // from an earlier kernel: wait for it, which has long completed).
+        pdl_wait();
+        const float gam = *gamma;
+        for (int c = tid; c < BN; c += kConverters)
+            s_f[c] = tok0 + c < M ? __fmul_rn(gam, tok_scale[tok0 + c]) : 0.0f;
+        asm volatile("bar.sync 1, %0;" ::"r"(kConverters) : "memory");  // warps 0-7
+        // The same outcome in all eight warps (the staged store below has a
+        // barrier of its own that all of them, or none, must reach).
+        bool have = mbar_wait_abortable_warp(accum, 0, wait_limit, abort);
+        have = bar_and(1, kConverters, have);
         if (!have) timed_out = true;
         tc_fence_after();
         if (have) {
             if constexpr (SPLIT)
-                stage_partial<BN>(tmem, warp, lane, reinterpret_cast<int32_t *>(smem));
+                stage_partial<BN>(tmem, warp, lane, reinterpret_cast<uint32_t *>(smem));
+            else if (omap)
+                store_tile_staged<BN>(tmem, warp, lane, tile, tok0, s_f, smem, omap, acc_out ? amap : nullptr);
             else
-                store_tile<BN>(tmem, warp, lane, tile, tok0, M, N, *gamma, tok_scale, out, acc_out);
+                store_tile<BN>(tmem, warp, lane, tile, tok0, M, N, s_f, out, acc_out);
         }
     }
     if constexpr (SPLIT) {
         __syncwarp();
         cluster_sync();  // every CTA's partial tile is in its shared memory
         if (warp < 8)
-            reduce_partials<BN>(reinterpret_cast<const int32_t *>(smem), split, S, tid, tile, tok0, M, N, *gamma,
-                                tok_scale, out, acc_out);
+            reduce_partials<BN>(reinterpret_cast<const uint32_t *>(smem), split, S, tid, tile, tok0, M, N, s_f, out,
+                                acc_out);
         __syncwarp();
         cluster_sync();  // the peers have read this CTA's partials
     }
@@ -295,9 +429,11 @@ __device__ __forceinline__ void split_range(int NS, int split, int S, int &st0, 
 template <int BN, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap wmap,
+                const __grid_constant__ CUtensorMap omap, const __grid_constant__ CUtensorMap amap, int staged,
                 const float *__restrict__ tok_scale, const float *__restrict__ gamma, int M, int N, int KT,
                 int RGN, __nv_bfloat16 *__restrict__ out, int32_t *__restrict__ acc_out, uint32_t wait_limit) {
     using L = Smem<BN>;
+    constexpr int kRaw = L::kRaw, kOps = L::kOps;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
@@ -356,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 uint8_t *raw = smem + L::kRawBase + rs * L::kRawStage;
                 mbar_arrive_expect_tx(&raw_full[rs], bytes);
-                tma_load_w8(raw, &wmap, st >> 1, rg0, &raw_full[rs]);
+                tma_load_w8(raw, &wmap, st & 1, st >> 1, rg0, &raw_full[rs]);
                 if (!waited) {
                     pdl_wait();
                     waited = true;
@@ -372,10 +508,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = 32 * (warp & 3) + lane;
         const int ri = row & 15, rgl = row >> 4, t2 = warp >> 2;
         const bool row_ok = rgl < nrg;
-        const uint32_t a_off = 512 * rgl + 16 * 4 * (ri & 7) + 4 * (ri >> 3);
         const uint32_t a_lane = static_cast<uint32_t>(32 * (warp & 3)) << 16;
         for (int j = 0; j < ns; ++j) {
-            const int st = st0 + j, rs = j % kRaw, slot = j % kOps;
+            const int rs = j % kRaw, slot = j % kOps;
             if (!mbar_wait_abortable_warp(&raw_full[rs], (j / kRaw) & 1, wait_limit, abort) ||
                 !mbar_wait_abortable_warp(&op_empty[slot], ((j / kOps) & 1) ^ 1, wait_limit, abort)) {
                 timed_out = true;
@@ -385,9 +520,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t *stage = smem + slot * L::kTileB;
             {
                 // column c of the stage holds k = 2c, 2c+1: word (t' = c/16, P = (c%16)/8), pair p = c%8
-                const uint32_t *wp = reinterpret_cast<const uint32_t *>(raw + a_off + 16 * (2 * (st & 1) + t2));
-                uint32_t f[16];
-                expand_codes(row_ok ? wp[0] : 0x55555555u, row_ok ? wp[2] : 0x55555555u, f);
+                uint32_t w0, w1, f[16];
+                load_codes(raw, rgl, ri, t2, row_ok, w0, w1);
+                expand_codes(w0, w1, f);
                 tc_st16(tmem + a_lane + L::kACol + 32 * slot + 16 * t2, f);
             }
             // int8 tile (token-major, 64 bytes per token) -> swizzled f16 tile
@@ -439,8 +574,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     }
 
-    finish_tile<BN, SPLIT>(smem, tmem, L::kCols, accum, raw_full, kRaw, ctl, abort, timed_out, split, S, tile, M,
-                           N, tok_scale, gamma, out, acc_out, wait_limit);
+    finish_tile<BN, SPLIT>(smem, tmem, L::kCols, accum, raw_full, kRaw, ctl,
+                           reinterpret_cast<float *>(smem + L::kBarOff + kFactorOff), abort, timed_out, split, S, tile, M,
+                           N, tok_scale, gamma, out, acc_out, staged ? &omap : nullptr, &amap, wait_limit);
 }
 
 // ---------------------------------------------------------------------------
@@ -452,6 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int BN, int NSTG, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm16_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap wmap,
+                const __grid_constant__ CUtensorMap omap, const __grid_constant__ CUtensorMap amap, int staged,
                   const float *__restrict__ tok_scale, const float *__restrict__ gamma, int M, int N, int KT,
                   int RGN, __nv_bfloat16 *__restrict__ out, int32_t *__restrict__ acc_out, uint32_t wait_limit) {
     using L = Smem16<BN, NSTG>;
@@ -506,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 uint8_t *stage = smem + s * L::kStage;
                 mbar_arrive_expect_tx(&full[s], bytes);
-                tma_load_w8(stage + L::kTileB, &wmap, st >> 1, rg0, &full[s]);
+                tma_load_w8(stage + L::kTileB, &wmap, st & 1, st >> 1, rg0, &full[s]);
                 if (!waited) {  // the weights are static; the activations come from earlier kernels
                     pdl_wait();
                     waited = true;
@@ -523,10 +660,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = 32 * (warp & 3) + lane;
         const int ri = row & 15, rgl = row >> 4;
         const bool row_ok = rgl < nrg;
-        const uint32_t a_off = 512 * rgl + 16 * 4 * (ri & 7) + 4 * (ri >> 3);
         const uint32_t a_lane = static_cast<uint32_t>(32 * (warp & 3)) << 16;
         for (int j = warp >> 2; j < ns; j += 2) {
-            const int st = st0 + j, s = j % NSTG;
+            const int s = j % NSTG;
             if (!mbar_wait_abortable_warp(&full[s], (j / NSTG) & 1, wait_limit, abort)) {
                 timed_out = true;
                 break;
@@ -534,9 +670,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint8_t *codes = smem + s * L::kStage + L::kTileB;
 #pragma unroll
             for (int t2 = 0; t2 < 2; ++t2) {  // two 16-column halves (fewer live registers)
-                const uint32_t *wp = reinterpret_cast<const uint32_t *>(codes + a_off + 16 * (2 * (st & 1) + t2));
-                uint32_t f[16];
-                expand_codes(row_ok ? wp[0] : 0x55555555u, row_ok ? wp[2] : 0x55555555u, f);
+                uint32_t w0, w1, f[16];
+                load_codes(codes, rgl, ri, t2, row_ok, w0, w1);
+                expand_codes(w0, w1, f);
                 tc_st16(tmem + a_lane + L::kACol + 32 * s + 16 * t2, f);
             }
             tc_wait_st();
@@ -569,8 +705,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     }
 
-    finish_tile<BN, SPLIT>(smem, tmem, L::kCols, accum, full, NSTG, ctl, abort, timed_out, split, S, tile, M, N,
-                           tok_scale, gamma, out, acc_out, wait_limit);
+    finish_tile<BN, SPLIT>(smem, tmem, L::kCols, accum, full, NSTG, ctl,
+                           reinterpret_cast<float *>(smem + L::kBarOff + kFactorOff), abort, timed_out, split, S, tile, M, N,
+                           tok_scale, gamma, out, acc_out, staged ? &omap : nullptr, &amap, wait_limit);
 }
 
 // ------------------------------------------------------------------ host ---
@@ -581,9 +718,18 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 // Tensor maps already encoded, keyed by address and shape: a map holds
 // nothing but those, so a cached one is valid for any buffer at that
 // address with that shape.
-struct MapEntry {
+struct MapKey {
     const void *ptr;
-    uint64_t key;
+    int kind;      // 0 activations, 1 weights, 2 outputs
+    int variant;   // activations: f16; outputs: int32
+    int box;       // token tile
+    int64_t a, b;  // the tensor's two extents
+    bool operator==(const MapKey &o) const {
+        return ptr == o.ptr && kind == o.kind && variant == o.variant && box == o.box && a == o.a && b == o.b;
+    }
+};
+struct MapEntry {
+    MapKey key;
     bool used;
     CUtensorMap map;
 };
@@ -593,11 +739,12 @@ int g_map_next = 0;
 
 // Encode a tiled tensor map through the driver (its entry point looked up
 // once), or copy it from the cache.  Caller holds g_encode_mutex.
-cudaError_t encode_locked(CUtensorMap *map, const void *ptr, uint64_t key, CUtensorMapDataType type, uint32_t rank,
+cudaError_t encode_locked(CUtensorMap *map, const MapKey &key, CUtensorMapDataType type, uint32_t rank,
                           const cuuint64_t *dims, const cuuint64_t *strides, const cuuint32_t *box,
                           CUtensorMapSwizzle swz) {
+    const void *ptr = key.ptr;
     for (int i = 0; i < kMapCache; ++i)
-        if (g_maps[i].used && g_maps[i].ptr == ptr && g_maps[i].key == key) {
+        if (g_maps[i].used && g_maps[i].key == key) {
             *map = g_maps[i].map;
             return cudaSuccess;
         }
@@ -608,14 +755,13 @@ cudaError_t encode_locked(CUtensorMap *map, const void *ptr, uint64_t key, CUten
         if (e != cudaSuccess || qr != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
         g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
-    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    const cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
     const CUresult r = g_encode(map, type, rank, const_cast<void *>(ptr), dims, strides, box, estr,
                                 CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     MapEntry &slot = g_maps[g_map_next];
     g_map_next = (g_map_next + 1) % kMapCache;
-    slot.ptr = ptr;
     slot.key = key;
     slot.map = *map;
     slot.used = true;
@@ -626,25 +772,38 @@ cudaError_t encode_locked(CUtensorMap *map, const void *ptr, uint64_t key, CUten
 // swizzle): boxes of 64 k x BN tokens.
 cudaError_t make_qmap(CUtensorMap *map, const void *q, int M, int K, int BN, bool f16) {
     std::lock_guard<std::mutex> lock(g_encode_mutex);
-    const uint64_t key = 0u | (static_cast<uint64_t>(f16) << 1) | (static_cast<uint64_t>(BN) << 2) |
-                         (static_cast<uint64_t>(K) << 11) | (static_cast<uint64_t>(M) << 28);
+    const MapKey key{q, 0, f16 ? 1 : 0, BN, M, K};
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * (f16 ? 2u : 1u)};
     const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(BN)};
-    return encode_locked(map, q, key, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dims,
+    return encode_locked(map, key, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dims,
                          strides, box, f16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-// Packed weights (layout of bitlinear_packed_bytes) as u64 [RGN][KT][64],
-// boxes of 64 x 1 x 8.
+// Packed weights (layout of bitlinear_packed_bytes: in a tile, lane chunk
+// (g, t) at 64g + 16t) with the dimensions listed as word (4 B), g (64 B),
+// t (16 B), k-tile, row group: boxes of 4 x 8 x 2 x 1 x 8 (one 64-k stage of
+// 8 row groups) land as [row group][t'][g][word].
 cudaError_t make_wmap(CUtensorMap *map, const uint8_t *packed, int RGN, int KT) {
     std::lock_guard<std::mutex> lock(g_encode_mutex);
-    const uint64_t key = 1u | (static_cast<uint64_t>(KT) << 11) | (static_cast<uint64_t>(RGN) << 28);
-    const cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(KT), static_cast<cuuint64_t>(RGN)};
-    const cuuint64_t strides[2] = {512u, static_cast<cuuint64_t>(KT) * 512u};
-    const cuuint32_t box[3] = {64u, 1u, 8u};
-    return encode_locked(map, packed, key, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, dims, strides, box,
+    const MapKey key{packed, 1, 0, 0, RGN, KT};
+    const cuuint64_t dims[5] = {4u, 8u, 4u, static_cast<cuuint64_t>(KT), static_cast<cuuint64_t>(RGN)};
+    const cuuint64_t strides[4] = {64u, 16u, 512u, static_cast<cuuint64_t>(KT) * 512u};
+    const cuuint32_t box[5] = {4u, 8u, 2u, 1u, 8u};
+    return encode_locked(map, key, CU_TENSOR_MAP_DATA_TYPE_UINT32, 5, dims, strides, box,
                          CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// Outputs [M, N] row-major (bf16 or int32): boxes of 128 rows (n) x BN
+// tokens, for the staged epilogue's tensor-map stores.
+cudaError_t make_omap(CUtensorMap *map, const void *o, int M, int N, int BN, bool i32) {
+    std::lock_guard<std::mutex> lock(g_encode_mutex);
+    const MapKey key{o, 2, i32 ? 1 : 0, BN, M, N};
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * (i32 ? 4u : 2u)};
+    const cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(BN)};
+    return encode_locked(map, key, i32 ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims,
+                         strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 int device_sms(int dev) {
@@ -757,12 +916,21 @@ cudaError_t launch_family(Fam &fam, int BN, const void *q, bool f16, const float
     if (e != cudaSuccess) return e;
     e = make_wmap(&wmap, packed, RGN, KT);
     if (e != cudaSuccess) return e;
+    // Tensor-map stores of the output tiles need rows of a multiple of 16
+    // bytes (N % 8 for bf16); otherwise each thread stores its own elements.
+    CUtensorMap omap = {}, amap = {};
+    const int staged = S == 1 && (N % 8) == 0;
+    if (staged) {
+        e = make_omap(&omap, out, M, N, BN, false);
+        if (e == cudaSuccess && acc_out) e = make_omap(&amap, acc_out, M, N, BN, true);
+        if (e != cudaSuccess) return e;
+    }
     const dim3 grid(row_tiles * S, tok_tiles);
     if (S == 1)
-        return launch_pdl(fam.plain, grid, dim3(kThreads), fam.smem, st, 1, qmap, wmap, tok_scale, gamma, M, N, KT,
-                          RGN, out, acc_out, wait_limit);
-    return launch_pdl(fam.split, grid, dim3(kThreads), fam.smem, st, static_cast<unsigned>(S), qmap, wmap, tok_scale,
-                      gamma, M, N, KT, RGN, out, acc_out, wait_limit);
+        return launch_pdl(fam.plain, grid, dim3(kThreads), fam.smem, st, 1, qmap, wmap, omap, amap, staged, tok_scale,
+                          gamma, M, N, KT, RGN, out, acc_out, wait_limit);
+    return launch_pdl(fam.split, grid, dim3(kThreads), fam.smem, st, static_cast<unsigned>(S), qmap, wmap, omap, amap,
+                      staged, tok_scale, gamma, M, N, KT, RGN, out, acc_out, wait_limit);
 }
 
 }  // namespace
@@ -789,10 +957,10 @@ cudaError_t launch_gemm16(const void *q16, const float *tok_scale, const uint8_t
                           int N, int K, __nv_bfloat16 *out, int32_t *acc_out, cudaStream_t st, uint32_t wait_limit,
                           int split) {
     if (M <= 64)
-        return launch_family(family16<64, 6>(), 64, q16, true, tok_scale, packed, gamma, M, N, K, out, acc_out, st,
+        return launch_family(family16<64, 10>(), 64, q16, true, tok_scale, packed, gamma, M, N, K, out, acc_out, st,
                              wait_limit, split);
     if (M <= 128)
-        return launch_family(family16<128, 6>(), 128, q16, true, tok_scale, packed, gamma, M, N, K, out, acc_out, st,
+        return launch_family(family16<128, 8>(), 128, q16, true, tok_scale, packed, gamma, M, N, K, out, acc_out, st,
                              wait_limit, split);
     if (token_tile(M, N) == 192)
         return launch_family(family16<192, 6>(), 192, q16, true, tok_scale, packed, gamma, M, N, K, out, acc_out, st,
