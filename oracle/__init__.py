@@ -6,8 +6,9 @@ shares no code with the CUDA path: it is a plain C restatement of the
 method's definitions (``bitlinear_oracle.c``) behind a ctypes wrapper.
 
 Pages cited by the C source: the asi.tokyo "BitNet B1.58 2B4T" write-up, the
-cheatsheet.md BitNet b1.58 summary (section "BitNet b1.58とは？") and the
-lumen-it.ai BitNet article.
+cheatsheet.md BitNet b1.58 summary (section "BitNet b1.58とは？"), the
+lumen-it.ai BitNet article, and the vi.news.hada.io topic 20406 comments on
+ternary packing (five ternary digits per byte).
 """
 from __future__ import annotations
 
@@ -67,6 +68,25 @@ def lib():
         L.bl_oracle_threads.restype = ctypes.c_int
         L.bl_oracle_set_threads.argtypes = [ctypes.c_int]
         L.bl_oracle_set_threads.restype = None
+        L.bl_oracle_packed5_bytes.argtypes = [I64, I64]
+        L.bl_oracle_packed5_bytes.restype = I64
+        L.bl_oracle_position5.argtypes = [I64, I64, I64, ctypes.POINTER(I64), ctypes.POINTER(ctypes.c_int)]
+        L.bl_oracle_encode5.argtypes = [P]
+        L.bl_oracle_encode5.restype = ctypes.c_uint8
+        L.bl_oracle_decode5.argtypes = [ctypes.c_uint8, P]
+        L.bl_oracle_decode5.restype = ctypes.c_int
+        L.bl_oracle_pack5.argtypes = [P, I64, I64, P]
+        L.bl_oracle_unpack5.argtypes = [P, I64, I64, P]
+        L.bl_oracle_unpack5.restype = I64
+        L.bl_oracle_beta.argtypes = [P, I64, I64, I64, P]
+        L.bl_oracle_binarize.argtypes = [P, I64, P]
+        L.bl_oracle_packed1_bytes.argtypes = [I64, I64]
+        L.bl_oracle_packed1_bytes.restype = I64
+        L.bl_oracle_position1.argtypes = [I64, I64, I64, ctypes.POINTER(I64), ctypes.POINTER(ctypes.c_int)]
+        L.bl_oracle_pack1.argtypes = [P, I64, I64, P]
+        L.bl_oracle_unpack1.argtypes = [P, I64, I64, P]
+        L.bl_oracle_unpack1.restype = I64
+        L.bl_oracle_epilogue_groups.argtypes = [P, P, P, I64, I64, I64, P]
         _lib = L
     return _lib
 
@@ -201,4 +221,101 @@ def ternary_hash(word: int, K: int, n0: int, n1: int) -> np.ndarray:
     the synthetic weights of the stacked workloads, from SplitMix64."""
     out = np.empty((n1 - n0, K), dtype=np.int8)
     lib().bl_oracle_ternary_hash(ctypes.c_uint64(word & (2**64 - 1)), K, n0, n1, _ptr(out))
+    return out
+
+
+# ----------------------------------------------- five digits per byte ---
+
+def packed5_bytes(N: int, K: int) -> int:
+    return int(lib().bl_oracle_packed5_bytes(N, K))
+
+
+def position5(n: int, k: int, K: int) -> tuple[int, int]:
+    b = ctypes.c_int64()
+    d = ctypes.c_int()
+    lib().bl_oracle_position5(n, k, K, ctypes.byref(b), ctypes.byref(d))
+    return b.value, d.value
+
+
+def encode5(digits) -> int:
+    e = np.ascontiguousarray(digits, dtype=np.int32)
+    assert e.shape == (5,)
+    return int(lib().bl_oracle_encode5(_ptr(e)))
+
+
+def decode5(b: int):
+    """The five digits of byte b, or None if b encodes nothing."""
+    e = np.zeros(5, dtype=np.int32)
+    return e if lib().bl_oracle_decode5(ctypes.c_uint8(b), _ptr(e)) else None
+
+
+def pack5(wq: np.ndarray) -> np.ndarray:
+    wq = np.ascontiguousarray(wq, dtype=np.int8)
+    N, K = wq.shape
+    out = np.empty(packed5_bytes(N, K), dtype=np.uint8)
+    lib().bl_oracle_pack5(_ptr(wq), N, K, _ptr(out))
+    return out
+
+
+def unpack5(packed: np.ndarray, N: int, K: int) -> tuple[np.ndarray, int]:
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    assert packed.size == packed5_bytes(N, K)
+    wq = np.empty((N, K), dtype=np.int8)
+    bad = int(lib().bl_oracle_unpack5(_ptr(packed), N, K, _ptr(wq)))
+    return wq, bad
+
+
+# ------------------------------------------------ original binary BitNet ---
+
+def beta(w: np.ndarray, G: int) -> np.ndarray:
+    """Mean |W| of each of G equal blocks of consecutive rows (float32 [G])."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    N, K = w.shape
+    assert N % G == 0
+    out = np.empty(G, dtype=np.float32)
+    lib().bl_oracle_beta(_ptr(w), N, K, G, _ptr(out))
+    return out
+
+
+def binarize(w: np.ndarray) -> np.ndarray:
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    out = np.empty(w.shape, dtype=np.int8)
+    lib().bl_oracle_binarize(_ptr(w), w.size, _ptr(out))
+    return out
+
+
+def packed1_bytes(N: int, K: int) -> int:
+    return int(lib().bl_oracle_packed1_bytes(N, K))
+
+
+def position1(n: int, k: int, K: int) -> tuple[int, int]:
+    b = ctypes.c_int64()
+    s = ctypes.c_int()
+    lib().bl_oracle_position1(n, k, K, ctypes.byref(b), ctypes.byref(s))
+    return b.value, s.value
+
+
+def pack1(wb: np.ndarray) -> np.ndarray:
+    wb = np.ascontiguousarray(wb, dtype=np.int8)
+    N, K = wb.shape
+    out = np.empty(packed1_bytes(N, K), dtype=np.uint8)
+    lib().bl_oracle_pack1(_ptr(wb), N, K, _ptr(out))
+    return out
+
+
+def unpack1(packed: np.ndarray, N: int, K: int) -> tuple[np.ndarray, int]:
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    assert packed.size == packed1_bytes(N, K)
+    wb = np.empty((N, K), dtype=np.int8)
+    bad = int(lib().bl_oracle_unpack1(_ptr(packed), N, K, _ptr(wb)))
+    return wb, bad
+
+
+def epilogue_groups(acc: np.ndarray, s_tok: np.ndarray, beta_g: np.ndarray) -> np.ndarray:
+    acc = np.ascontiguousarray(acc, dtype=np.int32)
+    s_tok = np.ascontiguousarray(s_tok, dtype=np.float32)
+    beta_g = np.ascontiguousarray(beta_g, dtype=np.float32)
+    M, N = acc.shape
+    out = np.empty((M, N), dtype=np.uint16)
+    lib().bl_oracle_epilogue_groups(_ptr(acc), _ptr(s_tok), _ptr(beta_g), beta_g.size, M, N, _ptr(out))
     return out

@@ -12,6 +12,8 @@
  *   [P1] asi.tokyo, "BitNet B1.58 2B4T" write-up (2025-04-27)
  *   [P2] cheatsheet.md, "1ビットLarge Language Models時代：マイクロソフトがBitNet b1.58を紹介"
  *   [P3] lumen-it.ai, BitNet (original 1-bit BitNet) article
+ *   [P4] vi.news.hada.io topic 20406 (and its Portuguese twin), comments
+ *        on ternary packing: five ternary digits per byte, 3^5 = 243 <= 256
  *
  * Build: gcc -O2 -std=c11 -fPIC -shared -ffp-contract=off -fopenmp
  * (no -ffast-math: every float operation below must be one IEEE-754
@@ -356,5 +358,199 @@ void bl_oracle_ternary_hash(uint64_t word, int64_t K, int64_t n0, int64_t n1, in
             const uint64_t i = (uint64_t)n * (uint64_t)K + (uint64_t)k;
             const uint64_t v = splitmix_mix(s + (i + 1u) * 0x9E3779B97F4A7C15ull);
             out[(n - n0) * K + k] = (int8_t)((int)(((v >> 32) * 3u) >> 32) - 1);
+        }
+}
+
+/* ------------------------------------------------------------------ */
+/* Variant layout: five ternary digits per byte (1.6 bit per weight).   */
+/* [P4], the Hacker News comments: five ternary digits fit one byte     */
+/* because 3^5 = 243 <= 256, so b1.58 weights need log2(3) = 1.58 bits  */
+/* rather than 2.  The pages give no digit order or byte encoding;     */
+/* this reading: digits e = Wq + 1, most significant first,             */
+/*   v = e0*81 + e1*27 + e2*9 + e3*3 + e4      (0 <= v <= 242)          */
+/* and the byte holds v as a base-3 fraction scaled to 256,             */
+/*   b = ceil(256 * v / 243),                                           */
+/* the fixed-point form of the ternary-packing write-up the comment     */
+/* links (its digits come back by repeated multiplication by 3).        */
+/* Decoding here is plain arithmetic: v = floor(243 * b / 256), then   */
+/* base-3 digits of v.                                                  */
+/*                                                                      */
+/* Layout (tiles of 16 rows x 160 k, 512 bytes each):                   */
+/*   Np = 16*ceil(N/16), K5 = 160*ceil(K/160), KT5 = K5/160             */
+/*   r = n/16, i = n%16, c = k/160, kk = k%160                          */
+/*   g = i%8, u = i/8, t = kk/40, j = (kk%40)/5, d = kk%5               */
+/*   byte = 512*(r*KT5 + c) + 16*(4g + t) + 8u + j, digit d of it       */
+/* so lane 4g+t's 16 bytes hold rows g (bytes 0-7) and g+8 (8-15) over  */
+/* k in [40t, 40t+40), five consecutive k per byte.  Padding positions  */
+/* (n >= N or k >= K) hold digit 1 (weight 0).                          */
+/* ------------------------------------------------------------------ */
+int64_t bl_oracle_packed5_bytes(int64_t N, int64_t K) {
+    int64_t Np = (N + 15) / 16 * 16;
+    int64_t K5 = (K + 159) / 160 * 160;
+    return Np * K5 / 5;
+}
+
+static void position5(int64_t n, int64_t k, int64_t KT5, int64_t *byte, int *digit) {
+    int64_t r = n / 16, c = k / 160;
+    int i = (int)(n % 16), kk = (int)(k % 160);
+    int g = i % 8, u = i / 8, t = kk / 40, j = (kk % 40) / 5;
+    *byte = 512 * (r * KT5 + c) + 16 * (4 * g + t) + 8 * u + j;
+    *digit = kk % 5;
+}
+
+/* Byte offset and digit index (0 = most significant) of weight (n, k). */
+void bl_oracle_position5(int64_t n, int64_t k, int64_t K, int64_t *byte, int *digit) {
+    position5(n, k, (K + 159) / 160, byte, digit);
+}
+
+/* One byte from its five digits (each 0, 1 or 2). */
+uint8_t bl_oracle_encode5(const int *e) {
+    int v = 0;
+    for (int d = 0; d < 5; ++d) v = 3 * v + e[d];
+    return (uint8_t)((256 * v + 242) / 243);
+}
+
+/* The five digits of a byte; returns 0 if the byte is not an encoding. */
+int bl_oracle_decode5(uint8_t b, int *e) {
+    int v = (243 * (int)b) / 256;
+    if ((256 * v + 242) / 243 != (int)b) return 0;
+    for (int d = 4; d >= 0; --d) {
+        e[d] = v % 3;
+        v /= 3;
+    }
+    return 1;
+}
+
+void bl_oracle_pack5(const int8_t *wq, int64_t N, int64_t K, uint8_t *packed) {
+    int64_t Np = (N + 15) / 16 * 16, K5 = (K + 159) / 160 * 160, KT5 = K5 / 160;
+    for (int64_t n = 0; n < Np; ++n)
+        for (int64_t k0 = 0; k0 < K5; k0 += 5) {
+            int e[5];
+            for (int d = 0; d < 5; ++d) {
+                int64_t k = k0 + d;
+                e[d] = (n < N && k < K) ? wq[n * K + k] + 1 : 1;
+            }
+            int64_t byte; int digit;
+            position5(n, k0, KT5, &byte, &digit);
+            packed[byte] = bl_oracle_encode5(e);
+        }
+}
+
+/* Inverse of bl_oracle_pack5.  Returns the number of bytes that are not
+ * encodings plus the number of padding digits that are not 1. */
+int64_t bl_oracle_unpack5(const uint8_t *packed, int64_t N, int64_t K, int8_t *wq) {
+    int64_t Np = (N + 15) / 16 * 16, K5 = (K + 159) / 160 * 160, KT5 = K5 / 160;
+    int64_t bad = 0;
+    for (int64_t n = 0; n < Np; ++n)
+        for (int64_t k0 = 0; k0 < K5; k0 += 5) {
+            int64_t byte; int digit;
+            position5(n, k0, KT5, &byte, &digit);
+            int e[5];
+            if (!bl_oracle_decode5(packed[byte], e)) { ++bad; continue; }
+            for (int d = 0; d < 5; ++d) {
+                int64_t k = k0 + d;
+                if (n < N && k < K) wq[n * K + k] = (int8_t)(e[d] - 1);
+                else if (e[d] != 1) ++bad;
+            }
+        }
+    return bad;
+}
+
+/* ------------------------------------------------------------------ */
+/* Variant: the original 1-bit BitNet.  [P3]: weights become binary     */
+/* values (+1 or -1) through the signum function, activations are       */
+/* absmax-quantised, and the weights are quantised and normalised in   */
+/* groups (for model parallelism).  Readings (the page gives no more):  */
+/*   - the groups are G equal blocks of consecutive output rows (the    */
+/*     model-parallel split of a weight matrix), N % G == 0;            */
+/*   - Wb = +1 where W > 0 and -1 elsewhere (a binary signum: zero has  */
+/*     to go to one side; it goes to -1);                               */
+/*   - each group's scale is its mean absolute weight,                  */
+/*     beta_g = mean |W| over the group's rows (exact sum, rounded      */
+/*     once, as gamma above), and the output is                         */
+/*     bf16(acc * (beta_g * s_tok)), acc = sum_k Wb * q exact;          */
+/*   - activations: the same per-token absmax int8 as above.            */
+/* ------------------------------------------------------------------ */
+void bl_oracle_beta(const float *w, int64_t N, int64_t K, int64_t G, float *beta) {
+    int64_t rows = N / G;
+    for (int64_t g = 0; g < G; ++g) {
+        double s = bl_oracle_sum_abs(w + g * rows * K, rows * K);
+        beta[g] = (float)(s / (double)(rows * K));
+    }
+}
+
+void bl_oracle_binarize(const float *w, int64_t n, int8_t *wb) {
+    for (int64_t i = 0; i < n; ++i) wb[i] = w[i] > 0.0f ? 1 : -1;
+}
+
+/* Packed binary layout (tiles of 16 rows x 256 k, 512 bytes each): one
+ * bit per weight, 1 for +1 and 0 for -1.
+ *   Np = 16*ceil(N/16), K1 = 256*ceil(K/256), KT1 = K1/256
+ *   r = n/16, i = n%16, c = k/256, kk = k%256
+ *   g = i%8, u = i/8, t = kk/64, j = kk%64
+ *   P = j/32, s = (j%32)/4, sb = (j%4)/2, h = j%2, p = 2s + sb
+ *   byte = 512*(r*KT1 + c) + 16*(4g + t) + 4*(2P + u) + (16h + p)/8,
+ *   bit = (16h + p)%8
+ * so lane 4g+t's 16 bytes hold rows g and g+8 over k in [64t, 64t+64),
+ * one 32-bit word per (row, 32-k half).  Padding positions hold 0 (-1);
+ * the matmul never reads them against a nonzero activation. */
+int64_t bl_oracle_packed1_bytes(int64_t N, int64_t K) {
+    int64_t Np = (N + 15) / 16 * 16;
+    int64_t K1 = (K + 255) / 256 * 256;
+    return Np * K1 / 8;
+}
+
+static void position1(int64_t n, int64_t k, int64_t KT1, int64_t *byte, int *bit) {
+    int64_t r = n / 16, c = k / 256;
+    int i = (int)(n % 16), kk = (int)(k % 256);
+    int g = i % 8, u = i / 8, t = kk / 64, j = kk % 64;
+    int P = j / 32, sidx = (j % 32) / 4, sb = (j % 4) / 2, h = j % 2;
+    int p = 2 * sidx + sb, b = 16 * h + p;
+    *byte = 512 * (r * KT1 + c) + 16 * (4 * g + t) + 4 * (2 * P + u) + b / 8;
+    *bit = b % 8;
+}
+
+void bl_oracle_position1(int64_t n, int64_t k, int64_t K, int64_t *byte, int *bit) {
+    position1(n, k, (K + 255) / 256, byte, bit);
+}
+
+void bl_oracle_pack1(const int8_t *wb, int64_t N, int64_t K, uint8_t *packed) {
+    int64_t Np = (N + 15) / 16 * 16, K1 = (K + 255) / 256 * 256, KT1 = K1 / 256;
+    memset(packed, 0, (size_t)(Np * K1 / 8));
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k)
+            if (wb[n * K + k] > 0) {
+                int64_t byte; int bit;
+                position1(n, k, KT1, &byte, &bit);
+                packed[byte] |= (uint8_t)(1u << bit);
+            }
+}
+
+/* Inverse of bl_oracle_pack1 on [0, N) x [0, K); returns the number of set
+ * padding bits. */
+int64_t bl_oracle_unpack1(const uint8_t *packed, int64_t N, int64_t K, int8_t *wb) {
+    int64_t Np = (N + 15) / 16 * 16, K1 = (K + 255) / 256 * 256, KT1 = K1 / 256;
+    int64_t bad = 0;
+    for (int64_t n = 0; n < Np; ++n)
+        for (int64_t k = 0; k < K1; ++k) {
+            int64_t byte; int bit;
+            position1(n, k, KT1, &byte, &bit);
+            int v = (packed[byte] >> bit) & 1;
+            if (n < N && k < K) wb[n * K + k] = v ? 1 : -1;
+            else if (v) ++bad;
+        }
+    return bad;
+}
+
+/* Rescale with one scale per group of N/G consecutive rows:
+ *   f = beta[n / (N/G)] * s_tok[m], out = bf16_rne((float)acc * f). */
+void bl_oracle_epilogue_groups(const int32_t *acc, const float *s_tok, const float *beta, int64_t G,
+                               int64_t M, int64_t N, uint16_t *out) {
+    int64_t rows = N / G;
+    for (int64_t mi = 0; mi < M; ++mi)
+        for (int64_t n = 0; n < N; ++n) {
+            float f = beta[n / rows] * s_tok[mi];
+            float y = (float)acc[mi * N + n] * f;
+            out[mi * N + n] = f32_to_bf16_rne(y);
         }
 }
