@@ -22,7 +22,9 @@ __all__ = [
     "bitlinear_pack_ternary",
     "bitlinear_quant_act", "bitlinear_forward", "bitlinear_check_status",
     "bitlinear_quant_act_f16", "bitlinear_forward_f16", "quant_act_f16", "forward_f16",
-    "bitlinear_set_wait_limit", "bitlinear_set_engine", "bitlinear_status_string", "bitlinear_version",
+    "bitlinear_set_wait_limit", "bitlinear_set_engine", "bitlinear_status_string",
+    "bitlinear_packed5_bytes", "bitlinear_repack5", "bitlinear_forward5", "repack5", "forward5",
+    "bitlinear_packed1_bytes", "bitlinear_pack_binary", "bitlinear_forward_binary", "pack_binary", "forward_binary", "bitlinear_version",
     "pack_weights", "pack_ternary", "quant_act", "forward", "bitlinear",
     "FusedProj", "bitlinear_fused_stats_bytes", "bitlinear_act_stats", "bitlinear_forward_fused",
     "bitlinear_fused_factors", "fused_factors", "new_stats",
@@ -84,6 +86,14 @@ def load_library():
     L.bitlinear_set_wait_limit.argtypes = [ctypes.c_uint32]
     L.bitlinear_set_wait_limit.restype = None
     L.bitlinear_set_engine.argtypes = [ctypes.c_int32, ctypes.c_int32]
+    L.bitlinear_packed5_bytes.argtypes = [I64, I64]
+    L.bitlinear_packed5_bytes.restype = ctypes.c_size_t
+    L.bitlinear_repack5.argtypes = [P, I64, I64, P, P]
+    L.bitlinear_forward5.argtypes = [P, P, P, P, I64, I64, I64, P, P, P]
+    L.bitlinear_packed1_bytes.argtypes = [I64, I64]
+    L.bitlinear_packed1_bytes.restype = ctypes.c_size_t
+    L.bitlinear_pack_binary.argtypes = [P, I64, I64, I64, P, P, P]
+    L.bitlinear_forward_binary.argtypes = [P, P, P, P, I64, I64, I64, I64, P, P, P]
     L.bitlinear_quant_act_f16.argtypes = [P, P, I64, I64, F, P, P, P]
     L.bitlinear_fused_stats_bytes.argtypes = []
     L.bitlinear_fused_stats_bytes.restype = ctypes.c_size_t
@@ -94,7 +104,8 @@ def load_library():
     for name in ("bitlinear_pack_weights", "bitlinear_pack_weights_noalloc", "bitlinear_pack_ternary", "bitlinear_quant_act",
                  "bitlinear_forward", "bitlinear_check_status",
                  "bitlinear_quant_act_f16", "bitlinear_forward_f16", "bitlinear_act_stats",
-                 "bitlinear_forward_fused", "bitlinear_fused_factors", "bitlinear_set_engine"):
+                 "bitlinear_forward_fused", "bitlinear_fused_factors", "bitlinear_set_engine",
+                 "bitlinear_repack5", "bitlinear_forward5", "bitlinear_pack_binary", "bitlinear_forward_binary"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -235,6 +246,40 @@ def bitlinear_set_wait_limit(iterations: int) -> None:
     load_library().bitlinear_set_wait_limit(int(iterations))
 
 
+def bitlinear_packed5_bytes(N: int, K: int) -> int:
+    return int(load_library().bitlinear_packed5_bytes(int(N), int(K)))
+
+
+def bitlinear_repack5(packed, N: int, K: int, packed5, stream=None) -> None:
+    _check(load_library().bitlinear_repack5(_ptr(packed), int(N), int(K), _ptr(packed5), _stream(stream)),
+           "bitlinear_repack5")
+
+
+def bitlinear_forward5(q, tok_scale, packed5, gamma, M: int, N: int, K: int, out, acc_out=None,
+                       stream=None) -> None:
+    _check(load_library().bitlinear_forward5(_ptr(q), _ptr(tok_scale), _ptr(packed5), _ptr(gamma), int(M), int(N),
+                                             int(K), _ptr(out), _ptr(acc_out), _stream(stream)),
+           "bitlinear_forward5")
+
+
+def bitlinear_packed1_bytes(N: int, K: int) -> int:
+    return int(load_library().bitlinear_packed1_bytes(int(N), int(K)))
+
+
+def bitlinear_pack_binary(W, N: int, K: int, groups: int, packed1, beta, stream=None) -> None:
+    _check(load_library().bitlinear_pack_binary(_ptr(W), int(N), int(K), int(groups), _ptr(packed1), _ptr(beta),
+                                                _stream(stream)),
+           "bitlinear_pack_binary")
+
+
+def bitlinear_forward_binary(q, tok_scale, packed1, beta, groups: int, M: int, N: int, K: int, out,
+                             acc_out=None, stream=None) -> None:
+    _check(load_library().bitlinear_forward_binary(_ptr(q), _ptr(tok_scale), _ptr(packed1), _ptr(beta),
+                                                   int(groups), int(M), int(N), int(K), _ptr(out), _ptr(acc_out),
+                                                   _stream(stream)),
+           "bitlinear_forward_binary")
+
+
 def bitlinear_set_engine(gemv_max_tokens: int = -1, split_k: int = 0) -> None:
     """Engine choice of the forward calls (-1 / 0 restore the defaults)."""
     _check(load_library().bitlinear_set_engine(int(gemv_max_tokens), int(split_k)), "bitlinear_set_engine")
@@ -291,6 +336,40 @@ def forward(q: torch.Tensor, tok_scale: torch.Tensor, packed: torch.Tensor, gamm
     if out is None:
         out = torch.empty(M, N, dtype=torch.bfloat16, device=q.device)
     bitlinear_forward(q, tok_scale, packed, gamma, M, N, K, out, acc_out)
+    return out
+
+
+def repack5(packed: torch.Tensor, N: int, K: int) -> torch.Tensor:
+    """2-bit packed matrix -> the five-digits-per-byte layout (uint8 tensor)."""
+    p5 = torch.empty(bitlinear_packed5_bytes(N, K), dtype=torch.uint8, device=packed.device)
+    bitlinear_repack5(packed, N, K, p5)
+    return p5
+
+
+def forward5(q: torch.Tensor, tok_scale: torch.Tensor, packed5: torch.Tensor, gamma: torch.Tensor,
+             N: int, out: torch.Tensor | None = None, acc_out: torch.Tensor | None = None):
+    M, K = q.shape
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=q.device)
+    bitlinear_forward5(q, tok_scale, packed5, gamma, M, N, K, out, acc_out)
+    return out
+
+
+def pack_binary(W: torch.Tensor, groups: int = 1):
+    """fp32 [N, K] CUDA tensor -> (packed sign bits uint8, beta float32 [groups])."""
+    N, K = W.shape
+    p1 = torch.empty(bitlinear_packed1_bytes(N, K), dtype=torch.uint8, device=W.device)
+    beta = torch.empty(groups, dtype=torch.float32, device=W.device)
+    bitlinear_pack_binary(W, N, K, groups, p1, beta)
+    return p1, beta
+
+
+def forward_binary(q: torch.Tensor, tok_scale: torch.Tensor, packed1: torch.Tensor, beta: torch.Tensor,
+                   N: int, out: torch.Tensor | None = None, acc_out: torch.Tensor | None = None):
+    M, K = q.shape
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=q.device)
+    bitlinear_forward_binary(q, tok_scale, packed1, beta, beta.numel(), M, N, K, out, acc_out)
     return out
 
 

@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libbitlinear.so")
-SOURCES = ["pack.cu", "quant.cu", "gemv.cu", "fused.cu", "gemm.cu", "api.cu"]
+SOURCES = ["pack.cu", "quant.cu", "gemv.cu", "fused.cu", "gemm.cu", "variants.cu", "api.cu"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

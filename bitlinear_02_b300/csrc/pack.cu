@@ -230,8 +230,75 @@ cudaError_t launch_pack(const void *src, bool from_float, int64_t N, int64_t K, 
     return cudaGetLastError();
 }
 
+// Original binary BitNet (lumen-it.ai BitNet article): signum weights, one
+// bit each (1 for W > 0, 0 otherwise), in tiles of 16 rows x 256 k: lane
+// 4g+t holds rows g, g+8 at k in [64t, 64t+64), word 2P+u (row g+8u, k half
+// P) holds k = 64t + 32P + j at bit 16(j%2) + 2(j/4) + (j%4)/2.  One thread
+// per output word reads its row's 32 consecutive floats.
+__global__ void __launch_bounds__(256) pack1_kernel(const float *__restrict__ W, int64_t N, int64_t K, int64_t KT1,
+                                                    int64_t nwords, uint32_t *__restrict__ out) {
+    const int64_t wi = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    if (wi >= nwords) return;
+    const int64_t tile = wi / 128;
+    const int lw = static_cast<int>(wi % 128);
+    const int64_t r = tile / KT1, c = tile % KT1;
+    const int lane = lw / 4, wd = lw % 4;
+    const int P = wd / 2, u = wd % 2, g = lane / 4, t = lane % 4;
+    const int64_t n = 16 * r + 8 * u + g;
+    const int64_t kb = 256 * c + 64 * t + 32 * P;
+    uint32_t word = 0;
+    if (n < N) {
+        const float *row = W + n * K;
+#pragma unroll 4
+        for (int j = 0; j < 32; ++j) {
+            const int64_t k = kb + j;
+            if (k < K && row[k] > 0.0f) word |= 1u << (16 * (j % 2) + 2 * (j / 4) + (j % 4) / 2);
+        }
+    }
+    out[wi] = word;
+}
+
 }  // namespace
 }  // namespace bl
+
+extern "C" size_t bitlinear_packed1_bytes(int64_t N, int64_t K) {
+    if (N < 1 || K < 1) return 0;
+    return static_cast<size_t>((N + 15) / 16 * 16 * ((K + 255) / 256 * 256) / 8);
+}
+
+extern "C" bitlinear_status_t bitlinear_pack_binary(const float *W, int64_t N, int64_t K, int64_t groups,
+                                                    uint8_t *packed1, float *beta, void *stream) {
+    using namespace bl;
+    if (!W || !packed1 || !beta || !shape_ok(N, K) || groups < 1 || N % groups != 0)
+        return BITLINEAR_ERR_INVALID_ARG;
+    if (!aligned16(W) || !aligned16(packed1) || !aligned4(beta)) return BITLINEAR_ERR_INVALID_ARG;
+    if (N * K > kMaxSumElems || groups > 65536) return BITLINEAR_ERR_UNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned long long *ws = nullptr;
+    if (workspace(&ws) != cudaSuccess) return BITLINEAR_ERR_CUDA;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // beta_g = mean |W| over the g-th block of N/G rows, each by the exact
+    // bucket sum (the blocks are contiguous and 64-byte aligned: K % 16 == 0)
+    const int64_t per = N / groups * K;
+    for (int64_t gi = 0; gi < groups; ++gi) {
+        if (cudaMemsetAsync(ws, 0, kBuckets * sizeof(unsigned long long), st) != cudaSuccess)
+            return BITLINEAR_ERR_CUDA;
+        const int64_t n4 = per / 4, want = (n4 + 255) / 256;
+        const unsigned blocks = static_cast<unsigned>(want < sms * 8 ? (want < 1 ? 1 : want) : sms * 8);
+        absmean_buckets_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4 *>(W + gi * per), n4, ws);
+        gamma_finish_kernel<<<1, 32, 0, st>>>(ws, per, beta + gi);
+        if (cudaGetLastError() != cudaSuccess) return BITLINEAR_ERR_CUDA;
+    }
+    const int64_t KT1 = (K + 255) / 256;
+    const int64_t nwords = static_cast<int64_t>(bitlinear_packed1_bytes(N, K)) / 4;
+    pack1_kernel<<<static_cast<unsigned>((nwords + 255) / 256), 256, 0, st>>>(W, N, K, KT1, nwords,
+                                                                             reinterpret_cast<uint32_t *>(packed1));
+    if (cudaGetLastError() != cudaSuccess) return BITLINEAR_ERR_CUDA;
+    publish_kernel<<<1, 32, 0, st>>>();  // as launch_pack: packed bytes final before any dependent starts
+    return cudaGetLastError() == cudaSuccess ? BITLINEAR_OK : BITLINEAR_ERR_CUDA;
+}
 
 extern "C" size_t bitlinear_packed_bytes(int64_t N, int64_t K) {
     if (N < 1 || K < 1) return 0;

@@ -330,6 +330,88 @@ BITLINEAR_API void bitlinear_set_wait_limit(uint32_t iterations);
  */
 BITLINEAR_API bitlinear_status_t bitlinear_set_engine(int32_t gemv_max_tokens, int32_t split_k);
 
+/* ---------------------------------------------------------------------
+ * Variant weight formats (decode engines, M <= 64 tokens).
+ *
+ * Five ternary digits per byte (vi.news.hada.io topic 20406, the comments
+ * on ternary packing: 3^5 = 243 <= 256, so a b1.58 weight needs 1.6 bits
+ * rather than 2).  Digits e = Wq + 1, most significant first, form
+ * v = e0*81 + e1*27 + e2*9 + e3*3 + e4, stored as b = ceil(256 v / 243).
+ * Layout: Np = 16*ceil(N/16), K5 = 160*ceil(K/160); Np*K5/5 bytes in
+ * 512-byte tiles, one per (row group r = n/16, k block c = k/160), tile
+ * index r*(K5/160) + c.  Inside a tile, with i = n%16, kk = k%160:
+ *   g = i%8, u = i/8, t = kk/40, j = (kk%40)/5, d = kk%5,
+ *   byte 16*(4g + t) + 8u + j of the tile holds digit d of (n, k).
+ * Padding positions hold digit 1 (weight 0).
+ */
+
+/* Bytes of the five-digit layout for an N x K matrix (0 if N or K < 1). */
+BITLINEAR_API size_t bitlinear_packed5_bytes(int64_t N, int64_t K);
+
+/*
+ * Re-encodes a 2-bit packed matrix (bitlinear_pack_weights /
+ * bitlinear_pack_ternary output) into the five-digit layout, on the device.
+ * packed: bitlinear_packed_bytes(N, K) bytes; packed5: caller-owned,
+ * bitlinear_packed5_bytes(N, K) bytes; both 16-byte aligned device pointers.
+ * The weight scale gamma is unchanged (bitlinear_forward5 takes it as is).
+ * N >= 1, K >= 16, K % 16 == 0.  Errors: INVALID_ARG (shape, null or
+ * misaligned pointer), UNSUPPORTED (more than 2^31 blocks of work), CUDA.
+ */
+BITLINEAR_API bitlinear_status_t bitlinear_repack5(const uint8_t *packed, int64_t N, int64_t K,
+                                                   uint8_t *packed5, void *stream);
+
+/*
+ * bitlinear_forward on the five-digit layout: the same arguments, the same
+ * int32 accumulators and bf16 outputs bit for bit, 20 % fewer weight bytes
+ * read.  M <= 64 (the decode engine, 16-token chunks); larger M returns
+ * UNSUPPORTED (the tensor-core GEMM reads the 2-bit layout).
+ */
+BITLINEAR_API bitlinear_status_t bitlinear_forward5(const int8_t *q, const float *tok_scale,
+                                                    const uint8_t *packed5, const float *gamma,
+                                                    int64_t M, int64_t N, int64_t K, void *out_bf16,
+                                                    int32_t *acc_out, void *stream);
+
+/*
+ * The original 1-bit BitNet (lumen-it.ai BitNet article: weights binarised
+ * to +1 / -1 by the signum function, absmax activations, quantisation in
+ * groups).  Wb = +1 where W > 0, -1 elsewhere (zero goes to -1); the N rows
+ * form G groups of N/G consecutive rows, each with its own scale
+ * beta_g = mean |W| over the group (exact sum rounded once, as gamma);
+ * out[m, n] = bf16(acc * (beta_{n / (N/G)} * tok_scale[m])),
+ * acc = sum_k Wb[n, k] * q[m, k] exact.  Activations: bitlinear_quant_act.
+ * Layout: Np = 16*ceil(N/16), K1 = 256*ceil(K/256); Np*K1/8 bytes in
+ * 512-byte tiles, one per (r = n/16, c = k/256), tile index r*(K1/256) + c.
+ * Inside a tile, with i = n%16, kk = k%256:
+ *   g = i%8, u = i/8, t = kk/64, j = kk%64, P = j/32, s = (j%32)/4,
+ *   sb = (j%4)/2, h = j%2, bit = 16h + 2s + sb,
+ *   byte 16*(4g + t) + 4*(2P + u) + bit/8, bit bit%8 of it; 1 means +1.
+ * Padding bits are 0.
+ */
+BITLINEAR_API size_t bitlinear_packed1_bytes(int64_t N, int64_t K);
+
+/*
+ * Binarises and packs fp32 W [N, K] (device, row-major, 16-byte aligned)
+ * and writes the G group scales to beta[G] (device, 4-byte aligned).
+ * packed1: caller-owned, bitlinear_packed1_bytes(N, K) bytes, 16-byte
+ * aligned.  N % groups == 0, 1 <= groups <= 65536, K >= 16, K % 16 == 0,
+ * N*K <= 2^40.  Errors: INVALID_ARG, UNSUPPORTED, CUDA.  Uses the same 2 KB
+ * device workspace as bitlinear_pack_weights.
+ */
+BITLINEAR_API bitlinear_status_t bitlinear_pack_binary(const float *W, int64_t N, int64_t K,
+                                                       int64_t groups, uint8_t *packed1, float *beta,
+                                                       void *stream);
+
+/*
+ * out = (Wb q) rescaled per group, as above.  q, tok_scale, out_bf16,
+ * acc_out as in bitlinear_forward; beta: the groups scales (device, 4-byte
+ * aligned).  M <= 64 (else UNSUPPORTED), N % groups == 0 (else
+ * INVALID_ARG).
+ */
+BITLINEAR_API bitlinear_status_t bitlinear_forward_binary(const int8_t *q, const float *tok_scale,
+                                                          const uint8_t *packed1, const float *beta,
+                                                          int64_t groups, int64_t M, int64_t N, int64_t K,
+                                                          void *out_bf16, int32_t *acc_out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -161,3 +161,22 @@ def test_set_engine_validates_without_a_gpu(lib):
     assert lib.bitlinear_set_engine(0, -1) == bl.ERR_INVALID_ARG
     assert lib.bitlinear_set_engine(0, 16) == bl.OK
     assert lib.bitlinear_set_engine(-1, 0) == bl.OK                # the defaults again
+
+
+def test_variant_sizes_and_argument_checks(lib):
+    assert bl.bitlinear_packed5_bytes(16, 160) == 512
+    assert bl.bitlinear_packed5_bytes(17, 336) == 32 * 480 // 5
+    assert bl.bitlinear_packed5_bytes(0, 16) == 0
+    assert bl.bitlinear_packed1_bytes(16, 256) == 512
+    assert bl.bitlinear_packed1_bytes(17, 272) == 32 * 512 // 8
+    P = ctypes.c_void_p
+    f = P(FAKE)
+    assert lib.bitlinear_repack5(f, 16, 10, f, None) == bl.ERR_INVALID_ARG          # K % 16
+    assert lib.bitlinear_repack5(None, 16, 16, f, None) == bl.ERR_INVALID_ARG
+    assert lib.bitlinear_forward5(f, f, f, f, 65, 32, 64, f, None, None) == bl.ERR_UNSUPPORTED  # decode only
+    assert lib.bitlinear_forward5(f, f, f, f, 4, 32, 60, f, None, None) == bl.ERR_INVALID_ARG
+    assert lib.bitlinear_forward5(f, f, f, f, 0, 32, 64, f, None, None) == bl.OK     # empty batch
+    assert lib.bitlinear_pack_binary(f, 32, 64, 0, f, f, None) == bl.ERR_INVALID_ARG  # no groups
+    assert lib.bitlinear_pack_binary(f, 30, 64, 4, f, f, None) == bl.ERR_INVALID_ARG  # N % G
+    assert lib.bitlinear_forward_binary(f, f, f, f, 3, 4, 32, 64, f, None, None) == bl.ERR_INVALID_ARG
+    assert lib.bitlinear_forward_binary(f, f, f, f, 2, 65, 32, 64, f, None, None) == bl.ERR_UNSUPPORTED
