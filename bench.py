@@ -458,6 +458,70 @@ def gemv_sweep(torch, bl, inputs, dev, stream, hbm_peak, reps=7, m_list=M_LIST):
                     f"{reps} replays / launches", "rows": rows}
 
 
+def variants_sweep(torch, bl, inputs, dev, stream, hbm_peak, reps=7, m_list=(1, 16)):
+    """The decode engines of the three weight formats on the same shapes:
+    2-bit (bitlinear_forward), five ternary digits per byte
+    (bitlinear_forward5) and the binary variant (bitlinear_forward_binary,
+    8 row groups).  Same method as the GEMV sweep (a graph of launches over
+    distinct copies, at least 512 MB, replayed after an L2 flush).  GB/s
+    counts each format's own bytes; weights/s compares the formats."""
+    T = torch
+    flush = T.empty(256 << 20, dtype=T.uint8, device=dev)
+    e0, e1 = T.cuda.Event(enable_timing=True), T.cuda.Event(enable_timing=True)
+    shapes = [("2b", "q,k,v,o", 2560, 2560), ("2b", "gate,up", 6912, 2560), ("2b", "down", 2560, 6912),
+              ("70b", "gate,up", 28672, 8192), ("70b", "down", 8192, 28672)]
+    rows = []
+    for si, (model, proj, N, K) in enumerate(shapes):
+        w = inputs.weights_fp32(N, K, seed=700 + si, device=dev)
+        p2, gam = bl.pack_weights(w, 1e-5)
+        p5 = bl.repack5(p2, N, K)
+        p1, beta = bl.pack_binary(w, 8)
+        del w
+        fmts = [("2bit", p2, lambda q, sc, p, out, M: bl.bitlinear_forward(q, sc, p, gam, M, N, K, out, None, stream)),
+                ("5trit", p5, lambda q, sc, p, out, M: bl.bitlinear_forward5(q, sc, p, gam, M, N, K, out, None,
+                                                                             stream)),
+                ("binary", p1, lambda q, sc, p, out, M: bl.bitlinear_forward_binary(q, sc, p, beta, 8, M, N, K, out,
+                                                                                    None, stream))]
+        for name, p0, fn in fmts:
+            pb = p0.numel()
+            ncopy = max(8, min(64, -(-(512 << 20) // pb)))
+            mats = [p0] + [p0.clone() for _ in range(ncopy - 1)]
+            for M in m_list:
+                x = inputs.activations_bf16(M, K, seed=900 + M, device=dev)
+                q, sc = bl.quant_act(x)
+                out = T.empty(M, N, dtype=T.bfloat16, device=dev)
+
+                def run():
+                    for p in mats:
+                        fn(q, sc, p, out, M)
+
+                g = capture(T, run, stream)
+                ts = []
+                with T.cuda.stream(stream):
+                    for _ in range(reps):
+                        flush.zero_()
+                        e0.record(stream)
+                        g.replay()
+                        e1.record(stream)
+                        e1.synchronize()
+                        ts.append(e0.elapsed_time(e1))
+                ms = statistics.median(ts) / ncopy
+                b = pb + M * K + 4 * M + 2 * M * N + 4
+                gbs = b / (ms * 1e-3) / 1e9
+                rows.append({"model": model, "proj": proj, "N": N, "K": K, "M": M, "format": name,
+                             "packed_bytes": pb, "us": round(ms * 1e3, 3), "GB/s": round(gbs, 1),
+                             "frac": round(gbs / hbm_peak, 4),
+                             "Gweights/s": round(N * K / (ms * 1e-3) / 1e9, 1), "launches": ncopy})
+                del g
+            del mats
+        del p2, p5, p1
+    del flush
+    T.cuda.empty_cache()
+    return {"mode": "per (shape, format, M): a graph of decode launches over distinct copies of the packed matrix "
+                    f"on a pre-quantised input, replayed after a 256 MB L2 flush; median of {reps} replays / "
+                    "launches; GB/s over each format's own bytes", "rows": rows}
+
+
 def quant_sweep(torch, bl, inputs, dev, stream, reps=7):
     """bitlinear_quant_act on its own at the decode sizes (20 distinct inputs per graph)."""
     T = torch
@@ -950,6 +1014,7 @@ def main():
         if not args.no_sweeps:
             sweep = gemv_sweep(torch, bl, inputs, dev, stream, hbm_peak)
             sweep["quant_act"] = quant_sweep(torch, bl, inputs, dev, stream)
+            sweep["formats"] = variants_sweep(torch, bl, inputs, dev, stream, hbm_peak)
             midm = midm_sweep(torch, bl, inputs, st, stream)
         del runs
         if not args.no_prefill:

@@ -63,16 +63,29 @@ extern "C" void bitlinear_set_wait_limit(uint32_t iterations) {
 constexpr int64_t kGemvMaxM = 64;
 namespace bl {
 namespace {
-constexpr int32_t kDefaultGemvMaxTokens = 64;
-std::atomic<int32_t> g_gemv_max_tokens{kDefaultGemvMaxTokens};
+std::atomic<int32_t> g_gemv_max_tokens{-1};  // -1: the measured default below
 std::atomic<int32_t> g_split_k{0};
+
+// The default engine choice (B300 measurements, weights from HBM): the GEMV
+// up to 48 tokens (three 16-token chunks); at 49-64 tokens (four chunks) the
+// split-K GEMM where K is large and the matrix is big - 8192x8192 34.8 us
+// against 43.0, 8192x28672 94 against 125-141, 2560x6912 18.4 against 19.7
+// - and the GEMV elsewhere (2560x2560 12.3 against 14.3, 6912x2560 16.4
+// against 18.4, 1024x8192 14.3 against 16.4); the GEMM above 64.
+bool use_gemv(int64_t M, int64_t N, int64_t K) {
+    const int32_t forced = g_gemv_max_tokens.load();
+    if (forced >= 0) return M <= forced;
+    if (M > kGemvMaxM) return false;
+    if (M > 48 && K >= 6912 && N * K >= (1ll << 24)) return false;
+    return true;
+}
 }  // namespace
 }  // namespace bl
 
 extern "C" bitlinear_status_t bitlinear_set_engine(int32_t gemv_max_tokens, int32_t split_k) {
     if (gemv_max_tokens < -1 || gemv_max_tokens > kGemvMaxM || split_k < 0 || split_k > 16)
         return BITLINEAR_ERR_INVALID_ARG;
-    bl::g_gemv_max_tokens.store(gemv_max_tokens < 0 ? bl::kDefaultGemvMaxTokens : gemv_max_tokens);
+    bl::g_gemv_max_tokens.store(gemv_max_tokens);
     bl::g_split_k.store(split_k);
     return BITLINEAR_OK;
 }
@@ -90,12 +103,13 @@ extern "C" bitlinear_status_t bitlinear_forward(const int8_t *q, const float *to
     if (!aligned16(q) || !aligned4(tok_scale) || !aligned16(packed) || !aligned4(gamma) ||
         !aligned16(out_bf16) || (acc_out && !aligned16(acc_out)))
         return BITLINEAR_ERR_INVALID_ARG;
-    if ((N + 15) / 16 > 65535 * 4 && M <= g_gemv_max_tokens.load()) return BITLINEAR_ERR_UNSUPPORTED;
+    const bool gemv = use_gemv(M, N, K);
+    if ((N + 15) / 16 > 65535 * 4 && gemv) return BITLINEAR_ERR_UNSUPPORTED;
     if ((M + 63) / 64 > 65535) return BITLINEAR_ERR_UNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     auto *out = static_cast<__nv_bfloat16 *>(out_bf16);
     cudaError_t e;
-    if (M <= g_gemv_max_tokens.load())  // the decode GEMV, in 16-token chunks above 16
+    if (gemv)  // the decode GEMV, in 16-token chunks above 16
         e = launch_gemv(q, tok_scale, packed, gamma, static_cast<int>(M), static_cast<int>(N),
                         static_cast<int>(K), out, acc_out, st, num_sms());
     else

@@ -318,8 +318,10 @@ BITLINEAR_API void bitlinear_set_wait_limit(uint32_t iterations);
  * same bits).
  *   gemv_max_tokens: batches of up to this many tokens run bitlinear_forward
  *     on the decode GEMV engine (16-token chunks of one launch), larger ones
- *     on the tensor-core GEMM.  -1 restores the default; 0 sends every batch
- *     to the GEMM; at most 64.
+ *     on the tensor-core GEMM; 0 sends every batch to the GEMM; at most 64.
+ *     -1 restores the default: the GEMV up to 48 tokens, and at 49-64 tokens
+ *     too unless K >= 6912 and N*K >= 2^24 (where the split-K GEMM was
+ *     measured faster).
  *   split_k: CTAs per cluster that share one GEMM output tile's k range
  *     (their int32 partial tiles summed through distributed shared memory).
  *     0 restores the default (the planner picks 1..16 from the tile count,
