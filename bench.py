@@ -861,6 +861,52 @@ def profile_gemv(spec):
     return 0
 
 
+def profile_format(spec):
+    """--profile-format FMT,N,K,M[,copies]: the decode engine of one weight
+    format (2bit, 5trit, binary) on `copies` distinct copies of one matrix,
+    2 warm-up passes + 3 timed passes (the driver for ncu captures)."""
+    import torch
+    import bitlinear_02_b300 as bl
+    from bitlinear_02_b300 import inputs
+    parts = spec.split(",")
+    fmt = parts[0]
+    N, K, M = (int(v) for v in parts[1:4])
+    copies = int(parts[4]) if len(parts) > 4 else 4
+    dev = torch.device("cuda:0")
+    w = inputs.weights_fp32(N, K, seed=5, device=dev)
+    p2, gam = bl.pack_weights(w, 1e-5)
+    if fmt == "5trit":
+        p0 = bl.repack5(p2, N, K)
+        fn = lambda q, s, p, out: bl.bitlinear_forward5(q, s, p, gam, M, N, K, out)
+    elif fmt == "binary":
+        p0, beta = bl.pack_binary(w, 8)
+        fn = lambda q, s, p, out: bl.bitlinear_forward_binary(q, s, p, beta, 8, M, N, K, out)
+    else:
+        p0 = p2
+        fn = lambda q, s, p, out: bl.bitlinear_forward(q, s, p, gam, M, N, K, out)
+    del w
+    mats = [p0] + [p0.clone() for _ in range(copies - 1)]
+    x = inputs.activations_bf16(M, K, seed=3, device=dev)
+    q, s = bl.quant_act(x)
+    out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    for _ in range(2):
+        for p in mats:
+            fn(q, s, p, out)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(3):
+        for p in mats:
+            fn(q, s, p, out)
+    e1.record()
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / (3 * copies)
+    assert bl.bitlinear_check_status() == bl.OK
+    print(json.dumps({"profile": "format", "format": fmt, "N": N, "K": K, "M": M, "us": round(ms * 1000, 2),
+                      "weight_GB/s": round(p0.numel() / (ms * 1e-3) / 1e9, 1)}))
+    return 0
+
+
 def profile_fused(spec):
     """--profile-fused L,M: the fused decode path on an L-layer 2B-shape
     stack at M tokens, eagerly launched: 3 warm-up + 5 timed passes (driver
@@ -903,6 +949,8 @@ def main():
     ap.add_argument("--profile-gemm", default=None, help="N,K,M[,int8]: time one GEMM shape (ncu driver)")
     ap.add_argument("--profile-gemv", default=None, help="N,K,M[,copies]: time the decode GEMV (ncu driver)")
     ap.add_argument("--profile-fused", default=None, help="L,M: time the fused decode path (ncu driver)")
+    ap.add_argument("--profile-format", default=None,
+                    help="FMT,N,K,M[,copies]: time one weight format's decode engine (ncu driver)")
     args = ap.parse_args()
     if args.profile_gemm:
         return profile_gemm(args.profile_gemm)
@@ -910,6 +958,8 @@ def main():
         return profile_gemv(args.profile_gemv)
     if args.profile_fused:
         return profile_fused(args.profile_fused)
+    if args.profile_format:
+        return profile_format(args.profile_format)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
@@ -1066,7 +1116,7 @@ def main():
                      "unit": "GB/s", "frac": round(fused_gbs / hbm_peak, 4),
                      "traffic": (round(FUSED_DRAM_PER_PACKED_BYTE * st.packed_bytes * len(M_LIST) / n_fused)
                                  if FUSED_DRAM_PER_PACKED_BYTE else None),
-                     "kernel": "decode_kernel<NT, true> (the fused decode path: quantiser folded into the GEMV)",
+                     "kernel": "fused_gemv_kernel<NT> (the fused decode path: quantiser folded into the GEMV)",
                      "launch_avg_us": round(launch_us, 3), "algo_bytes_per_launch": round(bytes_launch),
                      "peak_note": f"{peak_kind} HBM copy bandwidth",
                      "method": "CUDA events on the launching stream around the timed graph replays; the three "

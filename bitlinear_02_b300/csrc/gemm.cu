@@ -1047,7 +1047,10 @@ cudaError_t launch_gemm(const int8_t *q, const float *tok_scale, const uint8_t *
         const size_t bytes = static_cast<size_t>(M) * K * 2;
         void *q16 = nullptr;
         cudaError_t e = widen_alloc(&q16, bytes, st);
-        if (e != cudaSuccess) return e;
+        if (e != cudaSuccess) {
+            cudaGetLastError();  // a failed allocation is the call's error, not the caller's next one
+            return e;
+        }
         const int64_t n16 = static_cast<int64_t>(M) * K / 16;  // K % 16 == 0
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;

@@ -191,15 +191,24 @@ BITLINEAR_API bitlinear_status_t bitlinear_quant_act(const void *x_bf16, const v
  * cudaStreamWaitEvent.  Do not write it with a kernel of your own launched
  * immediately before this call on the same stream: launch that kernel on
  * another stream and join the streams with an event instead.
- * Engine choice is internal: M <= 64 runs the decode GEMV (legacy tensor
- * MMA on register-unpacked codes; above 16 tokens in 16-token chunks of one
- * launch), larger M runs the prefill GEMM (tcgen05 MMA with TMEM
- * accumulators).  Both give identical results.
+ * Engine choice is internal (bitlinear_set_engine overrides it): up to 48
+ * tokens, and up to 64 where K < 6912 or N*K < 2^24, the decode GEMV
+ * (legacy tensor MMA on register-unpacked codes; above 16 tokens in 16-token
+ * chunks of one launch); otherwise the tcgen05 GEMM (TMEM accumulators),
+ * with its K range split across a cluster where the output tiles alone
+ * would leave most SMs idle.  Above 256 tokens the int8 activations are
+ * first widened to f16 (exact) into a buffer taken, stream-ordered, from a
+ * memory pool the library keeps per device (M*K*2 bytes, returned to the
+ * pool at the end of the call; the pool keeps its memory for later calls).
+ * All engines give identical results.
  * Every bounded wait inside the GEMM that expires sets a device status
  * word; bitlinear_check_status reports it.
  * Errors: INVALID_ARG (null/misaligned pointer, M < 0, N < 1, K < 16,
  * K % 16 != 0, K > 65536: the fp32 tensor-core sums stay exact below
- * that), CUDA (launch failure).
+ * that), UNSUPPORTED (more than 65535*64 tokens, or more than 65535*4 row
+ * groups on the GEMV), CUDA (launch failure, or the widening buffer could
+ * not be allocated; the runtime's last-error state is cleared, so the
+ * failure is reported here only).
  */
 BITLINEAR_API bitlinear_status_t bitlinear_forward(const int8_t *q, const float *tok_scale,
                                      const uint8_t *packed, const float *gamma, int64_t M,

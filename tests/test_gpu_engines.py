@@ -187,3 +187,29 @@ def test_expired_wait_ends_the_gemm_promptly(M, split):
     wq_cpu = wq.cpu().numpy()
     want = oracle.matmul_pairs(q_ref, wq_cpu, ms, ns)
     np.testing.assert_array_equal(acc.cpu().numpy()[ms, ns], want)
+
+
+def test_failing_allocation_is_err_cuda_and_recovers():
+    """Host-side failure injection: a prefill call whose f16 widening buffer
+    cannot exist (4e6 tokens x 65536 x 2 bytes = 512 GB, above the 288 GB of
+    HBM) returns ERR_CUDA before any kernel runs and leaves no error behind;
+    the next calls compute the right bits.  (The activation buffers are
+    small: nothing reads them, the allocation fails first.)"""
+    M, N, K = 4_000_000, 16, 65536
+    # only where the buffer cannot fit in the device's memory at all
+    assert torch.cuda.mem_get_info()[1] < M * K * 2
+    q = torch.zeros(16, K, dtype=torch.int8, device=DEV)
+    s = torch.ones(16, dtype=torch.float32, device=DEV)
+    packed = bl.pack_ternary(inputs.ternary(N, K, seed=3).to(DEV))
+    gam = torch.ones(1, dtype=torch.float32, device=DEV)
+    out = torch.empty(16, N, dtype=torch.bfloat16, device=DEV)
+    torch.cuda.synchronize()
+    L = bl.load_library()
+    st = L.bitlinear_forward(bl._ptr(q), bl._ptr(s), bl._ptr(packed), bl._ptr(gam), M, N, K, bl._ptr(out), None,
+                             bl._stream(None))
+    assert st == bl.ERR_CUDA
+    torch.cuda.synchronize()  # no error left in the context or the runtime
+    assert bl.bitlinear_check_status() == bl.OK
+    # a normal prefill call afterwards is right
+    case = Case(300, 1040, 300, seed=41)
+    case.check()
