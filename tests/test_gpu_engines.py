@@ -89,8 +89,10 @@ class Case:
 
 
 @pytest.mark.parametrize("M", [1, 16, 40, 64, 65, 100, 176, 256])
-@pytest.mark.parametrize("N,K", [(300, 1040), (2560, 2560), (1000, 6912)])
+@pytest.mark.parametrize("N,K", [(300, 1040), (2560, 2560), (1000, 6912), (4112, 4096)])
 def test_every_route_bit_exact(N, K, M):
+    # 4112 x 4096 holds 2^24 + 2^16 weights: above 64 tokens the int8 input
+    # is widened to f16 first (and 4112 rows leave a ragged last row tile)
     case = Case(N, K, M, seed=31 * N + K + M)
     for route, (gmax, split) in ROUTES.items():
         bl.bitlinear_set_engine(gmax, split)
@@ -140,13 +142,19 @@ def _time_forward(fn, reps=3):
     return best
 
 
-@pytest.mark.parametrize("M,split", [(4096, 0), (100, 4)])
-def test_expired_wait_ends_the_gemm_promptly(M, split):
+@pytest.mark.parametrize("M,N,split", [(4096, 2560, 0), (64, 2560, 4)])
+def test_expired_wait_ends_the_gemm_promptly(M, N, split):
     """One expired wait ends every role's waits (a flag in shared memory):
-    with a wait limit of one try the GEMM over K = 65536 gives up within a
-    small fraction of its normal time, reports ERR_TIMEOUT, and the next call
-    computes the same bits as before."""
-    N, K = 2560, 65536
+    with a wait limit of one try the GEMM over K = 65536 reports ERR_TIMEOUT
+    and ends well before its normal time, and the next call computes the same
+    bits as before.  Without the flag every stage would still run (each
+    role's failed tries only set its own bit), so the call would take at
+    least its normal time.  When the first one-try wait expires depends on
+    how long the hardware suspends a try, hence the bound of half the normal
+    time.  (4096 tokens: the f16-operand kernel after the widening pass; 64
+    tokens through the GEMM: the int8-operand kernel split across clusters
+    of 4.)"""
+    K = 65536
     bl.bitlinear_set_engine(0, split)
     wq = inputs.ternary(N, K, seed=77, device=DEV)
     packed = bl.pack_ternary(wq)
@@ -172,7 +180,7 @@ def test_expired_wait_ends_the_gemm_promptly(M, split):
     finally:
         bl.bitlinear_set_wait_limit(0)
     assert st == bl.ERR_TIMEOUT
-    assert t_abort < 0.25 * t_norm, (t_abort, t_norm)
+    assert t_abort < 0.5 * t_norm, (t_abort, t_norm)
     assert wall < 5.0
     # recovery: the same bits as before the timeout
     assert bl.bitlinear_check_status() == bl.OK
