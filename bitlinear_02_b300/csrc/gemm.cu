@@ -1,10 +1,11 @@
-// Prefill engine (bitlinear_forward above 64 tokens, bitlinear_forward_f16 at
-// any M): a dense contraction on the 5th-generation tensor cores.
+// Prefill and mid-M engine (bitlinear_forward above 48-64 tokens,
+// bitlinear_forward_f16 at any M): a dense contraction on the 5th-generation
+// tensor cores.
 //
-// asi.tokyo 2B4T write-up, on its GPU kernel (four weights packed per byte):
-// packed ternary weights are unpacked next to the math units and multiplied
-// with 8-bit activations.  B300 (sm_103a) has no
-// int8 tcgen05 MMA, so both operands are fed as f16: ternary codes become
+// asi.tokyo, "マイクロソフトが偶然に作った史上最も効率的なAI" (2025-04-27), the paragraph on
+// running the model on a GPU: a custom kernel packs four weights per byte,
+// unpacks them next to the math units and multiplies them with 8-bit
+// activations.  B300 (sm_103a) has no int8 tcgen05 MMA, so both operands are fed as f16: ternary codes become
 // -1/0/+1 and int8 activations their exact f16 values.  Every product is an
 // integer of magnitude <= 128 and every partial sum an integer below 2^24
 // for K <= 65536, so the fp32 TMEM accumulator holds the exact int32 result.

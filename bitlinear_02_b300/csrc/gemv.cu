@@ -1,9 +1,10 @@
 // Decode engine (bitlinear_forward up to 64 tokens: 16-token chunks as
 // blockIdx.z): HBM-bound stream of packed ternary weights.
 //
-// asi.tokyo 2B4T write-up, on its GPU kernel (four weights packed per
-// byte): the weights travel packed four per byte and are unpacked right next
-// to the math units, then multiplied with 8-bit activations.  Here every 16-byte lane chunk of the packed layout is
+// asi.tokyo, "マイクロソフトが偶然に作った史上最も効率的なAI" (2025-04-27), the paragraph on
+// running the model on a GPU: the weights travel packed four per byte and are
+// unpacked right next to the math units, then multiplied with 8-bit
+// activations.  Here every 16-byte lane chunk of the packed layout is
 // loaded once (128-bit, streaming), unpacked in registers and fed to the
 // legacy tensor-core MMA (m16n8k16, f16 inputs, fp32 accumulate) - on B300
 // its f16 rate is four times its int8 rate and far above dp4a.

@@ -2,8 +2,9 @@
 //
 // BitNet b1.58 (cheatsheet.md, "BitNet b1.58とは？"): weights are divided by
 // their mean absolute value and rounded to the nearest integer in
-// {-1, 0, +1}.  The asi.tokyo 2B4T write-up: four ternary weights are
-// packed into each byte.
+// {-1, 0, +1}.  asi.tokyo, "マイクロソフトが偶然に作った史上最も効率的なAI"
+// (2025-04-27), the paragraph on running the model on a GPU: four ternary
+// weights are packed into each byte.
 //
 // gamma = mean|W| is computed exactly, so it does not depend on the order of
 // a floating-point reduction (a different order would move weights across

@@ -9,7 +9,9 @@
  *
  * Plain, slow, obviously correct.  Each function cites the passage of the
  * source pages it follows.  Pages (by title):
- *   [P1] asi.tokyo, "BitNet B1.58 2B4T" write-up (2025-04-27)
+ *   [P1] asi.tokyo, "マイクロソフトが偶然に作った史上最も効率的なAI" (2025-04-27),
+ *        on BitNet B1.58 2B4T (no section headings: passages are named by
+ *        their subject, e.g. the paragraph on running the model on a GPU)
  *   [P2] cheatsheet.md, "1ビットLarge Language Models時代：マイクロソフトがBitNet b1.58を紹介"
  *   [P3] lumen-it.ai, BitNet (original 1-bit BitNet) article
  *   [P4] vi.news.hada.io topic 20406 (and its Portuguese twin), comments
