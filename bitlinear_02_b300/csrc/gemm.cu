@@ -711,6 +711,245 @@ __global__ void __launch_bounds__(kThreads, 1)
                            tok_scale, gamma, out, acc_out, staged ? &omap : nullptr, &amap, wait_limit);
 }
 
+// ---------------------------------------------------------------------------
+// Persistent variant of the f16-operand GEMM, for grids of more tiles than
+// SMs: one CTA per SM walks the tiles t = blockIdx.x, + gridDim.x, ... with
+// two TMEM accumulators, so the epilogue of one tile (4 warps of their own)
+// runs under the next tile's MMAs instead of after them.  Tensor memory:
+// accumulators in columns [0, BN) and [BN, 2BN), then a ring of NA 32-column
+// weight slots (2 BN + 32 NA <= 512); the weight slots have their own
+// empty/ready barriers, decoupled from the NSTG shared-memory stages.  Warps:
+// 0-7 converters (parity w / 4 takes alternate stages), 8 MMA issuer, 9
+// loader, 10-13 epilogue (each drains its TMEM lane quarter, warp % 4).  The
+// output tile goes through one shared-memory buffer by tensor-map store.
+// ---------------------------------------------------------------------------
+constexpr int kThreadsP = kThreads + 128;
+
+template <int BN, int NSTG, int NA>
+struct SmemP {
+    static constexpr uint32_t kTileB = BN * 128;
+    static constexpr uint32_t kStage = kTileB + kRawA;  // multiple of 1024
+    static constexpr uint32_t kOutOff = NSTG * kStage;
+    static constexpr uint32_t kBarOff = kOutOff + BN * 256;
+    static constexpr uint32_t kFactOff = kBarOff + 512;          // s_f[2][256]
+    static constexpr uint32_t kBytes = kFactOff + 2048 + 1024 /*align*/;
+    static constexpr uint32_t kACol = 2 * BN;
+    static_assert(2 * BN + 32 * NA <= 512, "two accumulators and the weight ring fit in TMEM");
+    // the second accumulator (and every weight slot) starts on a 32-column
+    // boundary: with BN = 176 (second accumulator at column 176) the kernel
+    // faulted the GPU, BN = 128 and 160 ran exact
+    static_assert(BN % 32 == 0, "TMEM operands start on 32-column boundaries");
+    static_assert(kBytes <= 227 * 1024, "shared memory per CTA");
+    static_assert(8 * (2 * NSTG + 2 * NA + 5) + sizeof(int) * 3 <= 512, "barriers and control words");
+};
+
+template <int BN, int NSTG, int NA>
+__global__ void __launch_bounds__(kThreadsP, 1)
+    gemm16p_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap wmap,
+                   const __grid_constant__ CUtensorMap omap, const float *__restrict__ tok_scale,
+                   const float *__restrict__ gamma, int M, int N, int KT, int RGN, int row_tiles, int tiles,
+                   uint32_t wait_limit) {
+    using L = SmemP<BN, NSTG, NA>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
+    uint64_t *full = bars, *empty = bars + NSTG, *a_ready = bars + 2 * NSTG, *a_empty = bars + 2 * NSTG + NA;
+    uint64_t *acc_full = bars + 2 * NSTG + 2 * NA, *acc_empty = acc_full + 2, *mma_done = acc_full + 4;
+    Ctl *ctl = reinterpret_cast<Ctl *>(mma_done + 1);
+    volatile int *abort = &ctl->abort;
+    float *s_f = reinterpret_cast<float *>(smem + L::kFactOff);  // [2][256]
+
+    pdl_launch_dependents();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int NS = 2 * KT;
+    bool timed_out = false;
+    if (tid == 0) {
+        ctl->issued = 0;
+        ctl->abort = 0;
+        for (int i = 0; i < NSTG; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < NA; ++i) {
+            mbar_init(&a_ready[i], kConverters / 2);
+            mbar_init(&a_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], 128);
+        }
+        mbar_init(mma_done, 1);
+        mbar_fence_init();
+    }
+    if (warp == 8) {
+        tmem_alloc(&ctl->tmem, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem;
+
+    if (warp == 9) {
+        // ---------------- loader ----------------
+        if (lane == 0) {
+            bool waited = false, stop = false;
+            int g = 0;
+            for (int t = blockIdx.x; t < tiles && !stop; t += gridDim.x) {
+                const int rg0 = (t % row_tiles) * 8, tok0 = (t / row_tiles) * BN;
+                for (int j = 0; j < NS; ++j, ++g) {
+                    const int s = g % NSTG;
+                    if (!mbar_wait_abortable(&empty[s], ((g / NSTG) & 1) ^ 1, wait_limit, abort)) {
+                        timed_out = stop = true;
+                        break;
+                    }
+                    uint8_t *stage = smem + s * L::kStage;
+                    mbar_arrive_expect_tx(&full[s], L::kStage);
+                    tma_load_w8(stage + L::kTileB, &wmap, j & 1, j >> 1, rg0, &full[s]);
+                    if (!waited) {
+                        pdl_wait();
+                        waited = true;
+                    }
+                    tma_load_2d(stage, &qmap, j * 64, tok0, &full[s]);
+                    ctl->issued = g + 1;
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp < 8) {
+        // ---------------- converters ----------------
+        const int row = 32 * (warp & 3) + lane;
+        const int ri = row & 15, rgl = row >> 4, par = warp >> 2;
+        const uint32_t a_lane = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+        bool stop = false;
+        int g = 0;
+        for (int t = blockIdx.x; t < tiles && !stop; t += gridDim.x) {
+            const int rg0 = (t % row_tiles) * 8;
+            const bool row_ok = rgl < RGN - rg0;
+            for (int j = 0; j < NS; ++j, ++g) {
+                if ((g & 1) != par) continue;
+                const int s = g % NSTG, a = g % NA;
+                if (!mbar_wait_abortable_warp(&full[s], (g / NSTG) & 1, wait_limit, abort) ||
+                    !mbar_wait_abortable_warp(&a_empty[a], ((g / NA) & 1) ^ 1, wait_limit, abort)) {
+                    timed_out = stop = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint8_t *codes = smem + s * L::kStage + L::kTileB;
+#pragma unroll
+                for (int t2 = 0; t2 < 2; ++t2) {
+                    uint32_t w0, w1, f[16];
+                    load_codes(codes, rgl, ri, t2, row_ok, w0, w1);
+                    expand_codes(w0, w1, f);
+                    tc_st16(tmem + a_lane + L::kACol + 32 * a + 16 * t2, f);
+                }
+                tc_wait_st();
+                tc_fence_before();
+                mbar_arrive(&a_ready[a]);
+            }
+        }
+    } else if (warp == 8) {
+        // ---------------- MMA issuer ----------------
+        constexpr uint32_t idesc = idesc_f16_f32(128, BN);
+        const uint32_t base = smem_addr(smem);
+        bool stop = false;
+        int g = 0, i = 0;
+        for (int t = blockIdx.x; t < tiles && !stop; t += gridDim.x, ++i) {
+            const int b = i & 1;
+            if (!mbar_wait_abortable_warp(&acc_empty[b], ((i >> 1) & 1) ^ 1, wait_limit, abort)) {
+                timed_out = true;
+                break;
+            }
+            tc_fence_after();
+            for (int j = 0; j < NS; ++j, ++g) {
+                const int s = g % NSTG, a = g % NA;
+                if (!mbar_wait_abortable_warp(&full[s], (g / NSTG) & 1, wait_limit, abort) ||
+                    !mbar_wait_abortable_warp(&a_ready[a], (g / NA) & 1, wait_limit, abort)) {
+                    timed_out = stop = true;
+                    break;
+                }
+                tc_fence_after();
+                if (elect_one()) {
+                    const uint64_t bd = sw128_desc(base + s * L::kStage);
+                    const uint32_t at = tmem + L::kACol + 32 * a;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma_f16_ta(tmem + b * BN, at + 8 * kk, bd + 2 * kk, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(&empty[s]);
+                    tc_commit(&a_empty[a]);
+                }
+                __syncwarp();
+            }
+            if (stop) break;
+            if (elect_one()) tc_commit(&acc_full[b]);
+            __syncwarp();
+        }
+        if (elect_one()) tc_commit(mma_done);
+        __syncwarp();
+    } else {
+        // ---------------- epilogue (warps 10-13) ----------------
+        // a warp reaches only the TMEM lane quarter warp % 4 (warps 10-13:
+        // quarters 2, 3, 0, 1)
+        const int ew = warp & 3, etid = tid - 10 * 32, r = 32 * ew + lane;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * ew) << 16);
+        __nv_bfloat16 *ob = reinterpret_cast<__nv_bfloat16 *>(smem + L::kOutOff);
+        pdl_wait();  // the token scales come from an earlier kernel
+        const float gam = *gamma;
+        int i = 0;
+        for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+            const int b = i & 1, rt = t % row_tiles, tok0 = (t / row_tiles) * BN;
+            float *f = s_f + 256 * b;
+            for (int c = etid; c < BN; c += 128) f[c] = tok0 + c < M ? __fmul_rn(gam, tok_scale[tok0 + c]) : 0.0f;
+            bool have = mbar_wait_abortable_warp(&acc_full[b], (i >> 1) & 1, wait_limit, abort);
+            if (etid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // the buffer is free
+            have = bar_and(2, 128, have);  // also publishes f[] and the free buffer to all four warps
+            if (!have) {
+                timed_out = true;
+                break;
+            }
+            tc_fence_after();
+#pragma unroll 1
+            for (int col = 0; col < BN; col += 32) {
+                uint32_t v[32];
+                tc_ld16(lane_base + b * BN + col, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                tc_ld16(lane_base + b * BN + col + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                tc_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 32; k += 2) {
+                    const int c = col + k;
+                    const __nv_bfloat162 o = rescale2(__uint_as_float(v[k]), f[c], __uint_as_float(v[k + 1]), f[c + 1]);
+                    ob[c * 128 + r] = o.x;
+                    ob[(c + 1) * 128 + r] = o.y;
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&acc_empty[b]);  // the accumulator is read: the MMA may refill it
+            fence_proxy_async_smem();
+            asm volatile("bar.sync 2, 128;" ::: "memory");
+            if (etid == 0) {
+                tma_store_2d(&omap, ob, rt * 128, tok0);
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            }
+        }
+        if (etid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    }
+
+    if (timed_out) atomicOr(&g_gemm_status, 1u);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 8) {
+        if (lane == 0) {
+            mbar_wait_bounded(mma_done, 0, kDrainLimit);
+            const int n = ctl->issued;
+            for (int g = n > NSTG ? n - NSTG : 0; g < n; ++g)
+                mbar_wait_bounded(&full[g % NSTG], (g / NSTG) & 1, kDrainLimit);
+        }
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
 // ------------------------------------------------------------------ host ---
 
 std::mutex g_encode_mutex;
@@ -934,6 +1173,51 @@ cudaError_t launch_family(Fam &fam, int BN, const void *q, bool f16, const float
                       staged, tok_scale, gamma, M, N, KT, RGN, out, acc_out, wait_limit);
 }
 
+// The persistent f16-operand GEMM: one CTA per SM over all tiles.
+template <int BN, int NSTG, int NA>
+cudaError_t launch_persistent(const void *q16, const float *tok_scale, const uint8_t *packed, const float *gamma,
+                              int M, int N, int K, __nv_bfloat16 *out, cudaStream_t st, uint32_t wait_limit) {
+    using L = SmemP<BN, NSTG, NA>;
+    const int KT = (K + 127) / 128, RGN = (N + 15) / 16;
+    const int row_tiles = (RGN + 7) / 8, tiles = row_tiles * ((M + BN - 1) / BN);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    {
+        static bool configured[64] = {false};
+        std::lock_guard<std::mutex> lock(g_family_mutex);
+        if (!configured[dev]) {
+            e = cudaFuncSetAttribute(gemm16p_kernel<BN, NSTG, NA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(L::kBytes));
+            if (e != cudaSuccess) return e;
+            configured[dev] = true;
+        }
+    }
+    CUtensorMap qmap, wmap, omap;
+    e = make_qmap(&qmap, q16, M, K, BN, true);
+    if (e == cudaSuccess) e = make_wmap(&wmap, packed, RGN, KT);
+    if (e == cudaSuccess) e = make_omap(&omap, out, M, N, BN, false);
+    if (e != cudaSuccess) return e;
+    const int sms = device_sms(dev);
+    const int grid = tiles < sms ? tiles : sms;
+    return launch_pdl(gemm16p_kernel<BN, NSTG, NA>, dim3(grid), dim3(kThreadsP), L::kBytes, st, 1, qmap, wmap, omap,
+                      tok_scale, gamma, M, N, KT, RGN, row_tiles, tiles, wait_limit);
+}
+
+// Whether the persistent kernel (token tile 192) runs.  Measured with f16
+// operands on the 2B shapes (TFLOP/s, one tile per CTA -> persistent):
+// 2560x2560 at 4096 tokens 1048 -> 1121, at 2048 790 -> 790; 2560x6912 at
+// 4096 1296 -> 1245; 6912x2560 at 4096 1268 -> 1126 (192) / 926 (128).  It
+// pays where the tiles are the one-tile plan's (token tile 192 there too)
+// and the main loop is short against the epilogue it hides (K <= 4096);
+// elsewhere the one-tile kernel's stage rate wins.
+bool use_persistent(int M, int N, int K, int sms, int one_tile_bn) {
+    if (one_tile_bn != 192 || K > 4096) return false;
+    const int64_t tiles = static_cast<int64_t>((N + 127) / 128) * ((M + 191) / 192);
+    return tiles > sms;
+}
+
 }  // namespace
 
 // Token tile (MMA N) above 128 tokens, one CTA per SM holding a 128-row x
@@ -957,6 +1241,14 @@ int token_tile(int M, int N) {
 cudaError_t launch_gemm16(const void *q16, const float *tok_scale, const uint8_t *packed, const float *gamma, int M,
                           int N, int K, __nv_bfloat16 *out, int32_t *acc_out, cudaStream_t st, uint32_t wait_limit,
                           int split) {
+    // More tiles than SMs, bf16 rows of whole 16-byte units, no int32 copy
+    // wanted, no forced split: the persistent kernel.
+    if (!acc_out && (N % 8) == 0 && split <= 1 && M > 128) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+        if (use_persistent(M, N, K, device_sms(dev), token_tile(M, N)))
+            return launch_persistent<192, 6, 4>(q16, tok_scale, packed, gamma, M, N, K, out, st, wait_limit);
+    }
     if (M <= 64)
         return launch_family(family16<64, 10>(), 64, q16, true, tok_scale, packed, gamma, M, N, K, out, acc_out, st,
                              wait_limit, split);
