@@ -58,9 +58,11 @@ M_LIST = (1, 4, 16)
 LAYERS = 20
 FALLBACK_HBM_GBS = 6400.0
 FALLBACK_BF16_TFLOPS = 1800.0
-# DRAM bytes per packed-weight byte of the fused decode kernel, from an ncu
-# capture of its launches (profiles/), or None when the kernel changed since.
-FUSED_DRAM_PER_PACKED_BYTE = None
+# DRAM bytes (read + write) per packed-weight byte of the fused decode
+# kernel over the step's 240 launches, from an ncu capture of this kernel
+# (profiles/fused_gemv_decode_2b_dram_traffic.md); None once the kernel
+# changes after the capture.
+FUSED_DRAM_PER_PACKED_BYTE = 1.0209
 
 
 def peaks():
