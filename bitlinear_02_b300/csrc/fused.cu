@@ -117,66 +117,48 @@ __device__ __forceinline__ void token_factors(float mx, float ss, int K, float e
 }
 
 // Factors of tokens [0, M) of a factor buffer, by a CTA of 4 warps, into
-// c_out / ts_out (shared memory), in two parts so that a caller can issue
-// other loads between them.  factor_loads issues every load at once, whether
-// the buffer is pending or published (one round trip): the state word, the
+// c_out / ts_out (shared memory).  Every load is issued at once, whether the
+// buffer is pending or published (one round trip): the state word, the
 // published factors, and the 16 copies of each token's accumulator.  Warp w
 // takes token pairs w and w + 4: lanes 0-15 hold the copies of token 2p,
-// lanes 16-31 those of token 2p+1.  factor_reduce reduces max and the
-// compensated sum in a fixed butterfly, so every CTA and every caller gets
-// the same bits, and returns whether the buffer was pending.
-struct FactorLoads {
-    float mx[2], hi[2], pub_c, pub_ts;
-    int tk[2];
-    bool pend;
-};
-
-__device__ __forceinline__ FactorLoads factor_loads(const float *xs, int M) {
+// lanes 16-31 those of token 2p+1; max and the compensated sum are reduced in
+// a fixed butterfly, so every CTA and every caller gets the same bits.
+// Returns whether the buffer was pending.
+__device__ __forceinline__ bool cta_factors(const float *xs, int M, int K, float eps, float *c_out,
+                                            float *ts_out) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cp = lane & 15;
-    FactorLoads f;
+    float mx[2], hi[2], lo[2] = {0.0f, 0.0f};
+    int tk[2];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-        f.tk[r] = 2 * (warp + 4 * r) + (lane >> 4);
-        const bool ok = f.tk[r] < M;
-        f.mx[r] = ok ? ld_cg_f32(xs + kOffMax + cp * 16 + f.tk[r]) : 0.0f;
-        f.hi[r] = ok ? ld_cg_f32(xs + kOffSum + cp * 16 + f.tk[r]) : 0.0f;
+        tk[r] = 2 * (warp + 4 * r) + (lane >> 4);
+        const bool ok = tk[r] < M;
+        mx[r] = ok ? ld_cg_f32(xs + kOffMax + cp * 16 + tk[r]) : 0.0f;
+        hi[r] = ok ? ld_cg_f32(xs + kOffSum + cp * 16 + tk[r]) : 0.0f;
     }
-    f.pend = ld_cg_u32(xs + kOffState) == kPending;
-    f.pub_c = lane < 16 ? ld_cg_f32(xs + kOffC + lane) : 0.0f;
-    f.pub_ts = lane < 16 ? ld_cg_f32(xs + kOffTs + lane) : 0.0f;
-    return f;
-}
-
-__device__ __forceinline__ bool factor_reduce(FactorLoads f, int M, int K, float eps, float *c_out, float *ts_out) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int cp = lane & 15;
-    float lo[2] = {0.0f, 0.0f};
-    if (f.pend) {
+    const bool pend = ld_cg_u32(xs + kOffState) == kPending;
+    const float pub_c = lane < 16 ? ld_cg_f32(xs + kOffC + lane) : 0.0f;
+    const float pub_ts = lane < 16 ? ld_cg_f32(xs + kOffTs + lane) : 0.0f;
+    if (pend) {
 #pragma unroll
         for (int off = 8; off > 0; off >>= 1) {
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-                f.mx[r] = fmaxf(f.mx[r], __shfl_xor_sync(0xffffffffu, f.mx[r], off));
-                const float oh = __shfl_xor_sync(0xffffffffu, f.hi[r], off);
+                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], off));
+                const float oh = __shfl_xor_sync(0xffffffffu, hi[r], off);
                 const float ol = __shfl_xor_sync(0xffffffffu, lo[r], off);
-                ff_add(f.hi[r], lo[r], oh, ol);
+                ff_add(hi[r], lo[r], oh, ol);
             }
         }
 #pragma unroll
         for (int r = 0; r < 2; ++r)
-            if (cp == 0 && f.tk[r] < M)
-                token_factors(f.mx[r], __fadd_rn(f.hi[r], lo[r]), K, eps, c_out[f.tk[r]], ts_out[f.tk[r]]);
+            if (cp == 0 && tk[r] < M) token_factors(mx[r], __fadd_rn(hi[r], lo[r]), K, eps, c_out[tk[r]], ts_out[tk[r]]);
     } else if (warp == 0 && lane < 16) {
-        c_out[lane] = f.pub_c;
-        ts_out[lane] = f.pub_ts;
+        c_out[lane] = pub_c;
+        ts_out[lane] = pub_ts;
     }
-    return f.pend;
-}
-
-__device__ __forceinline__ bool cta_factors(const float *xs, int M, int K, float eps, float *c_out,
-                                            float *ts_out) {
-    return factor_reduce(factor_loads(xs, M), M, K, eps, c_out, ts_out);
+    return pend;
 }
 
 template <int NT>
@@ -259,14 +241,12 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 3) fused_gemv_kerne
     }
     const float gam = *P.gamma;  // static, like the weights
     pdl_wait();  // the input and its factors come from earlier kernels
-    // The input's factors (from its pending accumulator, or as published):
-    // their loads go out first, ahead of the input tiles, since the factors
-    // gate the whole CTA at the barrier below.
-    const FactorLoads fl = factor_loads(A.xs, M);
     load_x(SA, c);
     load_x(SB, c + kWarps);
+
+    // The input's factors: from its pending accumulator, or as published.
     unsigned *const xs_u = reinterpret_cast<unsigned *>(A.xs);
-    const bool pend = factor_reduce(fl, M, K, A.eps, s_c, s_ts);
+    const bool pend = cta_factors(A.xs, M, K, A.eps, s_c, s_ts);
     // This launch produces into P.stats: mark it pending (once per buffer).
     if (P.stats != nullptr && rbl == 0 && s == 0 && threadIdx.x == 0) {
         unsigned *const st = reinterpret_cast<unsigned *>(P.stats) + kOffState;
@@ -341,45 +321,29 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 3) fused_gemv_kerne
         __syncthreads();
     }
     float *vals = reinterpret_cast<float *>(&part[0][0][0]);  // bf16 outputs as floats, by entry
-    // Up to 4 entries per thread at a time, with every slice's total of all
-    // of them (this CTA's own included) in flight at once: one round trip to
-    // the peers' shared memory per 4 entries instead of per entry.
-    constexpr int kBatch = 4;
-    for (int eb = e0 + static_cast<int>(threadIdx.x); eb < e1; eb += kBatch * kWarps * 32) {
-        int pv[kBatch][8];
+    for (int e = e0 + static_cast<int>(threadIdx.x); e < e1; e += kWarps * 32) {
+        int v = total[e];
+        if (S > 1) {
+            // every slice's total (this CTA's own included), all loads in flight at once
+            const uint32_t la = smem_addr(&total[e]);
+            int pv[8];
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int e = eb + u * kWarps * 32;
-            const bool live = e < e1;
-            if (S > 1) {
-                const uint32_t la = smem_addr(&total[live ? e : e0]);
+            for (int r = 0; r < 8; ++r) pv[r] = r < S ? ld_cluster_s32(cluster_map(la, r)) : 0;
+            v = 0;
 #pragma unroll
-                for (int r = 0; r < 8; ++r) pv[u][r] = (live && r < S) ? ld_cluster_s32(cluster_map(la, r)) : 0;
-            } else {
-                pv[u][0] = live ? total[e] : 0;
-#pragma unroll
-                for (int r = 1; r < 8; ++r) pv[u][r] = 0;
-            }
+            for (int r = 0; r < 8; ++r) v += pv[r];
         }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int e = eb + u * kWarps * 32;
-            if (e >= e1) break;
-            int v = 0;
-#pragma unroll
-            for (int r = 0; r < 8; ++r) v += pv[u][r];
-            const int tk = e / kRows, rr = e % kRows;
-            const int n = rbl * kRows + rr;
-            float vf = 0.0f;
-            if (n < P.N) {
-                const float f = __fmul_rn(gam, s_ts[tk]);
-                const __nv_bfloat16 o = __float2bfloat16_rn(__fmul_rn(static_cast<float>(v), f));
-                P.out[static_cast<int64_t>(tk) * P.N + n] = o;
-                if (P.acc_out) P.acc_out[static_cast<int64_t>(tk) * P.N + n] = v;
-                vf = __bfloat162float(o);
-            }
-            vals[e] = vf;
+        const int tk = e / kRows, rr = e % kRows;
+        const int n = rbl * kRows + rr;
+        float vf = 0.0f;
+        if (n < P.N) {
+            const float f = __fmul_rn(gam, s_ts[tk]);
+            const __nv_bfloat16 o = __float2bfloat16_rn(__fmul_rn(static_cast<float>(v), f));
+            P.out[static_cast<int64_t>(tk) * P.N + n] = o;
+            if (P.acc_out) P.acc_out[static_cast<int64_t>(tk) * P.N + n] = v;
+            vf = __bfloat162float(o);
         }
+        vals[e] = vf;
     }
     if (S > 1) cluster_sync();  // peers have read this CTA's totals; vals complete
     else __syncthreads();
