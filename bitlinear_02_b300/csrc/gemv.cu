@@ -202,7 +202,12 @@ cudaError_t launch_gemv(const int8_t *q, const float *tok_scale, const uint8_t *
     const int RGN = (N + 15) / 16;
     const int RB = (RGN + kGroups - 1) / kGroups;
     const int Z = (M + 15) / 16;  // 16-token chunks (M <= 64)
+    // about two CTAs per SM, but never more than fit at once (4 per SM for
+    // the 8-token kernel, 3 for the 16-token one at 168 registers): a second
+    // wave cost up to 1.6x (3B gate/up at 32 tokens: 16.9 -> 10.3 us)
+    const int cap = ((M <= 8 ? 4 : 3) * num_sms) / (RB * Z);
     int S = (2 * num_sms + RB * Z - 1) / (RB * Z);
+    if (S > cap) S = cap;
     const int smax = KT / kWarps > 1 ? KT / kWarps : 1;
     if (S > smax) S = smax;
     if (S > 8) S = 8;
