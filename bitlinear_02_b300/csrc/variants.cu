@@ -396,7 +396,11 @@ cudaError_t launch_variant(const int8_t *q, const float *tok_scale, const uint8_
     const int RGN = (N + 15) / 16;
     const int RB = (RGN + kGroups - 1) / kGroups;
     const int Z = (M + 15) / 16;
+    // about two CTAs per SM, never more than fit at once (these kernels hold
+    // 127-168 registers a thread: 3 CTAs per SM)
+    const int cap = (3 * num_sms) / (RB * Z);
     int S = (2 * num_sms + RB * Z - 1) / (RB * Z);
+    if (S > cap) S = cap;
     const int smax = KT / kWarps > 1 ? KT / kWarps : 1;
     if (S > smax) S = smax;
     if (S > 8) S = 8;
