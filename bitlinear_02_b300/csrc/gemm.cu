@@ -1327,15 +1327,17 @@ cudaError_t widen_alloc(void **p, size_t bytes, cudaStream_t st) {
 }  // namespace
 
 // bitlinear_forward widens the int8 activations to f16 once (one pass over
-// M x K) and runs the f16-operand GEMM above 256 tokens, and above 64 for
-// matrices of at least 2^24 weights: in the int8 engine every row-tile CTA
+// M x K) and runs the f16-operand GEMM above 256 tokens, and above 48 for
+// matrices of at least 2^24 weights (at 49-64 tokens the f16-operand GEMM
+// takes 84 against 104 us on 28672x8192, 72 against 94 on 8192x28672): in
+// the int8 engine every row-tile CTA
 // converts the same activation tile again (20-224 times for the 2B-70B
 // shapes), which held it at 0.43 of the bf16 peak against 0.67 for f16
 // operands at 4096 tokens, and cost 30-55 % at 65-256 tokens on the 2B
 // gate/up and down matrices (measured; the 2560x2560 ones gain nothing
 // there, the extra launch eats the saving).
 bool widen_first(int M, int N, int K) {
-    return M > 256 || (M > 64 && static_cast<int64_t>(N) * K >= (1ll << 24));
+    return M > 256 || (M > 48 && static_cast<int64_t>(N) * K >= (1ll << 24));
 }
 
 cudaError_t launch_gemm(const int8_t *q, const float *tok_scale, const uint8_t *packed, const float *gamma, int M,

@@ -197,7 +197,7 @@ BITLINEAR_API bitlinear_status_t bitlinear_quant_act(const void *x_bf16, const v
  * (legacy tensor MMA on register-unpacked codes; above 16 tokens in 16-token
  * chunks of one launch); otherwise the tcgen05 GEMM (TMEM accumulators),
  * with its K range split across a cluster where the output tiles alone
- * would leave most SMs idle.  Above 256 tokens, and above 64 for matrices
+ * would leave most SMs idle.  Above 256 tokens, and above 48 for matrices
  * of at least 2^24 weights, the int8 activations are first widened to f16
  * (exact) into a buffer taken, stream-ordered, from a
  * memory pool the library keeps per device (M*K*2 bytes, returned to the
