@@ -101,11 +101,13 @@ def load_library():
     L.bitlinear_forward_fused.argtypes = [P, P, I64, I64, ctypes.c_int32, ctypes.POINTER(FusedProj), F, P]
     L.bitlinear_fused_factors.argtypes = [P, I64, I64, F, ctypes.c_int32, P, P, P]
     L.bitlinear_forward_f16.argtypes = [P, P, P, P, I64, I64, I64, P, P, P]
+    L.bitlinear_set_fused_prepass.argtypes = [I64]
     for name in ("bitlinear_pack_weights", "bitlinear_pack_weights_noalloc", "bitlinear_pack_ternary", "bitlinear_quant_act",
                  "bitlinear_forward", "bitlinear_check_status",
                  "bitlinear_quant_act_f16", "bitlinear_forward_f16", "bitlinear_act_stats",
                  "bitlinear_forward_fused", "bitlinear_fused_factors", "bitlinear_set_engine",
-                 "bitlinear_repack5", "bitlinear_forward5", "bitlinear_pack_binary", "bitlinear_forward_binary"):
+                 "bitlinear_repack5", "bitlinear_forward5", "bitlinear_pack_binary", "bitlinear_forward_binary",
+                 "bitlinear_set_fused_prepass"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -278,6 +280,11 @@ def bitlinear_forward_binary(q, tok_scale, packed1, beta, groups: int, M: int, N
                                                    int(groups), int(M), int(N), int(K), _ptr(out), _ptr(acc_out),
                                                    _stream(stream)),
            "bitlinear_forward_binary")
+
+
+def bitlinear_set_fused_prepass(min_weight_bytes: int = -1) -> None:
+    """Pre-pass threshold of bitlinear_forward_fused (-1 restores the default)."""
+    _check(load_library().bitlinear_set_fused_prepass(int(min_weight_bytes)), "bitlinear_set_fused_prepass")
 
 
 def bitlinear_set_engine(gemv_max_tokens: int = -1, split_k: int = 0) -> None:

@@ -27,8 +27,18 @@
 // path; the token scale agrees to about 1e-7.
 #include "decode_math.cuh"
 
+#include <atomic>
+
 namespace bl {
 cudaError_t status_word(unsigned int **dev_ptr);  // gemm.cu: the library's device status word
+cudaError_t scratch_alloc(void **p, size_t bytes, cudaStream_t st);  // gemm.cu: stream-ordered scratch
+
+// Launches of at least this many packed weight bytes quantise their input
+// in a pre-pass (bitlinear_set_fused_prepass; -1: this default).  Measured
+// on the 70B shapes at one token: gate+up (117 MB) and down (58.7 MB) gain
+// 5-8 us each; q+k+v (21 MB) and o (16.8 MB) lose the extra launch.
+constexpr int64_t kPrepassDefault = 32ll << 20;
+std::atomic<int64_t> g_prepass_min{-1};
 namespace {
 
 constexpr int kWarps = 4;
@@ -58,10 +68,12 @@ struct FProj {
 
 struct FArgs {
     const __nv_bfloat16 *x;
+    const int8_t *q;  // the input quantised by fused_quant_kernel (large launches), else unused
     float *xs;  // factor buffer of the input (consumed)
     unsigned int *status;
     FProj p[kMaxFused];
     int nproj, M, K, KT, tiles_per_cta;
+    int prefetch;  // bulk L2 prefetch of the weights past the register stages
     float eps;
 };
 
@@ -161,7 +173,9 @@ __device__ __forceinline__ bool cta_factors(const float *xs, int M, int K, float
     return pend;
 }
 
-template <int NT>
+// kQ: the input comes quantised (A.q, int8) from fused_quant_kernel instead
+// of as bf16 to quantise here.
+template <int NT, bool kQ>
 __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 3) fused_gemv_kernel(const FArgs A) {
     __shared__ int32_t part[kWarps][NT * 8][kRows];
     __shared__ int32_t total[NT * 8 * kRows];
@@ -181,20 +195,34 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 3) fused_gemv_kerne
     const int c_begin = s * A.tiles_per_cta;
     const int c_end = min(KT, c_begin + A.tiles_per_cta);
 
+    // Weight loads are clamped to the last row group instead of predicated
+    // (its outputs are not stored); the input loads stay predicated
+    // (clamping them measured 4 % slower at 16 tokens).
     auto load_w = [&](Stage<NT> &st, int c) {
         if (c >= c_end) return;
 #pragma unroll
         for (int i = 0; i < kGroups; ++i) {
-            const int rg = rbl * kGroups + i;
-            if (rg < P.RGN)
-                st.w[i] = ld_stream16(P.packed + (static_cast<int64_t>(rg) * KT + c) * 512 + lane * 16);
-            else
-                st.w[i] = make_uint4(0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u);
+            const int rg = min(rbl * kGroups + i, P.RGN - 1);
+            st.w[i] = ld_stream16(P.packed + (static_cast<int64_t>(rg) * KT + c) * 512 + lane * 16);
         }
     };
     auto load_x = [&](Stage<NT> &st, int c) {
         if (c >= c_end) return;
         const int k0 = c * 128 + t * 32;
+        if (kQ) {
+            // 32 int8 values per lane, clamped like the decode GEMV's large
+            // matrices: a token past M reads token M-1 (not stored), k past K
+            // rereads the row's last 16 values against padding codes c = 1,
+            // which add 1*q to the MMA sum and q to sum(q): nothing.
+            const int ka = min(k0, K - 16), kb = min(k0 + 16, K - 16);
+#pragma unroll
+            for (int jj = 0; jj < NT; ++jj) {
+                const int8_t *src = A.q + static_cast<int64_t>(min(8 * jj + g, M - 1)) * K;
+                st.x[jj][0] = ld_ro16(src + ka);
+                st.x[jj][1] = ld_ro16(src + kb);
+            }
+            return;
+        }
 #pragma unroll
         for (int jj = 0; jj < NT; ++jj) {
             const int tok = 8 * jj + g;
@@ -222,9 +250,13 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 3) fused_gemv_kerne
     auto compute = [&](const Stage<NT> &st) {
         uint32_t b[NT][8][2];
 #pragma unroll
-        for (int jj = 0; jj < NT; ++jj)
-            dm::build_b(quant16(st.x[jj][0], st.x[jj][1], cq[jj]), quant16(st.x[jj][2], st.x[jj][3], cq[jj]), b[jj],
-                        corr[jj]);
+        for (int jj = 0; jj < NT; ++jj) {
+            if (kQ)
+                dm::build_b(st.x[jj][0], st.x[jj][1], b[jj], corr[jj]);
+            else
+                dm::build_b(quant16(st.x[jj][0], st.x[jj][1], cq[jj]), quant16(st.x[jj][2], st.x[jj][3], cq[jj]),
+                            b[jj], corr[jj]);
+        }
         dm::mma_tile<NT>(st.w, b, d);
     };
 
@@ -232,8 +264,10 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 3) fused_gemv_kerne
     int c = c_begin + warp;
     load_w(SA, c);
     load_w(SB, c + kWarps);
-    // tiles past the two register stages: into L2 now, one bulk prefetch per row group
-    if (threadIdx.x < kGroups && c_end > c_begin + 2 * kWarps) {
+    // tiles past the two register stages: into L2 now, one bulk prefetch per
+    // row group - for launches of under 16 MB of weights, which it speeds up;
+    // it slows larger ones (70B down at 16 tokens: 49.4 -> 46.9 us without)
+    if (A.prefetch && threadIdx.x < kGroups && c_end > c_begin + 2 * kWarps) {
         const int rg = rbl * kGroups + static_cast<int>(threadIdx.x);
         if (rg < P.RGN)
             bulk_prefetch_l2(P.packed + (static_cast<int64_t>(rg) * KT + c_begin + 2 * kWarps) * 512,
@@ -397,6 +431,48 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 3) fused_gemv_kerne
     pdl_launch_dependents();
 }
 
+// The input of a large launch, quantised once (q = rint(x * c), the same
+// bits as the GEMV CTAs' own quantisation) into q [M, K] for
+// fused_gemv_kernel<NT, true>: quantising in every row block's CTAs costs
+// more integer work than the weights' decoding there (70B gate/up at one
+// token: 29.9 against 22 us for the GEMV on int8 input).  Consumes the input's
+// factor buffer like the GEMV CTAs do (ticket; the last CTA publishes the
+// factors and clears the accumulator), so the GEMV finds them published.
+// Its dependents may launch at once: their weight loads overlap this pass.
+__global__ void __launch_bounds__(kWarps * 32) fused_quant_kernel(const __nv_bfloat16 *__restrict__ x, float *xs,
+                                                                  int M, int K, float eps, int8_t *__restrict__ q) {
+    __shared__ float s_c[16], s_ts[16];
+    pdl_launch_dependents();
+    pdl_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    unsigned *const xs_u = reinterpret_cast<unsigned *>(xs);
+    const bool pend = cta_factors(xs, M, K, eps, s_c, s_ts);
+    __syncthreads();
+    unsigned ticket = 0u;
+    if (pend && threadIdx.x == 0) ticket = atomicAdd(xs_u + kOffTicket, 1u);
+    const int64_t n16 = static_cast<int64_t>(M) * K / 16;  // K % 16 == 0: a chunk is one token's
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int tok = static_cast<int>(i * 16 / K);
+        const uint4 *src = reinterpret_cast<const uint4 *>(x) + 2 * i;
+        reinterpret_cast<uint4 *>(q)[i] = quant16(__ldg(src), __ldg(src + 1), s_c[tok]);
+    }
+    if (pend && warp == 0) {
+        const unsigned tk0 = __shfl_sync(0xffffffffu, ticket, 0);
+        if (tk0 == gridDim.x - 1u) {
+            if (lane < M) {
+                xs[kOffC + lane] = s_c[lane];
+                xs[kOffTs + lane] = s_ts[lane];
+            }
+            for (int i = lane; i < 2 * 16 * kCopies; i += 32) xs_u[kOffMax + i] = 0u;
+            if (lane == 0) {
+                xs_u[kOffTicket] = 0u;
+                xs_u[kOffState] = 0u;
+            }
+        }
+    }
+}
+
 // Factors of an external input x [M, K]: one CTA per token.
 __global__ void __launch_bounds__(256) act_stats_kernel(const uint4 *__restrict__ x, int M, int K, float eps,
                                                         float *__restrict__ stats) {
@@ -549,6 +625,7 @@ extern "C" bitlinear_status_t bitlinear_forward_fused(const void *x_bf16, void *
         rbs = P.rb1;
     }
     if (rbs > 65535) return BITLINEAR_ERR_UNSUPPORTED;
+    A.prefetch = static_cast<int64_t>(rbs) * A.KT * 2048 < (16ll << 20);
     // every argument is checked: only now the first CUDA call
     if (status_word(&A.status) != cudaSuccess) return BITLINEAR_ERR_CUDA;
     // K split over a cluster of S CTAs (combined in distributed shared
@@ -571,7 +648,36 @@ extern "C" bitlinear_status_t bitlinear_forward_fused(const void *x_bf16, void *
         if (static_cast<int64_t>(A.p[j].rb1 - A.p[j].rb0) * S > (1 << 30)) return BITLINEAR_ERR_UNSUPPORTED;
     const dim3 grid(S, rbs), block(kWarps * 32);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const cudaError_t e = M <= 8 ? launch_pdl(fused_gemv_kernel<1>, grid, block, 0, st, S, A)
-                                 : launch_pdl(fused_gemv_kernel<2>, grid, block, 0, st, S, A);
-    return e == cudaSuccess ? BITLINEAR_OK : BITLINEAR_ERR_CUDA;
+    const int64_t wbytes = static_cast<int64_t>(rbs) * A.KT * 2048;
+    const int64_t pre_min = g_prepass_min.load();
+    if (wbytes < (pre_min >= 0 ? pre_min : kPrepassDefault)) {
+        const cudaError_t e = M <= 8 ? launch_pdl(fused_gemv_kernel<1, false>, grid, block, 0, st, S, A)
+                                     : launch_pdl(fused_gemv_kernel<2, false>, grid, block, 0, st, S, A);
+        return e == cudaSuccess ? BITLINEAR_OK : BITLINEAR_ERR_CUDA;
+    }
+    // Large launch: quantise the input once, then the GEMV on int8 input.
+    void *qs = nullptr;
+    cudaError_t e = scratch_alloc(&qs, static_cast<size_t>(M) * K, st);
+    if (e != cudaSuccess) {
+        cudaGetLastError();  // a failed allocation is this call's error, not the caller's next one
+        return BITLINEAR_ERR_CUDA;
+    }
+    const int64_t n16 = M * K / 16;
+    int64_t blocks = (n16 + kWarps * 32 - 1) / (kWarps * 32);
+    if (blocks > 2 * sms) blocks = 2 * sms;
+    e = launch_pdl(fused_quant_kernel, dim3(static_cast<unsigned>(blocks)), block, 0, st, 1, A.x, A.xs, A.M, A.K,
+                   A.eps, static_cast<int8_t *>(qs));
+    if (e == cudaSuccess) {
+        A.q = static_cast<const int8_t *>(qs);
+        e = M <= 8 ? launch_pdl(fused_gemv_kernel<1, true>, grid, block, 0, st, S, A)
+                   : launch_pdl(fused_gemv_kernel<2, true>, grid, block, 0, st, S, A);
+    }
+    const cudaError_t ef = cudaFreeAsync(qs, st);
+    return (e == cudaSuccess && ef == cudaSuccess) ? BITLINEAR_OK : BITLINEAR_ERR_CUDA;
+}
+
+extern "C" bitlinear_status_t bitlinear_set_fused_prepass(int64_t min_weight_bytes) {
+    if (min_weight_bytes < -1) return BITLINEAR_ERR_INVALID_ARG;
+    bl::g_prepass_min.store(min_weight_bytes);
+    return BITLINEAR_OK;
 }

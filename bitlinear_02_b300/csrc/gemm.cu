@@ -1326,6 +1326,10 @@ cudaError_t widen_alloc(void **p, size_t bytes, cudaStream_t st) {
 
 }  // namespace
 
+// Stream-ordered scratch memory for the other engines (the fused decode
+// path's quantised input).
+cudaError_t scratch_alloc(void **p, size_t bytes, cudaStream_t st) { return widen_alloc(p, bytes, st); }
+
 // bitlinear_forward widens the int8 activations to f16 once (one pass over
 // M x K) and runs the f16-operand GEMM above 256 tokens, and above 48 for
 // matrices of at least 2^24 weights (at 49-64 tokens the f16-operand GEMM

@@ -41,8 +41,8 @@ struct Stage {
     uint4 q[NT][2];    // 32 activation bytes per 8-token tile
 };
 
-template <int NT>
-__global__ void __launch_bounds__(kWarps * 32, 3)
+template <int NT, bool kClamp>
+__global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 3)
     gemv_kernel(const int8_t *__restrict__ q, const float *__restrict__ tok_scale,
                 const uint8_t *__restrict__ packed, const float *__restrict__ gamma, int M, int N,
                 int K, int KT, int RGN, int tiles_per_cta, __nv_bfloat16 *__restrict__ out,
@@ -67,26 +67,59 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
     const int c_begin = s * tiles_per_cta;
     const int c_end = min(KT, c_begin + tiles_per_cta);
 
+    // Large matrices (kClamp): loads are clamped into the buffers instead
+    // of predicated, from row pointers set once (no fill values or address
+    // arithmetic per stage; 70B gate/up and down at one token: 23.6 -> 21.9
+    // and 23.8 -> 21.5 us).  What they read at the edges cannot change a
+    // stored result: a row group past the matrix reads the last one, a token
+    // past M reads token M-1, and neither is stored; k past K (in the last
+    // 128-k tile) rereads the row's last 16 bytes, and since the weight codes
+    // there are padding (c = 1, weight 0) those bytes add 1*q to the MMA sum
+    // and the same q to sum(q): nothing to the result.  Small matrices keep
+    // the predicated loads, which start a few cycles sooner (the 512 x 256
+    // layer: 4.05 against 4.14 us).
+    const uint8_t *wrow[kGroups];
+    const int8_t *qrow[NT];
+    if (kClamp) {
+#pragma unroll
+        for (int i = 0; i < kGroups; ++i)
+            wrow[i] = packed + static_cast<int64_t>(min(rb * kGroups + i, RGN - 1)) * KT * 512 + lane * 16;
+#pragma unroll
+        for (int j = 0; j < NT; ++j) qrow[j] = q + static_cast<int64_t>(min(8 * j + g, M - 1)) * K;
+    }
     auto load_w = [&](Stage<NT> &st, int c) {
         if (c >= c_end) return;
 #pragma unroll
         for (int i = 0; i < kGroups; ++i) {
-            const int rg = rb * kGroups + i;
-            if (rg < RGN)
-                st.w[i] = ld_stream16(packed + (static_cast<int64_t>(rg) * KT + c) * 512 + lane * 16);
-            else
-                st.w[i] = make_uint4(0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u);
+            if (kClamp) {
+                st.w[i] = ld_stream16(wrow[i] + c * 512);
+            } else {
+                const int rg = rb * kGroups + i;
+                if (rg < RGN)
+                    st.w[i] = ld_stream16(packed + (static_cast<int64_t>(rg) * KT + c) * 512 + lane * 16);
+                else
+                    st.w[i] = make_uint4(0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u);
+            }
         }
     };
     auto load_q = [&](Stage<NT> &st, int c) {
         if (c >= c_end) return;
         const int k0 = c * 128 + t * 32;
+        if (kClamp) {
+            const int ka = min(k0, K - 16), kb = min(k0 + 16, K - 16);
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            const int tok = 8 * j + g;
-            const int8_t *src = q + static_cast<int64_t>(tok) * K + k0;
-            st.q[j][0] = (tok < M && k0 < K) ? ld_ro16(src) : make_uint4(0, 0, 0, 0);
-            st.q[j][1] = (tok < M && k0 + 16 < K) ? ld_ro16(src + 16) : make_uint4(0, 0, 0, 0);
+            for (int j = 0; j < NT; ++j) {
+                st.q[j][0] = ld_ro16(qrow[j] + ka);
+                st.q[j][1] = ld_ro16(qrow[j] + kb);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                const int tok = 8 * j + g;
+                const int8_t *src = q + static_cast<int64_t>(tok) * K + k0;
+                st.q[j][0] = (tok < M && k0 < K) ? ld_ro16(src) : make_uint4(0, 0, 0, 0);
+                st.q[j][1] = (tok < M && k0 + 16 < K) ? ld_ro16(src + 16) : make_uint4(0, 0, 0, 0);
+            }
         }
     };
 
@@ -204,9 +237,11 @@ cudaError_t launch_gemv(const int8_t *q, const float *tok_scale, const uint8_t *
     const int Z = (M + 15) / 16;  // 16-token chunks (M <= 64)
     // about two CTAs per SM, but never more than fit at once (4 per SM for
     // the 8-token kernel, 3 for the 16-token one at 168 registers): a second
-    // wave cost up to 1.6x (3B gate/up at 32 tokens: 16.9 -> 10.3 us)
+    // wave cost up to 1.6x (3B gate/up at 32 tokens: 16.9 -> 10.3 us).  Up
+    // to 8 tokens the split fills every resident slot (70B down and q/o at
+    // one token: 22.5 -> 21.3 and 9.7 -> 9.3 us; 3B gate/up 6.6 -> 6.3).
     const int cap = ((M <= 8 ? 4 : 3) * num_sms) / (RB * Z);
-    int S = (2 * num_sms + RB * Z - 1) / (RB * Z);
+    int S = M <= 8 ? cap : (2 * num_sms + RB * Z - 1) / (RB * Z);
     if (S > cap) S = cap;
     const int smax = KT / kWarps > 1 ? KT / kWarps : 1;
     if (S > smax) S = smax;
@@ -215,11 +250,13 @@ cudaError_t launch_gemv(const int8_t *q, const float *tok_scale, const uint8_t *
     int tpc = (KT + S - 1) / S;
     S = (KT + tpc - 1) / tpc;
     const dim3 grid(S, RB, Z), block(kWarps * 32);
-    if (M <= 8)
-        return launch_pdl(gemv_kernel<1>, grid, block, 0, st, S, q, tok_scale, packed, gamma, M, N, K,
-                          KT, RGN, tpc, out, acc_out);
-    return launch_pdl(gemv_kernel<2>, grid, block, 0, st, S, q, tok_scale, packed, gamma, M, N, K, KT,
-                      RGN, tpc, out, acc_out);
+    auto go = [&](auto kernel) {
+        return launch_pdl(kernel, grid, block, 0, st, S, q, tok_scale, packed, gamma, M, N, K, KT, RGN, tpc,
+                          out, acc_out);
+    };
+    const bool large = static_cast<int64_t>(N) * K >= (1ll << 20);
+    if (M <= 8) return large ? go(gemv_kernel<1, true>) : go(gemv_kernel<1, false>);
+    return large ? go(gemv_kernel<2, true>) : go(gemv_kernel<2, false>);
 }
 
 }  // namespace bl

@@ -311,6 +311,22 @@ BITLINEAR_API bitlinear_status_t bitlinear_fused_factors(void *stats, int64_t M,
                                                          void *stream);
 
 /*
+ * How bitlinear_forward_fused quantises its input.  Below the threshold
+ * (packed weight bytes of the launch: sum over j of the packed size of
+ * projection j, rounded up to 64-row blocks) every CTA quantises the slice
+ * of x it reads; at or above it, one pre-pass kernel quantises x into
+ * stream-ordered scratch memory (M * K bytes, from a library-owned pool) and
+ * the GEMV reads int8.  Same bits either way: the choice changes only the
+ * time.  min_weight_bytes: -1 restores the default (32 MiB, measured: the
+ * 70B gate+up and down launches gain 5-8 us at one token, the smaller ones
+ * would lose the extra launch), 0 uses the pre-pass always, larger values
+ * set the threshold.  Process-wide, not per stream.  Errors: INVALID_ARG
+ * (below -1).  With the pre-pass, bitlinear_forward_fused can also return
+ * CUDA when the scratch allocation fails (nothing is launched then).
+ */
+BITLINEAR_API bitlinear_status_t bitlinear_set_fused_prepass(int64_t min_weight_bytes);
+
+/*
  * Reads and clears the current device's kernel status word after
  * synchronising `stream`.  Returns BITLINEAR_OK, BITLINEAR_ERR_STATE (a
  * pending factor buffer was produced into again), BITLINEAR_ERR_TIMEOUT (a

@@ -163,6 +163,12 @@ def test_set_engine_validates_without_a_gpu(lib):
     assert lib.bitlinear_set_engine(-1, 0) == bl.OK                # the defaults again
 
 
+def test_set_fused_prepass_validates_without_a_gpu(lib):
+    assert lib.bitlinear_set_fused_prepass(-2) == bl.ERR_INVALID_ARG
+    for v in (0, 1, 1 << 40, -1):                                  # -1 last: the default again
+        assert lib.bitlinear_set_fused_prepass(v) == bl.OK
+
+
 def test_variant_sizes_and_argument_checks(lib):
     assert bl.bitlinear_packed5_bytes(16, 160) == 512
     assert bl.bitlinear_packed5_bytes(17, 336) == 32 * 480 // 5

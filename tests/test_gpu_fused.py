@@ -35,6 +35,18 @@ def _lib():
     torch.cuda.init()
 
 
+@pytest.fixture(autouse=True)
+def _default_prepass():
+    yield
+    bl.bitlinear_set_fused_prepass(-1)
+
+
+# bitlinear_set_fused_prepass thresholds: the default (in-kernel quantisation
+# for these small launches) and 0 (every launch through the quantising
+# pre-pass and the GEMV on int8 input)
+PREPASS = [-1, 0]
+
+
 def bits16(t):
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
@@ -124,8 +136,10 @@ def new_stats():
     return {k: bl.new_stats(DEV) for k in ("x", "v", "o", "up", "down")}
 
 
+@pytest.mark.parametrize("prepass", PREPASS)
 @pytest.mark.parametrize("M", [1, 3, 8, 9, 16])
-def test_fused_small_ragged_layer(M):
+def test_fused_small_ragged_layer(M, prepass):
+    bl.bitlinear_set_fused_prepass(prepass)
     # ragged: N not a multiple of 64, K not a multiple of 128
     hidden, ffn, kv = 272, 400, 144
     shapes = [(hidden, hidden), (kv, hidden), (kv, hidden), (hidden, kv), (ffn, hidden), (ffn, hidden),
@@ -139,8 +153,10 @@ def test_fused_small_ragged_layer(M):
     run_layer(M, hidden, ffn, kv, w, x2, stats)
 
 
+@pytest.mark.parametrize("prepass", PREPASS)
 @pytest.mark.parametrize("M", [1, 4, 16])
-def test_fused_2b_layer(M):
+def test_fused_2b_layer(M, prepass):
+    bl.bitlinear_set_fused_prepass(prepass)
     hidden, ffn, kv = 2560, 6912, 2560
     shapes = [(hidden, hidden), (kv, hidden), (kv, hidden), (hidden, kv), (ffn, hidden), (ffn, hidden),
               (hidden, ffn)]
@@ -149,7 +165,9 @@ def test_fused_2b_layer(M):
     run_layer(M, hidden, ffn, kv, w, x, new_stats())
 
 
-def test_fused_matches_unfused_path():
+@pytest.mark.parametrize("prepass", PREPASS)
+def test_fused_matches_unfused_path(prepass):
+    bl.bitlinear_set_fused_prepass(prepass)
     M, K, N = 5, 2560, 6912
     w = make_weights([(N, K)], seed=9500)[0]
     x = inputs.activations_bf16(M, K, seed=9600).to(DEV)
@@ -168,9 +186,12 @@ def test_fused_matches_unfused_path():
     np.testing.assert_allclose(ts, s.cpu().numpy(), rtol=S_TOK_RTOL)
 
 
-def test_factor_buffer_protocol():
+@pytest.mark.parametrize("prepass", PREPASS)
+def test_factor_buffer_protocol(prepass):
     """Pending until consumed; every consumer sees the same factors; a second
-    production into a pending buffer is reported; act_stats resets."""
+    production into a pending buffer is reported; act_stats resets.  (With
+    the pre-pass, the pre-pass kernel is the consumer.)"""
+    bl.bitlinear_set_fused_prepass(prepass)
     M, K, N, N2 = 7, 512, 640, 384
     w1 = make_weights([(N, K)], seed=9800)[0]
     w2 = make_weights([(N2, N)], seed=9801)[0]

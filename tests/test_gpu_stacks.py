@@ -33,6 +33,12 @@ def _lib():
     torch.cuda.init()
 
 
+@pytest.fixture(autouse=True)
+def _default_prepass():
+    yield
+    bl.bitlinear_set_fused_prepass(-1)
+
+
 def bits16(t):
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
@@ -86,10 +92,16 @@ def sample_rows(N, rng, n=24):
     return np.unique(np.concatenate([[0, N - 1], rng.integers(0, N, n)]))
 
 
-@pytest.mark.parametrize("workload,layers,M", [("stack_70b", 2, 1), ("stack_70b", 2, 16), ("stack_3b", 2, 4)])
-def test_stack_fused_path_sampled(workload, layers, M):
+# prepass: the threshold of bitlinear_set_fused_prepass (-1: the default,
+# under which the 70B gate+up and down launches quantise their input in a
+# pre-pass and the others in every CTA; 0: all launches; 2^40: none)
+@pytest.mark.parametrize("workload,layers,M,prepass", [("stack_70b", 2, 1, -1), ("stack_70b", 2, 16, -1),
+                                                       ("stack_70b", 1, 4, 1 << 40), ("stack_3b", 2, 4, -1),
+                                                       ("stack_3b", 1, 9, 0)])
+def test_stack_fused_path_sampled(workload, layers, M, prepass):
     """The fused decode path (act_stats + 4 launches per layer), as the
     benchmark runs it, through the first layers of the stack."""
+    bl.bitlinear_set_fused_prepass(prepass)
     S = StackLayers(workload, layers)
     rng = np.random.default_rng(M)
     x0 = inputs.activations_bf16(M, S.hidden, seed=7 * M + 3, device=DEV)
