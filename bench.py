@@ -62,7 +62,7 @@ FALLBACK_BF16_TFLOPS = 1800.0
 # kernel over the step's 240 launches, from an ncu capture of this kernel
 # (profiles/fused_gemv_decode_2b_dram_traffic.md); None once the kernel
 # changes after the capture.
-FUSED_DRAM_PER_PACKED_BYTE = None
+FUSED_DRAM_PER_PACKED_BYTE = 1.0207
 
 
 def peaks():
