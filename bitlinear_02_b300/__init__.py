@@ -8,6 +8,10 @@ library is missing (not built) every call raises ``RuntimeError``.
 
 Convenience wrappers (``pack_weights``, ``quant_act``, ``forward``,
 ``bitlinear``) allocate the outputs with torch and call the same entry points.
+
+With ``BITLINEAR_DEBUG=1`` in the environment the binding loads the debug
+build, ``libbitlinear_debug.so`` (device-side bounds checks; see
+``include/bitlinear.h``), instead.
 """
 from __future__ import annotations
 
@@ -31,7 +35,7 @@ __all__ = [
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_LIB_NAME = "libbitlinear.so"
+_LIB_NAME = "libbitlinear_debug.so" if os.environ.get("BITLINEAR_DEBUG") == "1" else "libbitlinear.so"
 
 OK = 0
 ERR_INVALID_ARG = 1
@@ -39,6 +43,7 @@ ERR_UNSUPPORTED = 2
 ERR_CUDA = 3
 ERR_TIMEOUT = 4
 ERR_STATE = 5
+ERR_BOUNDS = 6
 
 
 class FusedProj(ctypes.Structure):
@@ -102,12 +107,13 @@ def load_library():
     L.bitlinear_fused_factors.argtypes = [P, I64, I64, F, ctypes.c_int32, P, P, P]
     L.bitlinear_forward_f16.argtypes = [P, P, P, P, I64, I64, I64, P, P, P]
     L.bitlinear_set_fused_prepass.argtypes = [I64]
+    L.bitlinear_debug_selftest.argtypes = [P]
     for name in ("bitlinear_pack_weights", "bitlinear_pack_weights_noalloc", "bitlinear_pack_ternary", "bitlinear_quant_act",
                  "bitlinear_forward", "bitlinear_check_status",
                  "bitlinear_quant_act_f16", "bitlinear_forward_f16", "bitlinear_act_stats",
                  "bitlinear_forward_fused", "bitlinear_fused_factors", "bitlinear_set_engine",
                  "bitlinear_repack5", "bitlinear_forward5", "bitlinear_pack_binary", "bitlinear_forward_binary",
-                 "bitlinear_set_fused_prepass"):
+                 "bitlinear_set_fused_prepass", "bitlinear_debug_selftest"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -280,6 +286,12 @@ def bitlinear_forward_binary(q, tok_scale, packed1, beta, groups: int, M: int, N
                                                    int(groups), int(M), int(N), int(K), _ptr(out), _ptr(acc_out),
                                                    _stream(stream)),
            "bitlinear_forward_binary")
+
+
+def bitlinear_debug_selftest(stream=None) -> int:
+    """Debug build: records one failed bounds check (no memory access);
+    returns the status (ERR_UNSUPPORTED in a release build), does not raise."""
+    return int(load_library().bitlinear_debug_selftest(_stream(stream)))
 
 
 def bitlinear_set_fused_prepass(min_weight_bytes: int = -1) -> None:

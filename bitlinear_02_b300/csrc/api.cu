@@ -43,11 +43,53 @@ extern "C" const char *bitlinear_status_string(int status) {
         case BITLINEAR_ERR_CUDA: return "CUDA runtime error";
         case BITLINEAR_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
         case BITLINEAR_ERR_STATE: return "a pending factor buffer was produced into again";
+        case BITLINEAR_ERR_BOUNDS: return "a device bounds check failed (debug build)";
         default: return "unknown status";
     }
 }
 
 extern "C" int bitlinear_version(void) { return 100; }
+
+#ifdef BITLINEAR_DEBUG
+#include <cstdio>
+#include <mutex>
+#include <vector>
+namespace bl {
+namespace {
+struct DebugEntry {
+    DebugTake take;
+    const char *unit;
+};
+// Function-local statics: the units register from their static
+// initialisers, in whatever order the loader runs them.
+std::vector<DebugEntry> &debug_units() {
+    static std::vector<DebugEntry> v;
+    return v;
+}
+std::mutex &debug_mutex() {
+    static std::mutex m;
+    return m;
+}
+// Records a failed check without any memory access: the reporting path,
+// testable without an out-of-bounds access.
+__global__ void debug_selftest_kernel() { dbg_ok(false, 31u); }
+}  // namespace
+void debug_register(DebugTake take, const char *unit) {
+    std::lock_guard<std::mutex> lock(debug_mutex());
+    debug_units().push_back({take, unit});
+}
+}  // namespace bl
+#endif
+
+extern "C" bitlinear_status_t bitlinear_debug_selftest(void *stream) {
+#ifdef BITLINEAR_DEBUG
+    bl::debug_selftest_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>();
+    return cudaGetLastError() == cudaSuccess ? BITLINEAR_OK : BITLINEAR_ERR_CUDA;
+#else
+    (void)stream;
+    return BITLINEAR_ERR_UNSUPPORTED;
+#endif
+}
 
 namespace bl {
 uint32_t current_wait_limit() { return g_wait_limit.load(); }
@@ -141,6 +183,19 @@ extern "C" bitlinear_status_t bitlinear_forward_f16(const void *q_f16, const flo
 extern "C" bitlinear_status_t bitlinear_check_status(void *stream) {
     unsigned int v = 0;
     if (bl::gemm_status(&v, static_cast<cudaStream_t>(stream)) != cudaSuccess) return BITLINEAR_ERR_CUDA;
+#ifdef BITLINEAR_DEBUG
+    {
+        std::lock_guard<std::mutex> lock(bl::debug_mutex());
+        unsigned int bounds = 0u;
+        for (const auto &u : bl::debug_units()) {
+            unsigned int w = 0u;
+            if (u.take(&w, static_cast<cudaStream_t>(stream)) != cudaSuccess) return BITLINEAR_ERR_CUDA;
+            if (w) std::fprintf(stderr, "bitlinear: device bounds check failed in %s (site bits 0x%08x)\n", u.unit, w);
+            bounds |= w;
+        }
+        if (bounds) return BITLINEAR_ERR_BOUNDS;
+    }
+#endif
     // bit 0: a bounded wait gave up; bit 1: a pending factor buffer was produced into
     if (v & 1u) return BITLINEAR_ERR_TIMEOUT;
     return v ? BITLINEAR_ERR_STATE : BITLINEAR_OK;

@@ -24,6 +24,47 @@ uint32_t current_wait_limit();  // api.cu: spin limit of every bounded wait
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
+// ------------------------------------------------- debug bounds checks ---
+//
+// Built with -DBITLINEAR_DEBUG (libbitlinear_debug.so), every plain global
+// load and store of the kernels is preceded by a check of its offset
+// against its buffer's extent, stated apart from the index arithmetic that
+// produced it: if (dbg_ok(offset fits, site)) access.  A failed check sets
+// bit `site` of its translation unit's word and skips the access - no trap,
+// so the context stays usable - and bitlinear_check_status collects every
+// unit's word and reports BITLINEAR_ERR_BOUNDS.  Tensor-map (TMA) copies
+// are bounds-checked by the hardware and need none.  In release builds
+// dbg_ok is the constant true and the checks compile away.
+#ifdef BITLINEAR_DEBUG
+using DebugTake = cudaError_t (*)(unsigned int *, cudaStream_t);
+void debug_register(DebugTake take, const char *unit);  // api.cu
+static __device__ unsigned int g_dbg_bounds = 0u;       // one per translation unit
+__device__ __forceinline__ bool dbg_ok(bool in_bounds, unsigned int site) {
+    if (!in_bounds) atomicOr(&g_dbg_bounds, 1u << (site & 31u));
+    return in_bounds;
+}
+// Reads and clears this unit's word (stream-ordered, then synchronised).
+static cudaError_t dbg_take(unsigned int *v, cudaStream_t st) {
+    cudaError_t e = cudaMemcpyFromSymbolAsync(v, g_dbg_bounds, sizeof(unsigned int), 0, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return e;
+    const unsigned int zero = 0u;
+    e = cudaMemcpyToSymbolAsync(g_dbg_bounds, &zero, sizeof(unsigned int), 0, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return e;
+    return cudaStreamSynchronize(st);
+}
+namespace {
+struct DebugUnit {
+    DebugUnit() { debug_register(&dbg_take, __BASE_FILE__); }
+} g_debug_unit;
+}  // namespace
+#else
+__device__ __forceinline__ constexpr bool dbg_ok(bool, unsigned int) { return true; }
+#endif
+// Offset o (elements) of an access of n elements fits a buffer of `extent`.
+__device__ __forceinline__ constexpr bool fits(int64_t o, int64_t n, int64_t extent) {
+    return o >= 0 && o + n <= extent;
+}
+
 // Launch a kernel with programmatic dependent launch enabled (and an
 // optional cluster shape).  The kernel itself decides when it may start
 // reading data produced by the previous kernel in the stream

@@ -54,6 +54,7 @@ static_assert(kWarps == 4, "cta_factors covers 16 tokens with 4 warps");
 constexpr int kCopies = 16;
 constexpr int kOffC = 0, kOffTs = 16, kOffState = 32, kOffTicket = 33, kOffMax = 64, kOffSum = 64 + 16 * kCopies;
 constexpr size_t kStatsBytes = (64 + 32 * kCopies) * 4;
+constexpr int64_t kStatsFloats = static_cast<int64_t>(kStatsBytes / 4);
 constexpr unsigned kPending = 1u;     // state: the accumulator holds an unconsumed production
 constexpr unsigned kStateError = 2u;  // status bit: a factor buffer was produced twice unconsumed
 
@@ -203,13 +204,14 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 3) fused_gemv_kerne
 #pragma unroll
         for (int i = 0; i < kGroups; ++i) {
             const int rg = min(rbl * kGroups + i, P.RGN - 1);
-            st.w[i] = ld_stream16(P.packed + (static_cast<int64_t>(rg) * KT + c) * 512 + lane * 16);
+            const int64_t off = (static_cast<int64_t>(rg) * KT + c) * 512 + lane * 16;
+            if (dbg_ok(fits(off, 16, static_cast<int64_t>(P.RGN) * KT * 512), 0)) st.w[i] = ld_stream16(P.packed + off);
         }
     };
     auto load_x = [&](Stage<NT> &st, int c) {
         if (c >= c_end) return;
         const int k0 = c * 128 + t * 32;
-        if (kQ) {
+        if constexpr (kQ) {
             // 32 int8 values per lane, clamped like the decode GEMV's large
             // matrices: a token past M reads token M-1 (not stored), k past K
             // rereads the row's last 16 values against padding codes c = 1,
@@ -217,22 +219,26 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 3) fused_gemv_kerne
             const int ka = min(k0, K - 16), kb = min(k0 + 16, K - 16);
 #pragma unroll
             for (int jj = 0; jj < NT; ++jj) {
-                const int8_t *src = A.q + static_cast<int64_t>(min(8 * jj + g, M - 1)) * K;
-                st.x[jj][0] = ld_ro16(src + ka);
-                st.x[jj][1] = ld_ro16(src + kb);
+                const int64_t o = static_cast<int64_t>(min(8 * jj + g, M - 1)) * K;
+                if (dbg_ok(fits(o + ka, 16, static_cast<int64_t>(M) * K) && fits(o + kb, 16, static_cast<int64_t>(M) * K), 1)) {
+                    st.x[jj][0] = ld_ro16(A.q + o + ka);
+                    st.x[jj][1] = ld_ro16(A.q + o + kb);
+                }
             }
-            return;
-        }
+        } else {
 #pragma unroll
-        for (int jj = 0; jj < NT; ++jj) {
-            const int tok = 8 * jj + g;
-            const __nv_bfloat16 *src = A.x + static_cast<int64_t>(tok) * K + k0;
-            const uint4 z = make_uint4(0, 0, 0, 0);
-            const bool lo_ok = tok < M && k0 < K, hi_ok = tok < M && k0 + 16 < K;
-            st.x[jj][0] = lo_ok ? ld_ro16(src) : z;
-            st.x[jj][1] = lo_ok ? ld_ro16(src + 8) : z;
-            st.x[jj][2] = hi_ok ? ld_ro16(src + 16) : z;
-            st.x[jj][3] = hi_ok ? ld_ro16(src + 24) : z;
+            for (int jj = 0; jj < NT; ++jj) {
+                const int tok = 8 * jj + g;
+                const __nv_bfloat16 *src = A.x + static_cast<int64_t>(tok) * K + k0;
+                const uint4 z = make_uint4(0, 0, 0, 0);
+                const int64_t o = static_cast<int64_t>(tok) * K + k0, xe = static_cast<int64_t>(M) * K;
+                const bool lo_ok = tok < M && k0 < K && dbg_ok(fits(o, 16, xe), 2);
+                const bool hi_ok = tok < M && k0 + 16 < K && dbg_ok(fits(o + 16, 16, xe), 2);
+                st.x[jj][0] = lo_ok ? ld_ro16(src) : z;
+                st.x[jj][1] = lo_ok ? ld_ro16(src + 8) : z;
+                st.x[jj][2] = hi_ok ? ld_ro16(src + 16) : z;
+                st.x[jj][3] = hi_ok ? ld_ro16(src + 24) : z;
+            }
         }
     };
 
@@ -251,7 +257,7 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 3) fused_gemv_kerne
         uint32_t b[NT][8][2];
 #pragma unroll
         for (int jj = 0; jj < NT; ++jj) {
-            if (kQ)
+            if constexpr (kQ)
                 dm::build_b(st.x[jj][0], st.x[jj][1], b[jj], corr[jj]);
             else
                 dm::build_b(quant16(st.x[jj][0], st.x[jj][1], cq[jj]), quant16(st.x[jj][2], st.x[jj][3], cq[jj]),
@@ -370,11 +376,12 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 3) fused_gemv_kerne
         const int tk = e / kRows, rr = e % kRows;
         const int n = rbl * kRows + rr;
         float vf = 0.0f;
-        if (n < P.N) {
+        const int64_t oi = static_cast<int64_t>(tk) * P.N + n;
+        if (n < P.N && dbg_ok(fits(oi, 1, static_cast<int64_t>(M) * P.N), 3)) {
             const float f = __fmul_rn(gam, s_ts[tk]);
             const __nv_bfloat16 o = __float2bfloat16_rn(__fmul_rn(static_cast<float>(v), f));
-            P.out[static_cast<int64_t>(tk) * P.N + n] = o;
-            if (P.acc_out) P.acc_out[static_cast<int64_t>(tk) * P.N + n] = v;
+            P.out[oi] = o;
+            if (P.acc_out) P.acc_out[oi] = v;
             vf = __bfloat162float(o);
         }
         vals[e] = vf;
@@ -401,7 +408,7 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 3) fused_gemv_kerne
                 const float oh = __shfl_xor_sync(0xffffffffu, hi, off), ol = __shfl_xor_sync(0xffffffffu, lo, off);
                 ff_add(hi, lo, oh, ol);
             }
-            if (lane == 0) {
+            if (lane == 0 && dbg_ok(fits(kOffSum + cp * 16 + tk, 1, kStatsFloats) && tk < 16, 4)) {
                 atomicMax(reinterpret_cast<unsigned int *>(P.stats + kOffMax) + cp * 16 + tk, __float_as_uint(mx));
                 atomicAdd(P.stats + kOffSum + cp * 16 + tk, __fadd_rn(hi, lo));
             }
@@ -455,7 +462,8 @@ __global__ void __launch_bounds__(kWarps * 32) fused_quant_kernel(const __nv_bfl
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int tok = static_cast<int>(i * 16 / K);
         const uint4 *src = reinterpret_cast<const uint4 *>(x) + 2 * i;
-        reinterpret_cast<uint4 *>(q)[i] = quant16(__ldg(src), __ldg(src + 1), s_c[tok]);
+        if (dbg_ok(fits(16 * i, 16, static_cast<int64_t>(M) * K) && tok < M, 5))
+            reinterpret_cast<uint4 *>(q)[i] = quant16(__ldg(src), __ldg(src + 1), s_c[tok]);
     }
     if (pend && warp == 0) {
         const unsigned tk0 = __shfl_sync(0xffffffffu, ticket, 0);
@@ -496,6 +504,7 @@ __global__ void __launch_bounds__(256) act_stats_kernel(const uint4 *__restrict_
     };
     const uint4 *xr = x + static_cast<int64_t>(m) * (K / 8);
     for (int i = threadIdx.x; i < K / 8; i += 256) {
+        if (!dbg_ok(fits(static_cast<int64_t>(m) * K + 8 * i, 8, static_cast<int64_t>(M) * K), 6)) continue;
         const uint4 v = xr[i];
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll

@@ -214,12 +214,13 @@ __device__ __forceinline__ void store_tile(uint32_t tmem, int warp, int lane, in
         for (int i = 0; i < 32; i += 2) {
             const int c = col + i, tk = tok0 + c;
             const __nv_bfloat162 o = rescale2(__uint_as_float(v[i]), s_f[c], __uint_as_float(v[i + 1]), s_f[c + 1]);
+            const int64_t oe = static_cast<int64_t>(M) * N;
             if (n < N) {
-                if (tk < M) {
+                if (tk < M && dbg_ok(fits(static_cast<int64_t>(tk) * N + n, 1, oe), 0)) {
                     out[static_cast<int64_t>(tk) * N + n] = o.x;
                     if (acc_out) acc_out[static_cast<int64_t>(tk) * N + n] = __float2int_rn(__uint_as_float(v[i]));
                 }
-                if (tk + 1 < M) {
+                if (tk + 1 < M && dbg_ok(fits(static_cast<int64_t>(tk + 1) * N + n, 1, oe), 0)) {
                     out[static_cast<int64_t>(tk + 1) * N + n] = o.y;
                     if (acc_out)
                         acc_out[static_cast<int64_t>(tk + 1) * N + n] = __float2int_rn(__uint_as_float(v[i + 1]));
@@ -321,6 +322,7 @@ __device__ __forceinline__ void reduce_partials(const uint32_t *red, int split, 
         }
         const float f = s_f[col];
         const int64_t o = static_cast<int64_t>(tk) * N + n0;
+        if (!dbg_ok(fits(o, vec ? 4 : 1, static_cast<int64_t>(M) * N), 1)) continue;
         const __nv_bfloat162 lo = rescale2(a[0], f, a[1], f), hi = rescale2(a[2], f, a[3], f);
         if (vec) {
             uint2 pk;
@@ -374,7 +376,7 @@ __device__ __forceinline__ void finish_tile(uint8_t *smem, uint32_t tmem, uint32
         pdl_wait();
         const float gam = *gamma;
         for (int c = tid; c < BN; c += kConverters)
-            s_f[c] = tok0 + c < M ? __fmul_rn(gam, tok_scale[tok0 + c]) : 0.0f;
+            s_f[c] = tok0 + c < M && dbg_ok(fits(tok0 + c, 1, M), 2) ? __fmul_rn(gam, tok_scale[tok0 + c]) : 0.0f;
         asm volatile("bar.sync 1, %0;" ::"r"(kConverters) : "memory");  // warps 0-7
         // The same outcome in all eight warps (the staged store below has a
         // barrier of its own that all of them, or none, must reach).
@@ -899,7 +901,8 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
             const int b = i & 1, rt = t % row_tiles, tok0 = (t / row_tiles) * BN;
             float *f = s_f + 256 * b;
-            for (int c = etid; c < BN; c += 128) f[c] = tok0 + c < M ? __fmul_rn(gam, tok_scale[tok0 + c]) : 0.0f;
+            for (int c = etid; c < BN; c += 128)
+                f[c] = tok0 + c < M && dbg_ok(fits(tok0 + c, 1, M), 3) ? __fmul_rn(gam, tok_scale[tok0 + c]) : 0.0f;
             bool have = mbar_wait_abortable_warp(&acc_full[b], (i >> 1) & 1, wait_limit, abort);
             if (etid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // the buffer is free
             have = bar_and(2, 128, have);  // also publishes f[] and the free buffer to all four warps
@@ -1272,6 +1275,7 @@ __global__ void __launch_bounds__(256) widen_kernel(const uint4 *__restrict__ q,
     pdl_wait();  // q comes from the previous kernel
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n16; i += stride) {
+        if (!dbg_ok(fits(i, 1, n16), 4)) continue;
         const uint4 v = q[i];
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         uint32_t f[8];

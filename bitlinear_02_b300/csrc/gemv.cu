@@ -50,6 +50,12 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 3)
     __shared__ int32_t part[kWarps][NT * 8][kRows];
     __shared__ int32_t total[NT * 8 * kRows];
 
+    // Extents of the buffers, for the debug build's bounds checks (offsets
+    // from the unshifted pointers: q_base, o_base).
+    const int64_t w_ext = static_cast<int64_t>(RGN) * KT * 512, q_ext = static_cast<int64_t>(M) * K,
+                  o_ext = static_cast<int64_t>(M) * N, s_ext = M;
+    const int64_t q_base = static_cast<int64_t>(blockIdx.z) * 16 * K, o_base = static_cast<int64_t>(blockIdx.z) * 16 * N,
+                  s_base = 16 * static_cast<int64_t>(blockIdx.z);
     // Batches of up to 64 tokens: blockIdx.z picks a 16-token chunk (its rows
     // of q, scales and outputs); the chunks share the weights through L2.
     {
@@ -92,11 +98,12 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 3)
 #pragma unroll
         for (int i = 0; i < kGroups; ++i) {
             if (kClamp) {
-                st.w[i] = ld_stream16(wrow[i] + c * 512);
+                if (dbg_ok(fits(wrow[i] + c * 512 - packed, 16, w_ext), 0)) st.w[i] = ld_stream16(wrow[i] + c * 512);
             } else {
                 const int rg = rb * kGroups + i;
-                if (rg < RGN)
-                    st.w[i] = ld_stream16(packed + (static_cast<int64_t>(rg) * KT + c) * 512 + lane * 16);
+                const int64_t off = (static_cast<int64_t>(rg) * KT + c) * 512 + lane * 16;
+                if (rg < RGN && dbg_ok(fits(off, 16, w_ext), 1))
+                    st.w[i] = ld_stream16(packed + off);
                 else
                     st.w[i] = make_uint4(0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u);
             }
@@ -109,16 +116,22 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 3)
             const int ka = min(k0, K - 16), kb = min(k0 + 16, K - 16);
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
-                st.q[j][0] = ld_ro16(qrow[j] + ka);
-                st.q[j][1] = ld_ro16(qrow[j] + kb);
+                const int64_t o = q_base + (qrow[j] - q);
+                if (dbg_ok(fits(o + ka, 16, q_ext) && fits(o + kb, 16, q_ext), 2)) {
+                    st.q[j][0] = ld_ro16(qrow[j] + ka);
+                    st.q[j][1] = ld_ro16(qrow[j] + kb);
+                }
             }
         } else {
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
                 const int tok = 8 * j + g;
-                const int8_t *src = q + static_cast<int64_t>(tok) * K + k0;
-                st.q[j][0] = (tok < M && k0 < K) ? ld_ro16(src) : make_uint4(0, 0, 0, 0);
-                st.q[j][1] = (tok < M && k0 + 16 < K) ? ld_ro16(src + 16) : make_uint4(0, 0, 0, 0);
+                const int64_t o = static_cast<int64_t>(tok) * K + k0;
+                const int8_t *src = q + o;
+                const bool lo = tok < M && k0 < K && dbg_ok(fits(q_base + o, 16, q_ext), 3);
+                const bool hi = tok < M && k0 + 16 < K && dbg_ok(fits(q_base + o + 16, 16, q_ext), 3);
+                st.q[j][0] = lo ? ld_ro16(src) : make_uint4(0, 0, 0, 0);
+                st.q[j][1] = hi ? ld_ro16(src + 16) : make_uint4(0, 0, 0, 0);
             }
         }
     };
@@ -213,10 +226,11 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 3)
         }
         const int tk = e / kRows, rr = e % kRows;
         const int n = rb * kRows + rr;
-        if (tk < M && n < N) {
+        const int64_t o = static_cast<int64_t>(tk) * N + n;
+        if (tk < M && n < N && dbg_ok(fits(s_base + tk, 1, s_ext) && fits(o_base + o, 1, o_ext), 4)) {
             const float f = __fmul_rn(gam, tok_scale[tk]);
-            out[static_cast<int64_t>(tk) * N + n] = __float2bfloat16_rn(__fmul_rn(static_cast<float>(v), f));
-            if (acc_out) acc_out[static_cast<int64_t>(tk) * N + n] = v;
+            out[o] = __float2bfloat16_rn(__fmul_rn(static_cast<float>(v), f));
+            if (acc_out) acc_out[o] = v;
         }
     }
     if (S > 1) cluster_sync();  // keep this CTA's shared memory alive for its peers

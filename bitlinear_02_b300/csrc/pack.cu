@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const void *__restrict__ src,
             const int64_t n = 16 * r + 8 * u + g;
             const int64_t k0 = 128 * c + 32 * t + 16 * P;
             int codes[16];
-            if (n < N && k0 < K) {  // K % 16 == 0: the 16 k's are all in range
+            if (n < N && k0 < K && dbg_ok(fits(n * K + k0, 16, N * K), 0)) {  // K % 16 == 0: all 16 in range
                 if (kFromFloat) {
                     const float4 *row =
                         reinterpret_cast<const float4 *>(static_cast<const float *>(src) + n * K + k0);
@@ -174,7 +174,8 @@ __global__ void __launch_bounds__(256) pack_kernel(const void *__restrict__ src,
             words[2 * P + u] = wv;
         }
     }
-    packed[id] = make_uint4(words[0], words[1], words[2], words[3]);
+    // the packed layout holds RGN * KT tiles of 32 chunks
+    if (dbg_ok(fits(id, 1, (N + 15) / 16 * KT * 32), 1)) packed[id] = make_uint4(words[0], words[1], words[2], words[3]);
 }
 
 // Per-device bucket workspace, allocated on first use and kept until exit.
@@ -253,10 +254,11 @@ __global__ void __launch_bounds__(256) pack1_kernel(const float *__restrict__ W,
 #pragma unroll 4
         for (int j = 0; j < 32; ++j) {
             const int64_t k = kb + j;
-            if (k < K && row[k] > 0.0f) word |= 1u << (16 * (j % 2) + 2 * (j / 4) + (j % 4) / 2);
+            if (k < K && dbg_ok(fits(n * K + k, 1, N * K), 2) && row[k] > 0.0f)
+                word |= 1u << (16 * (j % 2) + 2 * (j / 4) + (j % 4) / 2);
         }
     }
-    out[wi] = word;
+    if (dbg_ok(fits(wi, 1, (N + 15) / 16 * KT1 * 128), 3)) out[wi] = word;
 }
 
 }  // namespace

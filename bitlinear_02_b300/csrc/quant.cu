@@ -76,6 +76,7 @@ __global__ void __launch_bounds__(kThreads)
         const uint4 *xr = x + m * chunks;
 #pragma unroll 4
         for (int64_t i = tid; i < chunks; i += nthr) {
+            if (!dbg_ok(fits(m * K + 8 * i, 8, M * K) && fits(8 * i, 8, K), 0)) continue;
             float v[8];
             bf16x8_to_f32(xr[i], v);
             if (kGain) {
@@ -125,6 +126,7 @@ __global__ void __launch_bounds__(kThreads)
     uint4 *qh = reinterpret_cast<uint4 *>(static_cast<__half *>(qout) + m * K);
 #pragma unroll 4
     for (int64_t i = tid; i < chunks; i += nthr) {
+        if (!dbg_ok(fits(m * K + 8 * i, 8, M * K) && fits(8 * i, 8, K), 1)) continue;
         float v[8];
         bf16x8_to_f32(xr[i], v);
         if (kGain) {
@@ -147,7 +149,7 @@ __global__ void __launch_bounds__(kThreads)
         else
             qr[i] = make_uint2(b[0], b[1]);
     }
-    if (tid == 0) {
+    if (tid == 0 && dbg_ok(fits(m, 1, M), 2)) {
         const float ms = __fadd_rn(__fdiv_rn(ss.value(), static_cast<float>(K)), eps);
         const float r = __fdiv_rn(1.0f, __fsqrt_rn(ms));
         tok_scale[m] = __fdiv_rn(__fmul_rn(r, mx), 127.0f);

@@ -135,8 +135,10 @@ __device__ __forceinline__ void trits_word(const VStage<Fmt::kTrits5, NT> &st, c
 // ---- binary ----
 template <int P>
 __device__ __forceinline__ uint32_t bit_reg(uint32_t w) {
-    if (P < 12) return w & (0x00010001u << P);
-    return (w >> 8) & (0x00010001u << (P - 8));
+    if constexpr (P < 12)
+        return w & (0x00010001u << P);
+    else
+        return (w >> 8) & (0x00010001u << (P - 8));
 }
 template <int P>
 constexpr int bit_exp() {
@@ -189,6 +191,11 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
     __shared__ int32_t part[kWarps][NT * 8][kRows];
     __shared__ int32_t total[NT * 8 * kRows];
 
+    // extents and chunk offsets, for the debug build's bounds checks
+    const int64_t w_ext = static_cast<int64_t>(RGN) * KT * 512, q_ext = static_cast<int64_t>(M) * K,
+                  o_ext = static_cast<int64_t>(M) * N, s_ext = M;
+    const int64_t q_base = static_cast<int64_t>(blockIdx.z) * 16 * K, o_base = static_cast<int64_t>(blockIdx.z) * 16 * N,
+                  s_base = 16 * static_cast<int64_t>(blockIdx.z);
     {
         const int z = static_cast<int>(blockIdx.z);
         q += static_cast<int64_t>(z) * 16 * K;
@@ -209,8 +216,9 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
 #pragma unroll
         for (int i = 0; i < kGroups; ++i) {
             const int rg = rb * kGroups + i;
-            if (rg < RGN)
-                st.w[i] = ld_stream16(packed + (static_cast<int64_t>(rg) * KT + c) * 512 + lane * 16);
+            const int64_t off = (static_cast<int64_t>(rg) * KT + c) * 512 + lane * 16;
+            if (rg < RGN && dbg_ok(fits(off, 16, w_ext), 0))
+                st.w[i] = ld_stream16(packed + off);
             else
                 st.w[i] = make_uint4(0u, 0u, 0u, 0u);  // never stored (rows past N)
         }
@@ -225,7 +233,8 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
             if constexpr (F == Fmt::kTrits5) {
 #pragma unroll
                 for (int p = 0; p < 5; ++p) {  // 8-byte pieces: k0 is a multiple of 8, K of 16
-                    const bool ok = tok < M && k0 + 8 * p < K;
+                    const bool ok = tok < M && k0 + 8 * p < K &&
+                                    dbg_ok(fits(q_base + static_cast<int64_t>(tok) * K + k0 + 8 * p, 8, q_ext), 1);
                     const uint2 v = ok ? __ldg(reinterpret_cast<const uint2 *>(src + 8 * p)) : make_uint2(0u, 0u);
                     st.q[j][2 * p] = v.x;
                     st.q[j][2 * p + 1] = v.y;
@@ -233,7 +242,8 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
             } else {
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
-                    const bool ok = tok < M && k0 + 16 * p < K;
+                    const bool ok = tok < M && k0 + 16 * p < K &&
+                                    dbg_ok(fits(q_base + static_cast<int64_t>(tok) * K + k0 + 16 * p, 16, q_ext), 1);
                     const uint4 v = ok ? ld_ro16(src + 16 * p) : make_uint4(0u, 0u, 0u, 0u);
                     st.q[j][4 * p] = v.x;
                     st.q[j][4 * p + 1] = v.y;
@@ -343,10 +353,13 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
         }
         const int tk = e / kRows, rr = e % kRows;
         const int n = rb * kRows + rr;
-        if (tk < M && n < N) {
+        const int64_t o = static_cast<int64_t>(tk) * N + n;
+        if (tk < M && n < N &&
+            dbg_ok(fits(o_base + o, 1, o_ext) && fits(s_base + tk, 1, s_ext) && fits(n / group_rows, 1, N / group_rows),
+                   2)) {
             const float f = __fmul_rn(scales[n / group_rows], tok_scale[tk]);
-            out[static_cast<int64_t>(tk) * N + n] = __float2bfloat16_rn(__fmul_rn(static_cast<float>(v), f));
-            if (acc_out) acc_out[static_cast<int64_t>(tk) * N + n] = v;
+            out[o] = __float2bfloat16_rn(__fmul_rn(static_cast<float>(v), f));
+            if (acc_out) acc_out[o] = v;
         }
     }
     if (S > 1) cluster_sync();  // keep this CTA's shared memory alive for its peers
@@ -381,11 +394,11 @@ __global__ void __launch_bounds__(256) repack5_kernel(const uint8_t *__restrict_
             const int P = j2 / 16, m = (j2 % 16) / 4, sb = (j2 % 4) / 2, h = j2 % 2;
             const int bit = 16 * h + 2 * (2 * m + sb);
             const int64_t byte = 512 * (r * KT + k / 128) + 16 * (4 * g + t2) + 4 * (2 * P + u) + bit / 8;
-            e = (src[byte] >> (bit % 8)) & 3;
+            if (dbg_ok(fits(byte, 1, (N + 15) / 16 * KT * 512), 3)) e = (src[byte] >> (bit % 8)) & 3;
         }
         v = 3 * v + e;
     }
-    dst[ob] = static_cast<uint8_t>((256 * v + 242) / 243);
+    if (dbg_ok(fits(ob, 1, (N + 15) / 16 * KT5 * 512), 4)) dst[ob] = static_cast<uint8_t>((256 * v + 242) / 243);
 }
 
 template <Fmt F>

@@ -66,7 +66,8 @@ typedef enum {
     BITLINEAR_ERR_UNSUPPORTED = 2, /* no sm_103a device / shape beyond limits */
     BITLINEAR_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
     BITLINEAR_ERR_TIMEOUT = 4,     /* a kernel gave up a bounded wait */
-    BITLINEAR_ERR_STATE = 5        /* a pending factor buffer was produced into again */
+    BITLINEAR_ERR_STATE = 5,       /* a pending factor buffer was produced into again */
+    BITLINEAR_ERR_BOUNDS = 6       /* debug build: a device bounds check failed */
 } bitlinear_status_t;
 
 /* Static, NUL-terminated description of a status code (never NULL). */
@@ -328,12 +329,28 @@ BITLINEAR_API bitlinear_status_t bitlinear_set_fused_prepass(int64_t min_weight_
 
 /*
  * Reads and clears the current device's kernel status word after
- * synchronising `stream`.  Returns BITLINEAR_OK, BITLINEAR_ERR_STATE (a
+ * synchronising `stream`.  Returns BITLINEAR_OK, BITLINEAR_ERR_BOUNDS
+ * (debug build, below), BITLINEAR_ERR_STATE (a
  * pending factor buffer was produced into again), BITLINEAR_ERR_TIMEOUT (a
  * bounded wait gave up), or BITLINEAR_ERR_CUDA if the stream reports an
  * error.
  */
 BITLINEAR_API bitlinear_status_t bitlinear_check_status(void *stream);
+
+/*
+ * Debug build.  Compiled with -DBITLINEAR_DEBUG (libbitlinear_debug.so,
+ * `python bitlinear_02_b300/build.py --debug`), every plain global load and
+ * store of the kernels first checks its offset against its buffer's extent;
+ * a failed check skips the access and is recorded (no trap: the context
+ * stays usable).  bitlinear_check_status then returns BITLINEAR_ERR_BOUNDS
+ * (before any other code) and names the source file and check sites on
+ * stderr.  Tensor-map copies are bounds-checked by the hardware.  Release
+ * builds carry no checks.
+ * bitlinear_debug_selftest enqueues a kernel that records one failed check
+ * without touching memory, to exercise that reporting path; release builds
+ * return BITLINEAR_ERR_UNSUPPORTED and enqueue nothing.
+ */
+BITLINEAR_API bitlinear_status_t bitlinear_debug_selftest(void *stream);
 
 /*
  * Test hook: sets the spin limit of every bounded wait in the library's

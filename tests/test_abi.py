@@ -38,14 +38,26 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, name), name
 
 
+def exported_abi(path):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    return {s for s in exported if s.startswith("bitlinear_")}
+
+
 def test_only_abi_symbols_are_exported(lib):
     # the build hides everything that is not declared extern "C" in the header
-    import subprocess
-    out = subprocess.run(["nm", "-D", "--defined-only", bl.library_path()], capture_output=True,
-                         text=True).stdout
-    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
-    ours = {s for s in exported if s.startswith("bitlinear_")}
-    assert ours == set(declared_functions())
+    assert exported_abi(bl.library_path()) == set(declared_functions())
+
+
+def test_debug_build_exports_the_same_boundary(lib):
+    """The -DBITLINEAR_DEBUG build (device-side bounds checks) has the same
+    ABI; in the release build the self-test reports that it has no checks."""
+    path = blbuild.build(debug=True)
+    assert os.path.basename(path) == "libbitlinear_debug.so"
+    assert exported_abi(path) == set(declared_functions())
+    assert lib.bitlinear_debug_selftest(None) == bl.ERR_UNSUPPORTED  # release: nothing enqueued
+    assert lib.bitlinear_status_string(bl.ERR_BOUNDS) == b"a device bounds check failed (debug build)"
 
 
 def test_packed_bytes(lib):
