@@ -246,6 +246,27 @@ def time_graphs(torch, graphs, steps, warmup, stream, barrier=None, clock=None):
     return e0.elapsed_time(e1)  # ms
 
 
+def time_graph_flushed(torch, g, steps, warmup, stream, flush):
+    """Mean ms per replay of graph g, each replay timed on its own with CUDA
+    events on `stream`, after a write of `flush` (larger than L2) that stays
+    outside the timed events, so no replay finds the previous one's data in
+    L2."""
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        tot = 0.0
+        for _ in range(steps):
+            flush.zero_()
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            tot += e0.elapsed_time(e1)
+    return tot / steps
+
+
 def capture(torch, fn, stream):
     """One eager run (host-side set-up happens outside capture), then a graph."""
     with torch.cuda.stream(stream):
@@ -600,7 +621,8 @@ def prefill_bench(torch, bl, inputs, dev, stream, bf16_peak, steps=5, warmup=3, 
     (bitlinear_quant_act_f16 + bitlinear_forward_f16) and through the int8
     entry points (bitlinear_quant_act + bitlinear_forward); TOPS of the
     tensor-core GEMMs alone (2*M*N*K per projection) and of the whole chain,
-    and each distinct shape's f16 GEMM on its own."""
+    and each distinct shape's f16 GEMM on its own.  Every replay is timed on
+    its own after a 256 MB L2 flush (outside the timed events)."""
     wl = inputs.WORKLOADS["prefill_2b"]
     shapes = wl["shapes"]
     plan, dims = chain_plan(shapes)
@@ -610,6 +632,7 @@ def prefill_bench(torch, bl, inputs, dev, stream, bf16_peak, steps=5, warmup=3, 
         W = inputs.weights_fp32(N, K, seed=wl["seed"] * 100 + i, device=dev)
         w[name] = bl.pack_weights(W, wl["eps_w"])
         del W
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     res = []
     for M in m_list:
         b = {"x": inputs.activations_bf16(M, hidden, seed=wl["seed"] * 1000 + M, outlier_frac=0.01,
@@ -642,9 +665,9 @@ def prefill_bench(torch, bl, inputs, dev, stream, bf16_peak, steps=5, warmup=3, 
         row = {"M": M}
         for path, int8 in (("f16", False), ("int8", True)):
             g = capture(torch, lambda: step(int8=int8), stream)
-            ms = time_graphs(torch, [g], steps, warmup, stream) / steps
+            ms = time_graph_flushed(torch, g, steps, warmup, stream, flush)
             g2 = capture(torch, lambda: step(kinds=("fwd",), int8=int8), stream)
-            ms2 = time_graphs(torch, [g2], steps, warmup, stream) / steps
+            ms2 = time_graph_flushed(torch, g2, steps, warmup, stream, flush)
             row[path] = {"chain_ms": round(ms, 4), "chain_tops": round(ops / (ms * 1e-3) / 1e12, 1),
                          "gemm_ms": round(ms2, 4), "gemm_tops": round(ops / (ms2 * 1e-3) / 1e12, 1),
                          "gemm_frac": round(ops / (ms2 * 1e-3) / 1e12 / bf16_peak, 4),
@@ -654,7 +677,7 @@ def prefill_bench(torch, bl, inputs, dev, stream, bf16_peak, steps=5, warmup=3, 
         for o in ("q", "gate", "down"):
             N, K = dims[o]
             g = capture(torch, lambda: step(kinds=("fwd",), only=(o,)), stream)
-            ms = time_graphs(torch, [g], steps * 4, warmup, stream) / (steps * 4)
+            ms = time_graph_flushed(torch, g, steps * 4, warmup, stream, flush)
             t = 2 * M * N * K / (ms * 1e-3) / 1e12
             per_shape.append({"proj": o, "N": N, "K": K, "us": round(ms * 1e3, 2), "TFLOP/s": round(t, 1),
                               "frac": round(t / bf16_peak, 4)})
@@ -662,32 +685,38 @@ def prefill_bench(torch, bl, inputs, dev, stream, bf16_peak, steps=5, warmup=3, 
         row["f16_per_shape"] = per_shape
         res.append(row)
         del b
-    del w
+    del w, flush
     torch.cuda.empty_cache()
     return {"shapes": "q,k,v,o 2560x2560; gate,up 2560->6912; down 6912->2560",
             "peak_note": "TOPS against the measured cuBLAS bf16 burst peak: the GEMM runs exact f16 tcgen05 "
                          "MMAs (sm_103a has no int8 tcgen05 MMA)", "rows": res}
 
 
-def small_layer_row(torch, bl, inputs, dev, stream, hbm_peak, reps=200):
+def small_layer_row(torch, bl, inputs, dev, stream, hbm_peak, reps=50):
     """The small single-layer workload (M = 1, K = 256, N = 512): quantise +
-    forward, back to back in a graph of 50 layers' worth of calls."""
+    forward, back to back in a graph of 50 layers' worth of calls over 50
+    distinct copies of the packed matrix, each replay timed after a 256 MB
+    L2 flush (outside the timed events): every layer reads its weights from
+    HBM."""
     wl = inputs.WORKLOADS["layer_small"]
     _, N, K = wl["shapes"][0]
     W = inputs.weights_fp32(N, K, seed=wl["seed"], device=dev)
     packed, gamma = bl.pack_weights(W, wl["eps_w"])
+    mats = [packed] + [packed.clone() for _ in range(49)]
     x = inputs.activations_bf16(1, K, seed=1, device=dev)
     q = torch.empty(1, K, dtype=torch.int8, device=dev)
     s = torch.empty(1, dtype=torch.float32, device=dev)
     out = torch.empty(1, N, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     def run():
-        for _ in range(50):
+        for p in mats:
             bl.bitlinear_quant_act(x, None, 1, K, wl["eps_a"], q, s, stream)
-            bl.bitlinear_forward(q, s, packed, gamma, 1, N, K, out, None, stream)
+            bl.bitlinear_forward(q, s, p, gamma, 1, N, K, out, None, stream)
 
     g = capture(torch, run, stream)
-    ms = time_graphs(torch, [g], reps, 5, stream) / reps / 50
+    ms = time_graph_flushed(torch, g, reps, 5, stream, flush) / 50
+    del g, flush
     b = algo_bytes_quant(1, K) + algo_bytes_forward(1, N, K)
     return {"M": 1, "K": K, "N": N, "us_per_layer": round(ms * 1e3, 3),
             "GB/s": round(b / (ms * 1e-3) / 1e9, 2), "frac": round(b / (ms * 1e-3) / 1e9 / hbm_peak, 5),
