@@ -109,8 +109,13 @@ std::atomic<int32_t> g_gemv_max_tokens{-1};  // -1: the measured default below
 std::atomic<int32_t> g_split_k{0};
 
 // The default engine choice (B300 measurements, weights from HBM): the GEMV
-// up to 48 tokens (three 16-token chunks); at 49-64 tokens (four chunks) the
-// split-K GEMM where K is large and the matrix is big - 8192x8192 34.8 us
+// up to 32 tokens (two 16-token chunks); at 33-48 tokens (three chunks) the
+// split-K GEMM on widened activations for matrices with K >= 8192, N <= K
+// and at least 2^24 weights - 8192x28672 68 against 88 us, 8192x8192 25.0
+// against 27.4, 3200x8640 15.1 against 17.5 - and the GEMV elsewhere
+// (28672x8192 79 against 81, 1024x8192 8.5 against 10.7, 2560x6912 11.7
+// against 12.5, 6912x2560 10.8 against 13.2); at 49-64 tokens (four chunks)
+// the GEMM where K is large and the matrix is big - 8192x8192 34.8 us
 // against 43.0, 8192x28672 94 against 125-141, 2560x6912 18.4 against 19.7
 // - and the GEMV elsewhere (2560x2560 12.3 against 14.3, 6912x2560 16.4
 // against 18.4, 1024x8192 14.3 against 16.4); the GEMM above 64.
@@ -119,6 +124,7 @@ bool use_gemv(int64_t M, int64_t N, int64_t K) {
     if (forced >= 0) return M <= forced;
     if (M > kGemvMaxM) return false;
     if (M > 48 && K >= 6912 && N * K >= (1ll << 24)) return false;
+    if (M > 32 && K >= 8192 && N <= K && N * K >= (1ll << 24)) return false;
     return true;
 }
 }  // namespace

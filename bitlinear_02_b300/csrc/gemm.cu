@@ -1335,9 +1335,10 @@ cudaError_t widen_alloc(void **p, size_t bytes, cudaStream_t st) {
 cudaError_t scratch_alloc(void **p, size_t bytes, cudaStream_t st) { return widen_alloc(p, bytes, st); }
 
 // bitlinear_forward widens the int8 activations to f16 once (one pass over
-// M x K) and runs the f16-operand GEMM above 256 tokens, and above 48 for
+// M x K) and runs the f16-operand GEMM above 256 tokens, and above 32 for
 // matrices of at least 2^24 weights (at 49-64 tokens the f16-operand GEMM
-// takes 84 against 104 us on 28672x8192, 72 against 94 on 8192x28672): in
+// takes 84 against 104 us on 28672x8192, 72 against 94 on 8192x28672; at
+// 33-48 tokens, with the widening pass, 81 against 99 and 68 against 90): in
 // the int8 engine every row-tile CTA
 // converts the same activation tile again (20-224 times for the 2B-70B
 // shapes), which held it at 0.43 of the bf16 peak against 0.67 for f16
@@ -1345,7 +1346,7 @@ cudaError_t scratch_alloc(void **p, size_t bytes, cudaStream_t st) { return wide
 // gate/up and down matrices (measured; the 2560x2560 ones gain nothing
 // there, the extra launch eats the saving).
 bool widen_first(int M, int N, int K) {
-    return M > 256 || (M > 48 && static_cast<int64_t>(N) * K >= (1ll << 24));
+    return M > 256 || (M > 32 && static_cast<int64_t>(N) * K >= (1ll << 24));
 }
 
 cudaError_t launch_gemm(const int8_t *q, const float *tok_scale, const uint8_t *packed, const float *gamma, int M,

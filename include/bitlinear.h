@@ -193,13 +193,14 @@ BITLINEAR_API bitlinear_status_t bitlinear_quant_act(const void *x_bf16, const v
  * cudaStreamWaitEvent.  Do not write it with a kernel of your own launched
  * immediately before this call on the same stream: launch that kernel on
  * another stream and join the streams with an event instead.
- * Engine choice is internal (bitlinear_set_engine overrides it): up to 48
- * tokens, and up to 64 where K < 6912 or N*K < 2^24, the decode GEMV
- * (legacy tensor MMA on register-unpacked codes; above 16 tokens in 16-token
- * chunks of one launch); otherwise the tcgen05 GEMM (TMEM accumulators),
- * with its K range split across a cluster where the output tiles alone
- * would leave most SMs idle.  Above 256 tokens, and above 48 for matrices
- * of at least 2^24 weights, the int8 activations are first widened to f16
+ * Engine choice is internal (bitlinear_set_engine overrides it): up to 32
+ * tokens, up to 48 unless K >= 8192, N <= K and N*K >= 2^24, and up to 64
+ * where K < 6912 or N*K < 2^24, the decode GEMV (legacy tensor MMA on
+ * register-unpacked codes; above 16 tokens in 16-token chunks of one
+ * launch); otherwise the tcgen05 GEMM (TMEM accumulators), with its K range
+ * split across a cluster where the output tiles alone would leave most SMs
+ * idle.  Above 256 tokens, and above 32 for matrices of at least 2^24
+ * weights, the int8 activations are first widened to f16
  * (exact) into a buffer taken, stream-ordered, from a
  * memory pool the library keeps per device (M*K*2 bytes, returned to the
  * pool at the end of the call; the pool keeps its memory for later calls).
@@ -367,9 +368,10 @@ BITLINEAR_API void bitlinear_set_wait_limit(uint32_t iterations);
  *   gemv_max_tokens: batches of up to this many tokens run bitlinear_forward
  *     on the decode GEMV engine (16-token chunks of one launch), larger ones
  *     on the tensor-core GEMM; 0 sends every batch to the GEMM; at most 64.
- *     -1 restores the default: the GEMV up to 48 tokens, and at 49-64 tokens
- *     too unless K >= 6912 and N*K >= 2^24 (where the split-K GEMM was
- *     measured faster).
+ *     -1 restores the default: the GEMV up to 32 tokens; at 33-48 tokens too
+ *     unless K >= 8192, N <= K and N*K >= 2^24, and at 49-64 tokens unless
+ *     K >= 6912 and N*K >= 2^24 (where the split-K GEMM on widened
+ *     activations was measured faster).
  *   split_k: CTAs per cluster that share one GEMM output tile's k range
  *     (their int32 partial tiles summed through distributed shared memory).
  *     0 restores the default (the planner picks 1..16 from the tile count,

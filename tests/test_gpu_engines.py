@@ -124,6 +124,34 @@ def test_split_on_narrow_70b_projection(M):
         np.testing.assert_array_equal(bits16(out), oracle.epilogue(acc_ref, s.cpu().numpy(), gam))
 
 
+@pytest.mark.parametrize("M", [33, 48])
+def test_mid_batch_default_route_on_deep_matrix(M):
+    """33-48 tokens on a matrix with K >= 8192, N <= K and N*K >= 2^24 (2064
+    x 8192, a ragged last row tile): the default route is the split GEMM on
+    widened activations; it gives the GEMV's bits, and sampled accumulators
+    match the oracle."""
+    N, K = 2064, 8192
+    wq = inputs.ternary(N, K, seed=950 + M)
+    gdev = torch.tensor([0.03], dtype=torch.float32, device=DEV)
+    packed = bl.pack_ternary(wq.to(DEV))
+    x = inputs.activations_bf16(M, K, seed=951 + M)
+    q, s = bl.quant_act(x.to(DEV))
+    runs = {}
+    for route, gmax in (("default", -1), ("gemv", 64)):
+        bl.bitlinear_set_engine(gmax, 0)
+        acc = torch.empty(M, N, dtype=torch.int32, device=DEV)
+        out = bl.forward(q, s, packed, gdev, N, acc_out=acc)
+        torch.cuda.synchronize()
+        assert bl.bitlinear_check_status() == bl.OK
+        runs[route] = (acc.cpu().numpy(), bits16(out))
+    np.testing.assert_array_equal(runs["default"][0], runs["gemv"][0])
+    np.testing.assert_array_equal(runs["default"][1], runs["gemv"][1])
+    rng = np.random.default_rng(M)
+    ms, ns = rng.integers(0, M, 512), rng.integers(0, N, 512)
+    want = oracle.matmul_pairs(q.cpu().numpy(), wq.numpy(), ms, ns)
+    np.testing.assert_array_equal(runs["default"][0][ms, ns], want)
+
+
 def test_set_engine_rejects_out_of_range():
     for args in ((65, 0), (-2, 0), (0, 17), (0, -1)):
         with pytest.raises(bl.BitLinearError):
