@@ -798,6 +798,99 @@ def oracle_step_sample(budget_s=20.0, threads=0):
     return nbytes / dt / 1e9, reps, dt, used
 
 
+def oracle_configs(threads=0):
+    """The oracle as it stands, on every host core, per config: the small
+    layer in full (repeated for about a second); the 2B prefill chain with M
+    capped at 64 tokens (TOPS; a full 4096-token run would take hours); one
+    layer of the 3B and 70B stacks at M = 1 (their own counter-based
+    weights, unpacked per call like every oracle call), scaled by the layer
+    count and labelled extrapolated."""
+    import numpy as np
+    import oracle
+    from bitlinear_02_b300 import inputs
+    oracle.set_threads(threads)
+    res = {}
+
+    def run_chain(shapes, M, packed, gam, x, eps_a, o_from):
+        plan, dims = chain_plan(shapes, o_from)
+        acts = {"x": x}
+        for kind, a, o in plan:
+            if kind == "quant":
+                acts[o] = oracle.quant_act(acts[a], None, eps_a)
+            else:
+                q, sc = acts[a]
+                N, K = dims[o]
+                wq, _ = oracle.unpack(packed[o], N, K)
+                acts[o] = oracle.epilogue(oracle.matmul(q, wq), sc, gam[o])
+
+    # config 1: quantise + forward, one 512 x 256 layer
+    wl = inputs.WORKLOADS["layer_small"]
+    _, N, K = wl["shapes"][0]
+    w = inputs.weights_fp32(N, K, seed=wl["seed"]).numpy()
+    g = oracle.gamma(w)
+    pk = oracle.pack(oracle.ternarize(w, g, wl["eps_w"]))
+    x = inputs.bf16_bits(inputs.activations_bf16(1, K, seed=1))
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        q, sc = oracle.quant_act(x, None, wl["eps_a"])
+        wq, _ = oracle.unpack(pk, N, K)
+        oracle.epilogue(oracle.matmul(q, wq), sc, g)
+        reps += 1
+        if time.perf_counter() - t0 >= 1.0:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    b = algo_bytes_quant(1, K) + algo_bytes_forward(1, N, K)
+    res["layer_small"] = {"us_per_layer": round(dt * 1e6, 1), "GB/s": round(b / dt / 1e9, 4),
+                          "tokens_per_s": round(1 / dt, 1), "sample": f"{reps} layers"}
+
+    # config 3: the prefill chain at 64 tokens
+    wl = inputs.WORKLOADS["prefill_2b"]
+    shapes = wl["shapes"]
+    packed, gam = {}, {}
+    for i, (name, N, K) in enumerate(shapes):
+        w = inputs.weights_fp32(N, K, seed=wl["seed"] * 100 + i).numpy()
+        gam[name] = oracle.gamma(w)
+        packed[name] = oracle.pack(oracle.ternarize(w, gam[name], wl["eps_w"]))
+        del w
+    M = 64
+    x = inputs.bf16_bits(inputs.activations_bf16(M, shapes[0][2], seed=wl["seed"] * 1000 + M, outlier_frac=0.01,
+                                                 outlier_scale=20.0))
+    t0 = time.perf_counter()
+    run_chain(shapes, M, packed, gam, x, wl["eps_a"], "v")
+    dt = time.perf_counter() - t0
+    _, dims = chain_plan(shapes)
+    ops = sum(2 * M * dims[o][0] * dims[o][1] for k, _, o in chain_plan(shapes)[0] if k == "fwd")
+    res["prefill_2b"] = {"M": M, "chain_ms": round(dt * 1e3, 1), "TOPS": round(ops / dt / 1e12, 5),
+                         "tokens_per_s": round(M / dt, 1),
+                         "sample": "one seven-projection chain at 64 tokens (M capped; 4096 would take hours)"}
+    del packed
+
+    # configs 4 and 5: one layer at M = 1, scaled by the layer count
+    for name in ("stack_3b", "stack_70b"):
+        wl = inputs.WORKLOADS[name]
+        shapes, layers = wl["shapes"], wl["layers"]
+        hidden = shapes[0][2]
+        o_from = "v" if shapes[2][1] == hidden else "q"
+        packed, gam = {}, {}
+        for i, (pname, N, K) in enumerate(shapes):
+            packed[pname] = oracle.pack(oracle.ternary_hash(inputs.stack_word(wl["seed"], 0, i), K, 0, N))
+            gam[pname] = np.float32(inputs.gamma_uniform(wl["seed"] * 100000 + i))
+        x = inputs.bf16_bits(inputs.activations_bf16(1, hidden, seed=3 + 7))
+        t0 = time.perf_counter()
+        run_chain(shapes, 1, packed, gam, x, wl["eps_a"], o_from)
+        dt = time.perf_counter() - t0
+        b = layer_bytes(1, shapes, o_from)
+        res[name] = {"GB/s": round(b / dt / 1e9, 4), "tokens_per_s": round(1 / (dt * layers), 4),
+                     "s_per_token": round(dt * layers, 2),
+                     "sample": f"one layer at M = 1 in {dt:.2f} s, extrapolated to {layers} layers"}
+        del packed
+    used = oracle.threads()
+    oracle.set_threads(0)
+    for v in res.values():
+        v["cores"] = used
+    return res
+
+
 # ------------------------------------------------------------ main --------
 
 def run_reference(args):
@@ -1126,7 +1219,8 @@ def main():
                "sample": f"{reps} x one 2B-shape layer for each M=1,4,16 (quantise, unpack, matmul, rescale; "
                          f"7 chained projections) in {dt:.1f} s",
                "single_thread": {"value": round(gbs1, 4), "unit": "GB/s", "cores": c1,
-                                 "sample": f"{reps1} x the same sample in {dt1:.1f} s"}}
+                                 "sample": f"{reps1} x the same sample in {dt1:.1f} s"},
+               "configs": oracle_configs()}
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
