@@ -994,7 +994,8 @@ cudaError_t encode_locked(CUtensorMap *map, const MapKey &key, CUtensorMapDataTy
     if (!g_encode) {
         cudaDriverEntryPointQueryResult qr;
         void *fn = nullptr;
-        cudaError_t e = cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &fn, cudaEnableDefault, &qr);
+        // the ABI version of the function the PFN type below describes
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qr);
         if (e != cudaSuccess || qr != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
         g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
