@@ -23,8 +23,12 @@
 //     accumulator for the next production.  Later launches reading the same
 //     buffer use those factors.
 // A decode layer becomes four launches, chained with programmatic dependent
-// launch.  q and the int32 accumulators are bit-identical to the unfused
-// path; the token scale agrees to about 1e-7.
+// launch.  Launches with many weight bytes (at least 16 MiB by default)
+// quantise their input once instead, in fused_quant_kernel, which consumes
+// the factor buffer the same way, and the GEMV reads int8 (every row block
+// quantising the whole input again costs more there than it saves).  q and
+// the int32 accumulators are bit-identical to the unfused path; the token
+// scale agrees to about 1e-7.
 #include "decode_math.cuh"
 
 #include <atomic>
@@ -35,9 +39,11 @@ cudaError_t scratch_alloc(void **p, size_t bytes, cudaStream_t st);  // gemm.cu:
 
 // Launches of at least this many packed weight bytes quantise their input
 // in a pre-pass (bitlinear_set_fused_prepass; -1: this default).  Measured
-// on the 70B shapes at one token: gate+up (117 MB) and down (58.7 MB) gain
-// 5-8 us each; q+k+v (21 MB) and o (16.8 MB) lose the extra launch.
-constexpr int64_t kPrepassDefault = 32ll << 20;
+// on the stacks: the 70B one at one token 8.28 ms without the pre-pass,
+// 7.48 with it from 32 MiB (gate+up 117 MB, down 58.7 MB), 7.32 from 16 MiB
+// (also q+k+v 21 MB and o 16.8 MB), 7.32 on every launch; the 3B one (all
+// launches under 14 MB) 0.865 ms without it and 0.920 with it everywhere.
+constexpr int64_t kPrepassDefault = 16ll << 20;
 std::atomic<int64_t> g_prepass_min{-1};
 namespace {
 

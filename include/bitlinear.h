@@ -319,9 +319,10 @@ BITLINEAR_API bitlinear_status_t bitlinear_fused_factors(void *stats, int64_t M,
  * of x it reads; at or above it, one pre-pass kernel quantises x into
  * stream-ordered scratch memory (M * K bytes, from a library-owned pool) and
  * the GEMV reads int8.  Same bits either way: the choice changes only the
- * time.  min_weight_bytes: -1 restores the default (32 MiB, measured: the
- * 70B gate+up and down launches gain 5-8 us at one token, the smaller ones
- * would lose the extra launch), 0 uses the pre-pass always, larger values
+ * time.  min_weight_bytes: -1 restores the default (16 MiB, measured: the
+ * 70B stack at one token takes 8.28 ms without the pre-pass and 7.32 with
+ * it from 16 MiB; the 3B stack's launches, all under 14 MB, are 6 % slower
+ * with it), 0 uses the pre-pass always, larger values
  * set the threshold.  Process-wide, not per stream.  Errors: INVALID_ARG
  * (below -1).  With the pre-pass, bitlinear_forward_fused can also return
  * CUDA when the scratch allocation fails (nothing is launched then).
