@@ -652,6 +652,17 @@ extern "C" bitlinear_status_t bitlinear_forward_fused(const void *x_bf16, void *
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int per_sm = M <= 8 ? 2 : 1;
     int S = (per_sm * sms + rbs - 1) / rbs;
+    const int64_t wbytes = static_cast<int64_t>(rbs) * A.KT * 2048;
+    const int64_t pre_min = g_prepass_min.load();
+    const bool prepass = wbytes >= (pre_min >= 0 ? pre_min : kPrepassDefault);
+    if (prepass) {
+        // Large launches split K until their CTAs fill every resident slot
+        // (4 per SM for the 8-token kernel, 3 for the 16-token one), as the
+        // decode GEMV does: the 70B stack 8.00 -> 7.60 ms at 4 tokens, 8.46
+        // -> 7.75 at 8 and 12.91 -> 11.81 at 16 (unchanged at one token).
+        const int cap = ((M <= 8 ? 4 : 3) * sms) / rbs;
+        if (cap > S) S = cap;
+    }
     const int smax = A.KT / kWarps > 1 ? A.KT / kWarps : 1;
     if (S > smax) S = smax;
     if (S > 8) S = 8;
@@ -663,9 +674,7 @@ extern "C" bitlinear_status_t bitlinear_forward_fused(const void *x_bf16, void *
         if (static_cast<int64_t>(A.p[j].rb1 - A.p[j].rb0) * S > (1 << 30)) return BITLINEAR_ERR_UNSUPPORTED;
     const dim3 grid(S, rbs), block(kWarps * 32);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const int64_t wbytes = static_cast<int64_t>(rbs) * A.KT * 2048;
-    const int64_t pre_min = g_prepass_min.load();
-    if (wbytes < (pre_min >= 0 ? pre_min : kPrepassDefault)) {
+    if (!prepass) {
         const cudaError_t e = M <= 8 ? launch_pdl(fused_gemv_kernel<1, false>, grid, block, 0, st, S, A)
                                      : launch_pdl(fused_gemv_kernel<2, false>, grid, block, 0, st, S, A);
         return e == cudaSuccess ? BITLINEAR_OK : BITLINEAR_ERR_CUDA;
