@@ -644,7 +644,8 @@ extern "C" bitlinear_status_t bitlinear_forward_fused(const void *x_bf16, void *
     // every argument is checked: only now the first CUDA call
     if (status_word(&A.status) != cudaSuccess) return BITLINEAR_ERR_CUDA;
     // K split over a cluster of S CTAs (combined in distributed shared
-    // memory), sized for about two CTAs per SM up to 8 tokens and one above
+    // memory).  Launches that quantise in the loop: sized for about two
+    // CTAs per SM up to 8 tokens and one above
     // (the 16-token kernel holds 168 registers a thread; measured on the 2B
     // step: 12.16 -> 11.68 us per launch at M = 16, while M <= 8 is 3 %
     // slower with one CTA per SM and 14 % slower with three)
