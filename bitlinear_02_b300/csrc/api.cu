@@ -48,7 +48,7 @@ extern "C" const char *bitlinear_status_string(int status) {
     }
 }
 
-extern "C" int bitlinear_version(void) { return 100; }
+extern "C" int bitlinear_version(void) { return 101; }
 
 #ifdef BITLINEAR_DEBUG
 #include <cstdio>

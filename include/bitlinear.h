@@ -73,7 +73,9 @@ typedef enum {
 /* Static, NUL-terminated description of a status code (never NULL). */
 BITLINEAR_API const char *bitlinear_status_string(int status);
 
-/* Library ABI version (major*100 + minor). */
+/* Library ABI version (major*100 + minor).  1.01 added
+ * bitlinear_set_fused_prepass, bitlinear_debug_selftest and
+ * BITLINEAR_ERR_BOUNDS; every 1.00 entry point is unchanged. */
 BITLINEAR_API int bitlinear_version(void);
 
 /* Bytes of the packed buffer for an [N, K] weight matrix:

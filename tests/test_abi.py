@@ -72,7 +72,7 @@ def test_status_strings(lib):
     assert "invalid" in bl.bitlinear_status_string(1)
     assert "bounded wait" in bl.bitlinear_status_string(4)
     assert bl.bitlinear_status_string(99) == "unknown status"
-    assert bl.bitlinear_version() == 100
+    assert bl.bitlinear_version() == 101
 
 
 FAKE = 1 << 20  # an aligned non-null address: never dereferenced, checks fail first
