@@ -96,6 +96,8 @@ def sample_rows(N, rng, n=24):
 # 16 MiB, under which every 70B launch quantises its input in a pre-pass and
 # every 3B launch in its CTAs; 0: all launches; 2^40: none)
 @pytest.mark.parametrize("workload,layers,M,prepass", [("stack_70b", 2, 1, -1), ("stack_70b", 2, 16, -1),
+                                                       ("stack_70b", 1, 5, -1), ("stack_70b", 1, 8, -1),
+                                                       ("stack_70b", 1, 11, -1),
                                                        ("stack_70b", 1, 4, 1 << 40), ("stack_3b", 2, 4, -1),
                                                        ("stack_3b", 1, 9, 0)])
 def test_stack_fused_path_sampled(workload, layers, M, prepass):
