@@ -176,10 +176,23 @@ __device__ __forceinline__ void load_codes(const uint8_t *codes, int rgl, int ri
 // lane in the packed tile) -> 16 registers of f16 pairs (Wq = code - 1),
 // i.e. 16 TMEM columns.  `w0`, `w1`: the row's 32-bit code words.
 __device__ __forceinline__ void expand_codes(uint32_t w0, uint32_t w1, uint32_t (&f)[16]) {
+    // Pair p <= 4 stays in place: (bits | 0x6400) reads as 1024 + c*4^p
+    // (mantissa bits 0-9), and one f16x2 FMA by 4^-p with offset
+    // -(1024*4^-p + 1) gives c - 1 exactly (a power-of-two scaling and an
+    // exactly representable result).  Pairs 5-7 come down to 0-2 with one
+    // shift shared by the three.  9 integer operations per 16 weights
+    // instead of 15 (shift, mask and OR per pair), the rest on the FMA pipe
+    // (measured: 28672x8192 at 64 tokens 81.6 -> 78.0 us, 2560x2560 at 4096
+    // 48.1 -> 46.9; the other prefill and mid-M shapes within 1 %).
+    constexpr uint32_t kScale[5] = {0x3C003C00u, 0x34003400u, 0x2C002C00u, 0x24002400u, 0x1C001C00u};
+    constexpr uint32_t kOffset[5] = {0xE401E401u, 0xDC04DC04u, 0xD410D410u, 0xCC40CC40u, 0xC500C500u};
+    const uint32_t v0 = w0 >> 10, v1 = w1 >> 10;
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
-        f[p] = hadd2(((w0 >> (2 * p)) & 0x00030003u) | 0x64006400u, 0xE401E401u);
-        f[8 + p] = hadd2(((w1 >> (2 * p)) & 0x00030003u) | 0x64006400u, 0xE401E401u);
+        const int s = p < 5 ? p : p - 5;
+        const uint32_t m = 0x00030003u << (2 * s);
+        f[p] = hfma2(((p < 5 ? w0 : v0) & m) | 0x64006400u, kScale[s], kOffset[s]);
+        f[8 + p] = hfma2(((p < 5 ? w1 : v1) & m) | 0x64006400u, kScale[s], kOffset[s]);
     }
 }
 
