@@ -24,7 +24,8 @@
  *   - Arguments are validated on the host before anything is enqueued; an
  *     invalid argument returns BITLINEAR_ERR_INVALID_ARG and enqueues nothing.
  *   - A failed kernel launch returns BITLINEAR_ERR_CUDA.
- *   - No exception crosses this boundary and nothing is printed.
+ *   - No exception crosses this boundary and nothing is printed (except the
+ *     debug build's report of a failed bounds check, on stderr).
  *   - Matrices are row-major.  W is [N out, K in] (K contiguous); x, q are
  *     [M tokens, K]; out, acc are [M, N].
  *   - K must be a multiple of 16 (so every row starts on a 16-byte
