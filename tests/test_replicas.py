@@ -70,3 +70,28 @@ def test_reference_arm_runs_on_rank_0_only(monkeypatch, capsys):
     args = type("A", (), {"steps": 3, "warmup": 3, "gpus": 2})()
     assert bench.run_reference(args) == 0   # returns at once, without work
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_line_on_rank_0(monkeypatch, capsys):
+    """Rank 0 (or a single process) times the oracle on a bounded sample and
+    prints one JSON line with the keys of the benchmark contract: the
+    reference tag, the metric and unit of the GPU line, a cpu_baseline
+    block describing the run, and an e2e block with no host-device copies."""
+    import json
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle
+    oracle.build()
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    args = type("A", (), {"steps": 1, "warmup": 3, "gpus": 1})()
+    assert bench.run_reference(args) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["unit"] == "GB/s"
+    for key in ("value", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling", "vs_baseline",
+                "dtype", "data", "config"):
+        assert key in line, key
+    assert line["value"] > 0 and line["higher_is_better"] is True and line["config"]["workload"] == "decode_2b"
+    cpu = line["cpu_baseline"]
+    assert cpu["kind"] == "oracle" and cpu["cores"] >= 1 and cpu["value"] == line["value"] and cpu["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
