@@ -1032,16 +1032,18 @@ def profile_format(spec):
 
 
 def profile_fused(spec):
-    """--profile-fused L,M: the fused decode path on an L-layer 2B-shape
-    stack at M tokens, eagerly launched: 3 warm-up + 5 timed passes (driver
-    for ncu captures)."""
+    """--profile-fused L,M[,WORKLOAD]: the fused decode path on an L-layer
+    stack (the 2B shapes, or stack_3b / stack_70b) at M tokens, eagerly
+    launched: 3 warm-up + 5 timed passes (driver for ncu captures)."""
     import torch
     import bitlinear_02_b300 as bl
     from bitlinear_02_b300 import inputs
-    L, M = (int(v) for v in spec.split(","))
+    parts = spec.split(",")
+    L, M = int(parts[0]), int(parts[1])
+    workload = parts[2] if len(parts) > 2 else WORKLOAD
     dev = torch.device("cuda:0")
     bl.load_library()
-    st = Stack(torch, bl, inputs, dev, WORKLOAD, layers=L)
+    st = Stack(torch, bl, inputs, dev, workload, layers=L)
     fr = FusedRunner(st, M)
     stream = torch.cuda.current_stream()
     for _ in range(3):
@@ -1055,7 +1057,7 @@ def profile_fused(spec):
     e1.synchronize()
     ms = e0.elapsed_time(e1) / 5
     assert bl.bitlinear_check_status() == bl.OK
-    print(json.dumps({"profile": "fused", "layers": L, "M": M, "ms_per_pass": round(ms, 4),
+    print(json.dumps({"profile": "fused", "workload": workload, "layers": L, "M": M, "ms_per_pass": round(ms, 4),
                       "launches_per_pass": fr.launches}))
     return 0
 
@@ -1072,7 +1074,7 @@ def main():
     ap.add_argument("--no-sweeps", action="store_true", help="skip the per-shape and mid-M sweeps")
     ap.add_argument("--profile-gemm", default=None, help="N,K,M[,int8]: time one GEMM shape (ncu driver)")
     ap.add_argument("--profile-gemv", default=None, help="N,K,M[,copies]: time the decode GEMV (ncu driver)")
-    ap.add_argument("--profile-fused", default=None, help="L,M: time the fused decode path (ncu driver)")
+    ap.add_argument("--profile-fused", default=None, help="L,M[,WORKLOAD]: time the fused decode path (ncu driver)")
     ap.add_argument("--profile-format", default=None,
                     help="FMT,N,K,M[,copies]: time one weight format's decode engine (ncu driver)")
     args = ap.parse_args()
